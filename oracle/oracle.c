@@ -97,9 +97,11 @@ void orc_allreduce(int dtype, int A, const void* const* x, int64_t i0, int64_t i
       if (refq) ((int32_t*)refq)[o] = (int32_t)acc;
       continue;
     }
-    double acc64 = 0.0;
-    float acc32 = 0.0f;
-    for (int k = 0; k < A; ++k) {
+    /* the sums start from their first term, as IEEE addition of the terms would
+     * (a sum of negative zeros stays -0) */
+    double acc64 = (double)load_f(dtype, x[0], i);
+    float acc32 = load_f(dtype, x[0], i);
+    for (int k = 1; k < A; ++k) {
       float v = load_f(dtype, x[k], i);
       acc64 += (double)v;
       acc32 = acc32 + v;
@@ -140,20 +142,21 @@ void orc_reduce_scatter(int dtype, int A, const void* const* x, int64_t m, int o
       if (refq) ((int32_t*)refq)[o] = (int32_t)acc;
       continue;
     }
-    double acc64 = 0.0;
-    for (int k = 0; k < A; ++k) acc64 += (double)load_f(dtype, x[k], p);
+    double acc64 = (double)load_f(dtype, x[0], p);
+    for (int k = 1; k < A; ++k) acc64 += (double)load_f(dtype, x[k], p);
     float acc32;
     if (i < helper_span) {
-      float partial = 0.0f;
-      for (int s = 0; s < A; ++s) {
+      int first = owner == 0 ? 1 : 0;
+      float partial = load_f(dtype, x[first], p);
+      for (int s = first + 1; s < A; ++s) {
         if (s == owner) continue;
         partial = partial + load_f(dtype, x[s], p);
       }
       partial = quantize(dtype, partial);
       acc32 = load_f(dtype, x[owner], p) + partial;
     } else {
-      acc32 = 0.0f;
-      for (int s = 0; s < A; ++s) acc32 = acc32 + load_f(dtype, x[s], p);
+      acc32 = load_f(dtype, x[0], p);
+      for (int s = 1; s < A; ++s) acc32 = acc32 + load_f(dtype, x[s], p);
     }
     float r32 = acc32 * scale;
     if (ref64) ref64[o] = acc64 * (double)scale;

@@ -90,6 +90,17 @@ def test_allreduce_matches_library_sum(orc, A, dtype):
     assert np.array_equal(rq, lib_q)
 
 
+def test_sum_of_negative_zeros_stays_negative(orc):
+    # IEEE: -0 + -0 = -0 (round to nearest); a sum seeded with +0 would lose the sign
+    nz = [np.array([-0.0, 0.0, -0.0], np.float32) for _ in range(3)]
+    nz[1][2] = 0.0
+    _, r32, _ = orc.allreduce(0, nz, 1.0)
+    assert np.signbit(r32).tolist() == [True, False, False]
+    blocks = [np.full(4, -0.0, np.float32) for _ in range(4)]   # A blocks of m = 1
+    _, r32, _ = orc.reduce_scatter(0, blocks, 1, 2, 1.0, 1)
+    assert np.signbit(r32).tolist() == [True]
+
+
 def test_allreduce_window_and_int_wrap(orc):
     big = np.array([2 ** 31 - 1, -2 ** 31, 5], np.int32)
     one = np.array([1, -1, 7], np.int32)
