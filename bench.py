@@ -1,0 +1,321 @@
+"""Relay-pass HBM throughput of the sharded relay collectives on GB300.
+
+Default workload: allreduce with A=2 active ranks of R=8 (6 helpers), bf16 payload
+with fp32 accumulation, scale 1/2 (AVG), 1 GiB per rank (2^29 elements), on the
+relay schedule the planner picks at that size (numChunks = H+2 = 8, reduce at the
+helpers). One step is one relay_allreduce call: every pass of the schedule.
+
+`value` = algorithmic bytes (read + written, summed over the schedule's passes, as
+`relay_plan_passes` reports them) of all steps on all GPUs / the slowest rank's time.
+Inputs are 1 GiB per rank, far above the 126 MiB L2, so no flush is needed between
+steps. `e2e` is the same metric through the same public call with the inputs copied
+in from pinned host memory and the outputs copied back inside the timed region.
+
+`python bench.py [--gpus N --steps K --warmup W] [--impl reference]`. Under
+torchrun each rank runs an independent replica (the path has no cross-GPU step).
+`--impl reference` times the CPU oracle (the plain C restatement of the collective's
+result) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+A, R = 2, 8
+COUNT = 1 << 29              # elements per rank (bf16: 1 GiB)
+SCALE = 0.5
+WORKLOAD = "allreduce A=2 of R=8, bf16 (fp32 accumulate), 1 GiB per rank, scale 1/2"
+CPU_SAMPLE = 1 << 24         # elements per rank in one oracle sample
+PROFILE = os.path.join(ROOT, "profiles", "relay_pass_kernel_allreduce_a2_bf16_1g.md")
+KERNEL_SRC = os.path.join(ROOT, "pack_virtual_rank_gb300", "csrc", "passes.cu")
+
+
+def _dist():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _profiled_traffic():
+    """Per-launch DRAM bytes of the dominant pass from the committed ncu summary, or
+    None when the kernel source changed since the counters were taken."""
+    try:
+        text = open(PROFILE).read()
+    except OSError:
+        return None, None
+    sha = hashlib.sha256(open(KERNEL_SRC, "rb").read()).hexdigest()[:16]
+    m_sha = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    out = {}
+    for m in re.finditer(r"traffic_bytes_per_launch\[(\w+)\]:\s*([0-9]+)", text):
+        out[m.group(1)] = int(m.group(2))
+    if not m_sha or m_sha.group(1) != sha:
+        return None, sha
+    return out, sha
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None:
+            return None
+        self.out.seek(0)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.out.read().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        os.unlink(self.out.name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def _cpu_oracle(sample: int, seed_config: int = 2):
+    """Time the oracle's allreduce on `sample` elements per rank (host cores)."""
+    import oracle as orc
+    import synth
+    xs = [synth.to_numpy(synth.rank_input(seed_config, r, sample, "bf16")) for r in range(A)]
+    t0 = time.perf_counter()
+    orc.allreduce(orc.BF16, xs, SCALE)
+    return time.perf_counter() - t0
+
+
+def _bytes_per_step(plan, rv, count=None):
+    if count is not None and count != plan.count:
+        plan = rv.relay_plan(rv.ALLREDUCE, count, rv.BF16, A, R)
+    ps = rv.relay_plan_passes(plan)
+    return sum(p["bytes_read"] + p["bytes_written"] for p in ps), ps
+
+
+def run_reference(args):
+    rank, world, _ = _dist()
+    if rank != 0:
+        return 0
+    import pack_virtual_rank_gb300.build as b
+    b.build()
+    import pack_virtual_rank_gb300 as rv
+    import oracle
+    oracle.build()
+    plan = rv.relay_plan(rv.ALLREDUCE, CPU_SAMPLE, rv.BF16, A, R)
+    nbytes, _ = _bytes_per_step(plan, rv)
+    for _ in range(args.warmup):
+        _cpu_oracle(CPU_SAMPLE)
+    ts = [_cpu_oracle(CPU_SAMPLE) for _ in range(args.steps)]
+    total = sum(ts)
+    value = nbytes * args.steps / total / 1e9
+    sample = (f"oracle allreduce (bf16, A=2, fp32 sum, scale 1/2) on {CPU_SAMPLE} elements per "
+              f"rank per step; GB/s counts the relay schedule's algorithmic bytes for that count")
+    line = {"impl": "reference", "metric": "relay-pass HBM GB/s (allreduce A=2 of R=8, bf16)",
+            "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) bf16)",
+            "config": {"workload": WORKLOAD, "sample_count": CPU_SAMPLE, "A": A, "R": R},
+            "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": 1,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def run_ours(args):
+    rank, world, local = _dist()
+    import torch
+    import torch.distributed as dist
+    if world > 1:
+        dist.init_process_group("gloo")
+    import pack_virtual_rank_gb300.build as b
+    if rank == 0 or world == 1:
+        b.build()
+    if world > 1:
+        dist.barrier()
+    import pack_virtual_rank_gb300 as rv
+    import synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    plan = rv.relay_plan(rv.ALLREDUCE, COUNT, rv.BF16, A, R)
+    nbytes, passes = _bytes_per_step(plan, rv)
+    npass = len(passes)
+    launches_per_step = sum((p["num_segments"] + 383) // 384 for p in passes)
+
+    xs = [synth.rank_input(2, r, COUNT, "bf16", device=dev) for r in range(A)]
+    ys = [torch.empty_like(x) for x in xs]
+    scratch = rv.alloc_scratch(plan, dev)
+    send = xs + [None] * (R - A)
+    recv = ys + [None] * (R - A)
+
+    def barrier():
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        rv.relay_allreduce(send, recv, scratch, COUNT, rv.BF16, A, R, SCALE)
+    # per-pass events of every timed step
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(npass + 1)]
+          for _ in range(args.steps)]
+    opts = [rv.make_opts(pass_events=e) for e in ev]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    with Clocks(local) as clk:
+        barrier()
+        start.record(stream)
+        for k in range(args.steps):
+            rv.relay_allreduce(send, recv, scratch, COUNT, rv.BF16, A, R, SCALE, opts[k])
+        stop.record(stream)
+        barrier()
+    ms = start.elapsed_time(stop)
+    clocks = clk.summary()
+    per_pass = [statistics.mean(ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(args.steps))
+                for i in range(npass)]
+
+    # end to end: pinned host inputs in, results out, through the same call
+    hx = [x.cpu().pin_memory() for x in xs]
+    hy = [torch.empty(COUNT, dtype=torch.bfloat16).pin_memory() for _ in range(A)]
+    e2e_steps = max(1, min(args.steps, 5))
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        for a in range(A):
+            xs[a].copy_(hx[a], non_blocking=True)
+        rv.relay_allreduce(send, recv, scratch, COUNT, rv.BF16, A, R, SCALE)
+        for a in range(A):
+            hy[a].copy_(ys[a], non_blocking=True)
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1)
+
+    if world > 1:
+        t = torch.tensor([ms, e2e_ms], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, e2e_ms = float(t[0]), float(t[1])
+
+    if rank == 0:
+        peak, peak_kind = _peaks()
+        value = nbytes * args.steps * world / (ms / 1e3) / 1e9
+        e2e = nbytes * e2e_steps * world / (e2e_ms / 1e3) / 1e9
+        top = max(range(npass), key=lambda i: per_pass[i])
+        top_bytes = passes[top]["bytes_read"] + passes[top]["bytes_written"]
+        achieved = top_bytes / (per_pass[top] / 1e3) / 1e9
+        traffic, _sha = _profiled_traffic()
+        tr = traffic.get(passes[top]["name"]) if traffic else None
+        cpu_t = _cpu_oracle(CPU_SAMPLE)
+        cpu_bytes, _ = _bytes_per_step(plan, rv, CPU_SAMPLE)
+        cpu_val = cpu_bytes / cpu_t / 1e9
+        line = {
+            "metric": "relay-pass HBM GB/s (allreduce A=2 of R=8, bf16)",
+            "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) bf16, generated on the device)",
+            "config": {"workload": WORKLOAD, "count": COUNT, "A": A, "R": R,
+                       "schedule": ["relay", "zero_chunk", "direct", "legacy"][plan.kind],
+                       "numChunks": plan.H + 2, "chunk": plan.chunk,
+                       "l2": "inputs larger than L2 (1 GiB per rank); no flush",
+                       "bytes_per_step": nbytes, "parallelism": f"replicas x{world}"},
+            "passes": {p["name"]: {"ms": round(t, 4), "bytes": p["bytes_read"] + p["bytes_written"],
+                                   "gbs": round((p["bytes_read"] + p["bytes_written"]) / t / 1e6, 1),
+                                   "frac": round((p["bytes_read"] + p["bytes_written"]) / t / 1e6
+                                                 / peak, 4)}
+                       for p, t in zip(passes, per_pass)},
+            "roofline": {"kernel": f"relay_pass_kernel ({passes[top]['name']})", "bound": "hbm",
+                         "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": tr,
+                         "peak_source": f"{peak_kind} hbm_gbs (copy, burst)",
+                         "algorithmic_bytes_per_launch": top_bytes},
+            "cpu_baseline": {"value": round(cpu_val, 3), "unit": "GB/s", "cores": 1,
+                             "kind": "oracle",
+                             "sample": f"oracle allreduce on {CPU_SAMPLE} elements per rank "
+                                       f"({cpu_t:.2f} s); GB/s counts the relay schedule's "
+                                       "algorithmic bytes for that count"},
+            "e2e": {"value": round(e2e, 2), "unit": "GB/s",
+                    "h2d_bytes_per_step": A * COUNT * 2, "d2h_bytes_per_step": A * COUNT * 2},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)   # at least 3 untimed steps before timing
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,336 @@
+// abi.cpp -- the extern "C" entry points declared in relay.h: validation, planning,
+// the link-byte accountant, and the pass-by-pass execution of a collective.
+//
+// Page: "Link-balance the sharded relay schedules (up to 3.2x vs NCCL)" (torchrec pull
+// request #4570): "item k" of its summary, "Dnnnnnnnnn" a commit of its stack.
+#include <stdint.h>
+#include <string.h>
+
+#include <algorithm>
+#include <string>
+#include <vector>
+
+#include "program.h"
+
+namespace relay {
+namespace {
+
+thread_local std::string g_last_error;
+
+relay_status_t fail(relay_status_t st, const std::string& msg) {
+  g_last_error = msg;
+  return st;
+}
+
+// Fake, widely spaced, 256-byte aligned buffer addresses: enough to build a program
+// whose segment lengths and ranks can be counted without touching memory.
+struct FakeBuffers {
+  std::vector<void*> send, recv, scratch;
+  FakeBuffers(const relay_plan_t& p, bool in_place) {
+    send.resize(p.R);
+    recv.resize(p.R);
+    scratch.resize(p.R);
+    for (int r = 0; r < p.R; ++r) {
+      auto base = [&](int k) { return reinterpret_cast<void*>((uintptr_t)(4 * r + k + 1) << 42); };
+      send[r] = base(0);
+      recv[r] = base(1);
+      scratch[r] = base(2);
+      if (in_place && r < p.A) {
+        const int64_t E = p.esize;
+        switch (p.coll) {
+          case RELAY_ALLREDUCE: recv[r] = send[r]; break;
+          case RELAY_REDUCE_SCATTER: recv[r] = (char*)send[r] + r * p.count * E; break;
+          case RELAY_ALL_GATHER: send[r] = (char*)recv[r] + r * p.count * E; break;
+          default: break;
+        }
+      }
+    }
+  }
+  Buffers view() const { return Buffers{send.data(), recv.data(), scratch.data()}; }
+};
+
+struct Range {
+  uintptr_t lo, hi;  // [lo, hi)
+  std::string what;
+};
+
+bool overlaps(const Range& a, const Range& b) { return a.lo < b.hi && b.lo < a.hi; }
+
+// Two segments of one launch must not write what the other reads or writes: nothing
+// orders CTAs within a launch.
+bool find_hazard(const Pass& pass, int E, std::string* why) {
+  const auto& s = pass.segs;
+  auto rng = [&](const void* p, int64_t n) {
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+    return Range{lo, lo + (uintptr_t)(n * E), ""};
+  };
+  for (size_t i = 0; i < s.size(); ++i)
+    for (int d = 0; d < s[i].ndst; ++d) {
+      const Range w = rng(s[i].dst[d], s[i].n);
+      for (size_t j = 0; j < s.size(); ++j) {
+        if (j == i) continue;
+        for (int k = 0; k < s[j].nsrc; ++k)
+          if (overlaps(w, rng(s[j].src[k], s[j].n))) {
+            *why = "segment " + std::to_string(i) + " writes what segment " + std::to_string(j) +
+                   " reads in pass " + relay_pass_name(pass.kind);
+            return true;
+          }
+        for (int k = 0; k < s[j].ndst; ++k)
+          if (overlaps(w, rng(s[j].dst[k], s[j].n))) {
+            *why = "segments " + std::to_string(i) + " and " + std::to_string(j) +
+                   " write the same bytes in pass " + relay_pass_name(pass.kind);
+            return true;
+          }
+      }
+    }
+  return false;
+}
+
+// Every range a segment reads or writes must lie inside one declared buffer.
+bool find_out_of_bounds(const Pass& pass, int E, const std::vector<Range>& bufs,
+                        std::string* why) {
+  auto inside = [&](const void* p, int64_t n) {
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(p), hi = lo + (uintptr_t)(n * E);
+    for (const Range& b : bufs)
+      if (lo >= b.lo && hi <= b.hi) return true;
+    return false;
+  };
+  for (size_t i = 0; i < pass.segs.size(); ++i) {
+    const Seg& s = pass.segs[i];
+    bool ok = true;
+    for (int k = 0; k < s.nsrc; ++k) ok &= inside(s.src[k], s.n);
+    for (int d = 0; d < s.ndst; ++d) ok &= inside(s.dst[d], s.n);
+    if (!ok) {
+      *why = "segment " + std::to_string(i) + " of pass " + relay_pass_name(pass.kind) +
+             " leaves the declared buffers";
+      return true;
+    }
+  }
+  return false;
+}
+
+relay_status_t run_collective(relay_coll_t coll, void* const* send, void* const* recv,
+                              void* const* scratch, size_t count, relay_dtype_t dtype, int A,
+                              int R, float scale, const relay_opts_t* opts, cudaStream_t stream) {
+  if (count > (size_t)INT64_MAX) return fail(RELAY_ERR_INVALID_ARGUMENT, "count too large");
+  relay_plan_t p;
+  std::string why;
+  relay_status_t st = make_plan(coll, (int64_t)count, dtype, A, R, opts, &p, &why);
+  if (st != RELAY_OK) return fail(st, why);
+  const bool reduces = coll == RELAY_ALLREDUCE || coll == RELAY_REDUCE_SCATTER;
+  // D115998376: SUM (scale 1) and AVG (scale 1/A) only; an integer average is not
+  // defined on the page, so int32 takes scale 1 only
+  if (reduces && dtype == RELAY_I32 && scale != 1.0f)
+    return fail(RELAY_ERR_INVALID_ARGUMENT, "int32 reductions take scale == 1 only");
+  if (p.count == 0) return RELAY_OK;
+  if (send == nullptr || recv == nullptr || scratch == nullptr)
+    return fail(RELAY_ERR_INVALID_ARGUMENT, "pointer arrays must not be NULL");
+
+  const int64_t E = p.esize;
+  std::vector<Range> ranges;
+  auto add = [&](const void* ptr, int64_t elems, const std::string& what) -> bool {
+    if (ptr == nullptr) return false;
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(ptr);
+    ranges.push_back(Range{lo, lo + (uintptr_t)(elems * E), what});
+    return true;
+  };
+  for (int a = 0; a < A; ++a) {
+    const std::string ra = std::to_string(a);
+    if (send[a] == nullptr || recv[a] == nullptr)
+      return fail(RELAY_ERR_INVALID_ARGUMENT, "active " + ra + ": send/recv is NULL");
+    if ((reinterpret_cast<uintptr_t>(send[a]) | reinterpret_cast<uintptr_t>(recv[a])) % E)
+      return fail(RELAY_ERR_INVALID_ARGUMENT, "active " + ra + ": buffer not element-aligned");
+    const char* s = static_cast<const char*>(send[a]);
+    const char* r = static_cast<const char*>(recv[a]);
+    bool send_in_recv = false, recv_in_send = false;
+    switch (coll) {
+      case RELAY_ALLREDUCE: recv_in_send = r == s; break;                                // D115998369
+      case RELAY_REDUCE_SCATTER: recv_in_send = r == s + a * p.count * E; break;        // D115998376
+      case RELAY_ALL_GATHER: send_in_recv = s == r + a * p.count * E; break;            // D115998385
+      default: break;                                                                     // D115998370
+    }
+    if (!send_in_recv) add(send[a], p.input_elems, "send[" + ra + "]");
+    if (!recv_in_send) add(recv[a], p.output_elems, "recv[" + ra + "]");
+    if (p.active_scratch_elems > 0) {
+      if (scratch[a] == nullptr)
+        return fail(RELAY_ERR_INVALID_ARGUMENT, "active " + ra + " needs scratch");
+      if (reinterpret_cast<uintptr_t>(scratch[a]) % E)
+        return fail(RELAY_ERR_INVALID_ARGUMENT, "scratch[" + ra + "] not element-aligned");
+      add(scratch[a], p.active_scratch_elems, "scratch[" + ra + "]");
+    }
+  }
+  if (p.helper_elems > 0)
+    for (int h = 0; h < p.H; ++h) {
+      const std::string rh = std::to_string(A + h);
+      if (scratch[A + h] == nullptr)
+        return fail(RELAY_ERR_INVALID_ARGUMENT, "helper rank " + rh + " needs scratch");
+      if (reinterpret_cast<uintptr_t>(scratch[A + h]) % E)
+        return fail(RELAY_ERR_INVALID_ARGUMENT, "scratch[" + rh + "] not element-aligned");
+      add(scratch[A + h], p.helper_elems, "scratch[" + rh + "]");
+    }
+  for (size_t i = 0; i < ranges.size(); ++i)
+    for (size_t j = i + 1; j < ranges.size(); ++j)
+      if (overlaps(ranges[i], ranges[j]))
+        return fail(RELAY_ERR_INVALID_ARGUMENT,
+                    ranges[i].what + " overlaps " + ranges[j].what + " (not an in-place form)");
+
+  std::vector<Pass> passes;
+  build_program(p, Buffers{send, recv, scratch}, false, &passes);
+
+  const int flags = opts ? opts->flags : 0;
+  if (flags & RELAY_FLAG_CHECK_HAZARDS)
+    for (const Pass& ps : passes) {
+      if (find_out_of_bounds(ps, (int)E, ranges, &why) || find_hazard(ps, (int)E, &why))
+        return fail(RELAY_ERR_UNSUPPORTED, "internal: " + why);
+    }
+  if (flags & RELAY_FLAG_DRY_RUN) return RELAY_OK;
+
+  cudaEvent_t* events = nullptr;
+  if (opts && opts->pass_events) {
+    if (opts->n_pass_events < (int)passes.size() + 1)
+      return fail(RELAY_ERR_INVALID_ARGUMENT, "pass_events holds fewer than passes + 1 events");
+    events = static_cast<cudaEvent_t*>(opts->pass_events);
+  }
+  for (size_t i = 0; i < passes.size(); ++i) {
+    if (events && cudaEventRecord(events[i], stream) != cudaSuccess)
+      return fail(RELAY_ERR_CUDA, "cudaEventRecord failed");
+    const cudaError_t e = launch_pass(dtype, passes[i], scale, stream);
+    if (e != cudaSuccess) return fail(RELAY_ERR_CUDA, cudaGetErrorString(e));
+  }
+  if (events && cudaEventRecord(events[passes.size()], stream) != cudaSuccess)
+    return fail(RELAY_ERR_CUDA, "cudaEventRecord failed");
+  return RELAY_OK;
+}
+
+}  // namespace
+}  // namespace relay
+
+using namespace relay;
+
+extern "C" {
+
+void relay_opts_init(relay_opts_t* o) {
+  if (!o) return;
+  memset(o, 0, sizeof *o);
+  o->offload_permille = -1;
+  o->schedule = RELAY_SCHEDULE_AUTO;
+  o->relay_threshold_bytes = -1;
+}
+
+int relay_abi_version(void) { return RELAY_ABI_VERSION; }
+
+const char* relay_last_error(void) { return g_last_error.c_str(); }
+
+relay_status_t relay_plan(relay_coll_t coll, size_t count, relay_dtype_t dtype, int A, int R,
+                          const relay_opts_t* opts, relay_plan_t* out) {
+  if (count > (size_t)INT64_MAX) return fail(RELAY_ERR_INVALID_ARGUMENT, "count too large");
+  std::string why;
+  const relay_status_t st = make_plan(coll, (int64_t)count, dtype, A, R, opts, out, &why);
+  if (st != RELAY_OK) return fail(st, why);
+  return RELAY_OK;
+}
+
+relay_status_t relay_plan_link_bytes(const relay_plan_t* plan, uint64_t* out, size_t cap) {
+  if (!plan || !out) return fail(RELAY_ERR_INVALID_ARGUMENT, "NULL argument");
+  const int R = plan->R, G = plan->num_groups;
+  if (R <= 0 || R > RELAY_MAX_RANKS || G < 0 || G > 3)
+    return fail(RELAY_ERR_INVALID_ARGUMENT, "not a plan");
+  const size_t need = (size_t)G * R * R;
+  if (cap < need) return fail(RELAY_ERR_INVALID_ARGUMENT, "link table too small");
+  std::fill(out, out + need, 0);
+  FakeBuffers fb(*plan, false);
+  std::vector<Pass> passes;
+  build_program(*plan, fb.view(), false, &passes);
+  for (const Pass& ps : passes)
+    for (size_t i = 0; i < ps.segs.size(); ++i) {
+      const SegMeta& m = ps.meta[i];
+      if (m.group < 0) continue;
+      if (m.group >= G) return fail(RELAY_ERR_INVALID_ARGUMENT, "internal: group out of range");
+      for (int d = 0; d < ps.segs[i].ndst; ++d)
+        if (m.dst_rank[d] != m.exec_rank)
+          out[((size_t)m.group * R + m.exec_rank) * R + m.dst_rank[d]] +=
+              (uint64_t)ps.segs[i].n * plan->esize;
+    }
+  return RELAY_OK;
+}
+
+uint64_t relay_plan_cost_bytes(const relay_plan_t* plan) {
+  if (!plan || plan->R <= 0 || plan->R > RELAY_MAX_RANKS || plan->num_groups > 3) return 0;
+  std::vector<uint64_t> t((size_t)std::max(plan->num_groups, 1) * plan->R * plan->R);
+  if (relay_plan_link_bytes(plan, t.data(), t.size()) != RELAY_OK) return 0;
+  uint64_t total = 0;
+  const size_t per = (size_t)plan->R * plan->R;
+  for (int g = 0; g < plan->num_groups; ++g)
+    total += *std::max_element(t.begin() + g * per, t.begin() + (g + 1) * per);
+  return total;
+}
+
+int relay_plan_passes(const relay_plan_t* plan, int in_place, relay_pass_info_t* out, int cap) {
+  if (!plan || plan->R <= 0 || plan->R > RELAY_MAX_RANKS) return -1;
+  FakeBuffers fb(*plan, in_place != 0);
+  std::vector<Pass> passes;
+  build_program(*plan, fb.view(), in_place != 0, &passes);
+  for (size_t i = 0; i < passes.size() && (int)i < cap && out; ++i) {
+    relay_pass_info_t& q = out[i];
+    q.kind = passes[i].kind;
+    q.num_segments = (int32_t)passes[i].segs.size();
+    q.bytes_read = q.bytes_written = 0;
+    for (const Seg& s : passes[i].segs) {
+      q.bytes_read += s.n * plan->esize * s.nsrc;
+      q.bytes_written += s.n * plan->esize * s.ndst;
+    }
+  }
+  return (int)passes.size();
+}
+
+const char* relay_pass_name(int kind) {
+  switch (kind) {
+    case RELAY_PASS_G1: return "group1";
+    case RELAY_PASS_G2: return "group2";
+    case RELAY_PASS_G3: return "group3";
+    case RELAY_PASS_ACTIVE_REDUCE: return "active_reduce";
+    case RELAY_PASS_PACK: return "pack";
+    case RELAY_PASS_HELPER_FORWARD: return "helper_forward";
+    case RELAY_PASS_UNPACK: return "unpack";
+    default: return "unknown";
+  }
+}
+
+// D115998394, D115998388, D115998370: A slots, each a whole number of 128-element
+// chunks, never more than the group count itself
+int64_t relay_passthrough_helper_size(int64_t count_g, int A, int num_chunks) {
+  if (count_g < 0 || A <= 0 || num_chunks <= 0) return -1;
+  const int64_t chunk = (count_g / num_chunks) / RELAY_ALIGN_ELEMS * RELAY_ALIGN_ELEMS;
+  if (chunk == 0) return count_g;
+  return std::min<int64_t>(count_g, (int64_t)A * chunk);
+}
+
+relay_status_t relay_allreduce(void* const* send, void* const* recv, void* const* scratch,
+                               size_t count, relay_dtype_t dtype, int A, int R, float scale,
+                               const relay_opts_t* opts, cudaStream_t stream) {
+  return run_collective(RELAY_ALLREDUCE, send, recv, scratch, count, dtype, A, R, scale, opts,
+                        stream);
+}
+
+relay_status_t relay_reduce_scatter(void* const* send, void* const* recv, void* const* scratch,
+                                    size_t recv_count, relay_dtype_t dtype, int A, int R,
+                                    float scale, const relay_opts_t* opts, cudaStream_t stream) {
+  return run_collective(RELAY_REDUCE_SCATTER, send, recv, scratch, recv_count, dtype, A, R, scale,
+                        opts, stream);
+}
+
+relay_status_t relay_all_gather(void* const* send, void* const* recv, void* const* scratch,
+                                size_t send_count, relay_dtype_t dtype, int A, int R,
+                                const relay_opts_t* opts, cudaStream_t stream) {
+  return run_collective(RELAY_ALL_GATHER, send, recv, scratch, send_count, dtype, A, R, 1.0f, opts,
+                        stream);
+}
+
+relay_status_t relay_all_to_all(void* const* send, void* const* recv, void* const* scratch,
+                                size_t segment_count, relay_dtype_t dtype, int A, int R,
+                                const relay_opts_t* opts, cudaStream_t stream) {
+  return run_collective(RELAY_ALL_TO_ALL, send, recv, scratch, segment_count, dtype, A, R, 1.0f,
+                        opts, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,393 @@
+// passes.cu -- the one streaming kernel behind every relay pass (sm_103a).
+//
+// A pass is a table of segments (program.h) executed by one launch. Each segment is
+// cut into tiles of 16 KiB of payload; the grid is persistent (a multiple of the SM
+// count) and walks the tiles of the whole table, so one launch covers every transfer
+// and reduction of a schedule group regardless of how many there are (the page
+// "Link-balance the sharded relay schedules (up to 3.2x vs NCCL)", item 5, blames the
+// per-op launch overhead of many small groups; here a group costs one launch).
+//
+// Per tile a CTA of 256 threads issues all its 16-byte loads first (4 per thread per
+// source), then reduces in fp32 (int32: wrapping uint32) in ascending source order,
+// scales once, rounds to nearest-even into the payload type and stores the result to
+// each destination. Copies move raw 16-byte vectors. Segments whose pointers are not
+// 16-byte aligned (after a host-side prologue split) take a per-element path.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <algorithm>
+
+#include "program.h"
+
+namespace relay {
+namespace {
+
+template <int CAP>
+struct PassArgs {
+  int32_t nseg;
+  int32_t ntiles;
+  float scale;
+  int32_t pad;
+  Seg seg[CAP];
+};
+
+// ---------------------------------------------------------------- memory access --
+
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(p));
+  return r;
+}
+__device__ __forceinline__ void st_v4(void* p, uint4 v) {
+  asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ uint32_t ld_u32(const void* p) {
+  uint32_t r;
+  asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(r) : "l"(p));
+  return r;
+}
+__device__ __forceinline__ uint16_t ld_u16(const void* p) {
+  uint16_t r;
+  asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(r) : "l"(p));
+  return r;
+}
+__device__ __forceinline__ void st_u32(void* p, uint32_t v) {
+  asm volatile("st.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_u16(void* p, uint16_t v) {
+  asm volatile("st.global.u16 [%0], %1;" ::"l"(p), "h"(v) : "memory");
+}
+
+// ------------------------------------------------------------- payload traits --
+// bf16 is the upper half of a binary32, so widening is a shift; narrowing rounds to
+// nearest-even in one cvt instruction (two lanes at a time).
+
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+struct TF32 {
+  static constexpr int kE = 4, kLanes = 4;
+  using Acc = float;
+  static __device__ __forceinline__ void unpack(uint4 v, float* a) {
+    a[0] = __uint_as_float(v.x); a[1] = __uint_as_float(v.y);
+    a[2] = __uint_as_float(v.z); a[3] = __uint_as_float(v.w);
+  }
+  static __device__ __forceinline__ uint4 pack(const float* a) {
+    return make_uint4(__float_as_uint(a[0]), __float_as_uint(a[1]), __float_as_uint(a[2]),
+                      __float_as_uint(a[3]));
+  }
+  static __device__ __forceinline__ float add(float x, float y) { return __fadd_rn(x, y); }
+  static __device__ __forceinline__ float scale(float x, float s) { return __fmul_rn(x, s); }
+  static __device__ __forceinline__ float load1(const void* p) { return __uint_as_float(ld_u32(p)); }
+  static __device__ __forceinline__ void store1(void* p, float v) { st_u32(p, __float_as_uint(v)); }
+};
+
+struct TBF16 {
+  static constexpr int kE = 2, kLanes = 8;
+  using Acc = float;
+  static __device__ __forceinline__ void unpack(uint4 v, float* a) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      a[2 * i] = __uint_as_float(w[i] << 16);
+      a[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+  }
+  static __device__ __forceinline__ uint4 pack(const float* a) {
+    return make_uint4(bf16x2_rn(a[0], a[1]), bf16x2_rn(a[2], a[3]), bf16x2_rn(a[4], a[5]),
+                      bf16x2_rn(a[6], a[7]));
+  }
+  static __device__ __forceinline__ float add(float x, float y) { return __fadd_rn(x, y); }
+  static __device__ __forceinline__ float scale(float x, float s) { return __fmul_rn(x, s); }
+  static __device__ __forceinline__ float load1(const void* p) {
+    return __uint_as_float((uint32_t)ld_u16(p) << 16);
+  }
+  static __device__ __forceinline__ void store1(void* p, float v) {
+    st_u16(p, (uint16_t)(bf16x2_rn(v, 0.0f) & 0xffffu));
+  }
+};
+
+struct TI32 {
+  static constexpr int kE = 4, kLanes = 4;
+  using Acc = uint32_t;  // two's-complement sums wrap modulo 2^32
+  static __device__ __forceinline__ void unpack(uint4 v, uint32_t* a) {
+    a[0] = v.x; a[1] = v.y; a[2] = v.z; a[3] = v.w;
+  }
+  static __device__ __forceinline__ uint4 pack(const uint32_t* a) {
+    return make_uint4(a[0], a[1], a[2], a[3]);
+  }
+  static __device__ __forceinline__ uint32_t add(uint32_t x, uint32_t y) { return x + y; }
+  static __device__ __forceinline__ uint32_t scale(uint32_t x, float) { return x; }
+  static __device__ __forceinline__ uint32_t load1(const void* p) { return ld_u32(p); }
+  static __device__ __forceinline__ void store1(void* p, uint32_t v) { st_u32(p, v); }
+};
+
+// ---------------------------------------------------------------- tile bodies --
+
+// Whole tile on the 16-byte vector path: every thread loads kUnroll vectors per
+// source (in batches that keep at most 8 loads in flight per thread), reduces and
+// stores them. base is the tile's first element.
+template <class P, int NSRC>
+__device__ __forceinline__ void reduce_full_tile(const Seg& s, int64_t base, float scale) {
+  constexpr int L = P::kLanes;
+  constexpr int UB = NSRC <= 2 ? kUnroll : kUnroll / 2;
+  using Acc = typename P::Acc;
+  const int64_t v0 = base / L + threadIdx.x;
+  const bool do_scale = (s.flags & kFlagScale) != 0;
+#pragma unroll
+  for (int u0 = 0; u0 < kUnroll; u0 += UB) {
+    uint4 v[NSRC][UB];
+#pragma unroll
+    for (int u = 0; u < UB; ++u)
+#pragma unroll
+      for (int k = 0; k < NSRC; ++k)
+        v[k][u] = ld_stream_v4(static_cast<const uint4*>(s.src[k]) + v0 + (u0 + u) * kThreads);
+#pragma unroll
+    for (int u = 0; u < UB; ++u) {
+      Acc acc[L], t[L];
+      P::unpack(v[0][u], acc);
+#pragma unroll
+      for (int k = 1; k < NSRC; ++k) {
+        P::unpack(v[k][u], t);
+#pragma unroll
+        for (int i = 0; i < L; ++i) acc[i] = P::add(acc[i], t[i]);
+      }
+      if (do_scale) {
+#pragma unroll
+        for (int i = 0; i < L; ++i) acc[i] = P::scale(acc[i], scale);
+      }
+      const uint4 r = P::pack(acc);
+#pragma unroll
+      for (int d = 0; d < kMaxDst; ++d)
+        if (d < s.ndst) st_v4(static_cast<uint4*>(s.dst[d]) + v0 + (u0 + u) * kThreads, r);
+    }
+  }
+}
+
+__device__ __forceinline__ void copy_full_tile(const Seg& s, int64_t vbase) {
+  const int64_t v0 = vbase + threadIdx.x;
+  uint4 v[kUnroll];
+#pragma unroll
+  for (int u = 0; u < kUnroll; ++u)
+    v[u] = ld_stream_v4(static_cast<const uint4*>(s.src[0]) + v0 + u * kThreads);
+#pragma unroll
+  for (int u = 0; u < kUnroll; ++u)
+#pragma unroll
+    for (int d = 0; d < kMaxDst; ++d)
+      if (d < s.ndst) st_v4(static_cast<uint4*>(s.dst[d]) + v0 + u * kThreads, v[u]);
+}
+
+template <class P>
+__device__ __forceinline__ void run_full_tile(const Seg& s, int64_t base, float scale) {
+  if (s.op == kOpCopy) {
+    copy_full_tile(s, base / P::kLanes);
+    return;
+  }
+  switch (s.nsrc) {
+    case 1: reduce_full_tile<P, 1>(s, base, scale); break;
+    case 2: reduce_full_tile<P, 2>(s, base, scale); break;
+    case 3: reduce_full_tile<P, 3>(s, base, scale); break;
+    default: reduce_full_tile<P, 4>(s, base, scale); break;
+  }
+}
+
+// The last, partial tile of a segment and every tile of a segment whose pointers are
+// not 16-byte aligned: one vector (or one element) per source at a time, with the
+// source count read at run time. Rare, so it is kept small rather than fast.
+template <class P>
+__device__ __noinline__ void run_partial_tile(const Seg& s, int64_t base, int64_t len,
+                                              float scale) {
+  using Acc = typename P::Acc;
+  constexpr int L = P::kLanes;
+  const bool do_scale = (s.flags & kFlagScale) != 0;
+  const bool copy = s.op == kOpCopy;
+  int64_t done = 0;
+  if (s.flags & kFlagVector) {
+    const int64_t vb = base / L, nvec = len / L;
+#pragma unroll 1
+    for (int64_t vi = threadIdx.x; vi < nvec; vi += kThreads) {
+      uint4 r = ld_stream_v4(static_cast<const uint4*>(s.src[0]) + vb + vi);
+      if (!copy) {
+        Acc acc[L], t[L];
+        P::unpack(r, acc);
+#pragma unroll 1
+        for (int k = 1; k < s.nsrc; ++k) {
+          P::unpack(ld_stream_v4(static_cast<const uint4*>(s.src[k]) + vb + vi), t);
+#pragma unroll
+          for (int i = 0; i < L; ++i) acc[i] = P::add(acc[i], t[i]);
+        }
+        if (do_scale) {
+#pragma unroll
+          for (int i = 0; i < L; ++i) acc[i] = P::scale(acc[i], scale);
+        }
+        r = P::pack(acc);
+      }
+#pragma unroll 1
+      for (int d = 0; d < s.ndst; ++d) st_v4(static_cast<uint4*>(s.dst[d]) + vb + vi, r);
+    }
+    done = nvec * L;
+  }
+#pragma unroll 1
+  for (int64_t e = done + threadIdx.x; e < len; e += kThreads) {
+    const int64_t off = (base + e) * P::kE;
+    if (copy) {
+      if (P::kE == 4) {
+        const uint32_t x = ld_u32(static_cast<const char*>(s.src[0]) + off);
+#pragma unroll 1
+        for (int d = 0; d < s.ndst; ++d) st_u32(static_cast<char*>(s.dst[d]) + off, x);
+      } else {
+        const uint16_t x = ld_u16(static_cast<const char*>(s.src[0]) + off);
+#pragma unroll 1
+        for (int d = 0; d < s.ndst; ++d) st_u16(static_cast<char*>(s.dst[d]) + off, x);
+      }
+      continue;
+    }
+    Acc acc = P::load1(static_cast<const char*>(s.src[0]) + off);
+#pragma unroll 1
+    for (int k = 1; k < s.nsrc; ++k)
+      acc = P::add(acc, P::load1(static_cast<const char*>(s.src[k]) + off));
+    if (do_scale) acc = P::scale(acc, scale);
+#pragma unroll 1
+    for (int d = 0; d < s.ndst; ++d) P::store1(static_cast<char*>(s.dst[d]) + off, acc);
+  }
+}
+
+template <class P, int CAP>
+__global__ void __launch_bounds__(kThreads) relay_pass_kernel(const __grid_constant__ PassArgs<CAP> args) {
+  constexpr int64_t kTile = kTileBytes / P::kE;
+  for (int t = blockIdx.x; t < args.ntiles; t += gridDim.x) {
+    // last segment whose first tile is <= t (uniform across the CTA)
+    int lo = 0, hi = args.nseg - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (args.seg[mid].tile0 <= t) lo = mid; else hi = mid - 1;
+    }
+    const Seg& s = args.seg[lo];
+    const int64_t base = (int64_t)(t - s.tile0) * kTile;
+    const int64_t len = min(kTile, s.n - base);
+    if ((s.flags & kFlagVector) && len == kTile) run_full_tile<P>(s, base, args.scale);
+    else run_partial_tile<P>(s, base, len, args.scale);
+  }
+}
+
+// ------------------------------------------------------------------- host side --
+
+// Split segments so that as much as possible takes the vector path: when every
+// pointer of a segment sits at the same offset modulo 16 bytes, peel that many bytes
+// off the front as a per-element segment and vectorize the rest.
+void split_for_alignment(const std::vector<Seg>& in, int E, std::vector<Seg>* out) {
+  out->clear();
+  out->reserve(in.size() + 8);
+  for (const Seg& s0 : in) {
+    Seg s = s0;
+    auto mis = [](const void* p) { return (unsigned)(reinterpret_cast<uintptr_t>(p) & 15u); };
+    const unsigned m0 = mis(s.src[0]);
+    bool same = true;
+    for (int k = 0; k < s.nsrc; ++k) same &= mis(s.src[k]) == m0;
+    for (int d = 0; d < s.ndst; ++d) same &= mis(s.dst[d]) == m0;
+    if (!same || m0 % E != 0) {
+      s.flags &= ~kFlagVector;
+      out->push_back(s);
+      continue;
+    }
+    const int64_t head = m0 == 0 ? 0 : std::min<int64_t>((16 - m0) / E, s.n);
+    if (head > 0) {
+      Seg h = s;
+      h.n = head;
+      h.flags &= ~kFlagVector;
+      out->push_back(h);
+      for (int k = 0; k < s.nsrc; ++k) s.src[k] = static_cast<const char*>(s.src[k]) + head * E;
+      for (int d = 0; d < s.ndst; ++d) s.dst[d] = static_cast<char*>(s.dst[d]) + head * E;
+      s.n -= head;
+    }
+    if (s.n > 0) {
+      s.flags |= kFlagVector;
+      out->push_back(s);
+    }
+  }
+}
+
+int sm_count() {
+  static int cached[RELAY_MAX_RANKS] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (dev >= 0 && dev < RELAY_MAX_RANKS && cached[dev] > 0) return cached[dev];
+  int n = 1;
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  if (dev >= 0 && dev < RELAY_MAX_RANKS) cached[dev] = n;
+  return n;
+}
+
+template <class P, int CAP>
+int blocks_per_sm() {
+  static int cached = 0;
+  if (cached == 0) {
+    int nb = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, relay_pass_kernel<P, CAP>, kThreads, 0) !=
+            cudaSuccess ||
+        nb <= 0)
+      nb = 1;
+    cached = nb;
+  }
+  return cached;
+}
+
+template <class P, int CAP>
+cudaError_t launch_cap(const Seg* segs, int nseg, float scale, cudaStream_t stream) {
+  static thread_local PassArgs<CAP> a;  // up to ~30 KiB: keep it off the stack
+  constexpr int64_t kTile = kTileBytes / P::kE;
+  int64_t tiles = 0;
+  for (int i = 0; i < nseg; ++i) {
+    a.seg[i] = segs[i];
+    a.seg[i].tile0 = (int32_t)tiles;
+    tiles += (segs[i].n + kTile - 1) / kTile;
+  }
+  if (tiles > INT32_MAX) return cudaErrorInvalidValue;
+  a.nseg = nseg;
+  a.ntiles = (int32_t)tiles;
+  a.scale = scale;
+  a.pad = 0;
+  const int64_t cap = (int64_t)sm_count() * blocks_per_sm<P, CAP>();
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, cap));
+  relay_pass_kernel<P, CAP><<<grid, kThreads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+template <class P>
+cudaError_t launch_typed(const std::vector<Seg>& segs, float scale, cudaStream_t stream) {
+  constexpr int kMaxCap = 384;  // 16 + 384 * 80 bytes of parameters, under the 32 KiB limit
+  size_t i = 0;
+  while (i < segs.size()) {
+    const int n = (int)std::min<size_t>(segs.size() - i, kMaxCap);
+    cudaError_t e;
+    if (n <= 8) e = launch_cap<P, 8>(segs.data() + i, n, scale, stream);
+    else if (n <= 32) e = launch_cap<P, 32>(segs.data() + i, n, scale, stream);
+    else if (n <= 128) e = launch_cap<P, 128>(segs.data() + i, n, scale, stream);
+    else e = launch_cap<P, kMaxCap>(segs.data() + i, n, scale, stream);
+    if (e != cudaSuccess) return e;
+    i += n;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_pass(int dtype, const Pass& pass, float scale, cudaStream_t stream) {
+  static thread_local std::vector<Seg> segs;
+  split_for_alignment(pass.segs, esize_of(dtype), &segs);
+  if (segs.empty()) return cudaSuccess;
+  switch (dtype) {
+    case RELAY_F32: return launch_typed<TF32>(segs, scale, stream);
+    case RELAY_BF16: return launch_typed<TBF16>(segs, scale, stream);
+    default: return launch_typed<TI32>(segs, scale, stream);
+  }
+}
+
+}  // namespace relay

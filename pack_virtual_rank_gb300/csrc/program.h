@@ -1,0 +1,80 @@
+// program.h -- internal: the relay schedule as a list of kernel passes.
+//
+// A pass is one batched launch over a table of segments. A segment is a contiguous
+// run of n elements that is either copied from one source to up to four
+// destinations, or reduced from up to four sources (summed in ascending order,
+// optionally scaled, rounded to the payload type) and stored to up to four
+// destinations. Every transfer of a schedule group is a segment whose destination
+// belongs to another virtual rank; the host metadata beside each segment records who
+// executes it and where its stores land, which is what the link-byte accountant sums.
+#pragma once
+
+#include <stdint.h>
+
+#include <string>
+#include <vector>
+
+#include "relay.h"
+
+namespace relay {
+
+constexpr int kMaxSrc = 4;
+constexpr int kMaxDst = 4;
+
+enum SegOp : uint8_t { kOpCopy = 0, kOpReduce = 1 };
+enum SegFlag : uint8_t { kFlagScale = 1, kFlagVector = 2 };
+
+// Device-visible segment descriptor (kernel parameter space).
+struct Seg {
+  const void* src[kMaxSrc];
+  void* dst[kMaxDst];
+  int64_t n;      // elements
+  int32_t tile0;  // first tile of this segment within its launch
+  uint8_t op, nsrc, ndst, flags;
+};
+static_assert(sizeof(Seg) == 80, "Seg layout");
+
+// Host-only bookkeeping for one segment.
+struct SegMeta {
+  int8_t group;           // schedule group whose transfer this is; -1: local work only
+  int8_t exec_rank;       // rank whose kernel work this is (owner of the sources)
+  int8_t dst_rank[kMaxDst];
+};
+
+struct Pass {
+  relay_pass_kind_t kind;
+  std::vector<Seg> segs;
+  std::vector<SegMeta> meta;
+};
+
+// Plan (relay_plan_t is the public POD) -- plan.cpp.
+relay_status_t make_plan(relay_coll_t coll, int64_t count, relay_dtype_t dtype, int A, int R,
+                         const relay_opts_t* opts, relay_plan_t* out, std::string* why);
+
+// Buffers of one call: R entries each (helpers' send/recv unused).
+struct Buffers {
+  void* const* send;
+  void* const* recv;
+  void* const* scratch;
+};
+
+// Build the passes of a planned collective -- program.cpp. in_place tells the builder
+// which in-place form the buffers use (it only removes redundant self copies).
+void build_program(const relay_plan_t& p, const Buffers& b, bool in_place,
+                   std::vector<Pass>* out);
+
+// Launch one pass on `stream` -- passes.cu. Splits into several launches when the
+// segment table exceeds one launch's parameter capacity.
+cudaError_t launch_pass(int dtype, const Pass& pass, float scale, cudaStream_t stream);
+
+// Tile size in elements for a payload of esize bytes (shared by host tiling and the
+// kernel).
+constexpr int kThreads = 256;
+constexpr int kVecBytes = 16;
+constexpr int kUnroll = 4;
+constexpr int64_t kTileBytes = (int64_t)kThreads * kUnroll * kVecBytes;  // 16 KiB
+inline int64_t tile_elems(int esize) { return kTileBytes / esize; }
+
+inline int esize_of(int dtype) { return dtype == RELAY_BF16 ? 2 : 4; }
+
+}  // namespace relay

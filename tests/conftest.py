@@ -31,3 +31,18 @@ def orc():
     import oracle
     oracle.lib()
     return oracle
+
+
+@pytest.fixture(scope="session")
+def relay_lib():
+    from pack_virtual_rank_gb300.build import build
+    build()
+    import pack_virtual_rank_gb300 as rv
+    return rv.lib()
+
+
+@pytest.fixture(autouse=True, scope="session")
+def _built_library():
+    """The relay library is built once per session (no-op when up to date)."""
+    from pack_virtual_rank_gb300.build import build
+    build()

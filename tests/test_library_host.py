@@ -1,0 +1,319 @@
+"""Host-side checks of the C-ABI library (no GPU): every declared symbol is exported,
+the planner and the link-byte accountant agree with the oracle's independent
+restatement, pass byte counts follow the schedules' closed forms, and invalid calls
+are rejected before anything is launched.
+
+Page: "Link-balance the sharded relay schedules (up to 3.2x vs NCCL)" -- "item k" of
+its summary, "Dnnnnnnnnn" a commit of its stack.
+"""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import pack_virtual_rank_gb300 as rv
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+GOLDEN = os.path.join(ROOT, "tests", "golden")
+
+
+def test_every_declared_symbol_is_exported(relay_lib):
+    header = open(os.path.join(ROOT, "include", "relay.h")).read()
+    declared = set(re.findall(r"\b(relay_[a-z0-9_]+)\s*\(", header))
+    assert {"relay_plan", "relay_allreduce", "relay_reduce_scatter", "relay_all_gather",
+            "relay_all_to_all"} <= declared
+    for name in sorted(declared):
+        assert hasattr(relay_lib, name), name
+    assert relay_lib.relay_abi_version() == 1
+
+
+def test_struct_sizes_match_header():
+    # the ctypes mirrors must have the C layouts (all fields 4- or 8-byte, no padding)
+    assert ctypes.sizeof(rv.RelayPlan) == 10 * 4 + 15 * 8
+    assert ctypes.sizeof(rv.RelayOpts) == 4 + 4 + 8 + 8 + 4 + 4
+    assert ctypes.sizeof(rv.RelayPassInfo) == 24
+
+
+# ---------------------------------------------------------------- planner parity --
+
+def _grid():
+    counts = [0, 1, 2, 127, 128, 1023, 1024, 1025, 1792, 2047, 4109, 65536, (1 << 20) + 13,
+              5120 * 1024, 50 << 20]
+    for coll in range(4):
+        for A in (2, 4):
+            for R in (A + 1, 8, 12):
+                for dt in (rv.F32, rv.BF16):
+                    for count in counts:
+                        for sched in (0, 1, 2, 3):
+                            if sched == 3 and A == 4:
+                                continue
+                            yield coll, A, R, dt, count, sched
+
+
+@pytest.mark.parametrize("coll", range(4))
+def test_planner_and_accountant_match_oracle(orc, coll):
+    n = 0
+    for c, A, R, dt, count, sched in _grid():
+        if c != coll:
+            continue
+        E = rv.ESIZE[dt]
+        for pm in (500, 780):
+            opts = rv.make_opts(offload_permille=pm, schedule=sched)
+            try:
+                g, gv = orc.plan(coll, A, R, count, E, permille=pm, force=sched)
+            except ValueError:
+                with pytest.raises(rv.RelayError):
+                    rv.relay_plan(coll, count, dt, A, R, opts)
+                continue
+            p = rv.relay_plan(coll, count, dt, A, R, opts)
+            assert (p.kind, p.num_groups, p.chunk) == (g["kind"], g["groups"], g["chunk"])
+            if A == 2:
+                assert (p.dirA_offset, p.dirA_size, p.dirB_size) == (g["dirA_off"], g["dirA"],
+                                                                      g["dirB"])
+            else:
+                assert (p.direct_total, p.direct_g1, p.direct_g2) == (g["pD"], g["d1"], g["d2"])
+                assert (p.owner_slice, p.owner_slice_last) == (g["owner_slice"],
+                                                               g["owner_last"])
+            lib_t = rv.relay_plan_link_bytes(p)
+            orc_t = orc.link_elems(gv).astype(np.uint64) * np.uint64(E)
+            assert lib_t.shape == orc_t.shape and np.array_equal(lib_t, orc_t)
+            assert rv.relay_plan_cost_bytes(p) == orc.cost_elems(gv) * E
+            n += 1
+    assert n > 300
+
+
+def test_reference_workload_geometry():
+    # allreduce, A=2 of R=8, 65536 fp32, relay forced: numChunks = 8, chunk 8192, direct
+    # share d = count/4 = 16384 riding the two groups; cost 0.25*count per link direction
+    p = rv.relay_plan(rv.ALLREDUCE, 65536, rv.F32, 2, 8, rv.make_opts(schedule=rv.SCHEDULE_RELAY))
+    assert (p.chunk, p.dirA_offset, p.dirA_size, p.dirB_size) == (8192, 49152, 8192, 8192)
+    assert p.dirA_size + p.dirB_size == 65536 // 4
+    t = rv.relay_plan_link_bytes(p)
+    assert t[:, 0, 1].sum() == t[:, 1, 0].sum() == 65536 // 4 * 4
+    assert rv.relay_plan_cost_bytes(p) == 65536 // 4 * 4
+    for g in range(2):   # every used link carries exactly one chunk per direction
+        nz = t[g][t[g] > 0]
+        assert np.all(nz == 8192 * 4)
+
+
+# ---------------------------------------------------------- pass byte closed forms --
+
+def _passes(coll, count, dt, A, R, sched=rv.SCHEDULE_RELAY, in_place=False, **kw):
+    p = rv.relay_plan(coll, count, dt, A, R, rv.make_opts(schedule=sched, **kw))
+    return p, rv.relay_plan_passes(p, in_place)
+
+
+def test_pass_bytes_a2_allreduce():
+    n, E = 1 << 20, 2
+    p, ps = _passes(rv.ALLREDUCE, n, rv.BF16, 2, 8)
+    cs = p.chunk
+    assert [q["name"] for q in ps] == ["group1", "group2", "active_reduce"]
+    # group 1: 12 relay chunks to helpers + 2 dirA chunks, each read once, written once
+    assert ps[0]["bytes_read"] == ps[0]["bytes_written"] == 14 * cs * E
+    # group 2: 6 helpers read 2 slots and write 2 returned chunks; 2 dirB copies
+    assert ps[1]["bytes_read"] == ps[1]["bytes_written"] == (12 + 2) * cs * E
+    # actives: own + received over dirA+dirB (2 chunks), 2 actives
+    assert ps[2]["bytes_read"] == 8 * cs * E and ps[2]["bytes_written"] == 4 * cs * E
+
+
+def test_pass_bytes_a2_reduce_scatter_and_a4():
+    m, E = 1 << 20, 4
+    p, ps = _passes(rv.REDUCE_SCATTER, m, rv.F32, 2, 8)
+    cs = p.chunk
+    assert ps[0]["bytes_read"] == 14 * cs * E
+    assert ps[1]["bytes_read"] == 14 * cs * E     # 12 forwarded slots + 2 dirB
+    assert ps[2]["bytes_read"] == 2 * 2 * m * E and ps[2]["bytes_written"] == 2 * m * E
+    n = 1 << 22
+    p, ps = _passes(rv.ALLREDUCE, n, rv.BF16, 4, 8)
+    oc, ds, E = p.chunk, p.owner_slice, 2
+    assert ps[0]["bytes_read"] == (16 * oc + 12 * ds) * E
+    # helpers and owners: 4 sources in, 4 destinations out
+    assert ps[1]["bytes_read"] == ps[1]["bytes_written"] == (4 * 4 * oc + 4 * 4 * ds) * E
+    p, ps = _passes(rv.REDUCE_SCATTER, n, rv.BF16, 4, 8)
+    oc = p.chunk
+    assert ps[0]["bytes_read"] - 12 * p.direct_g1 * E == 48 * oc * E   # pack 4x4x3 chunks
+    helper = ps[1]["bytes_read"] - 12 * p.direct_g2 * E
+    assert helper == 4 * 4 * 3 * oc * E     # 16 reductions of 3 chunks
+
+
+def test_pass_bytes_all_to_all_pack_unpack():
+    seg, E = 120000 * 8, 2
+    p, ps = _passes(rv.ALL_TO_ALL, seg, rv.BF16, 4, 8)
+    oc = p.chunk
+    assert [q["name"] for q in ps] == ["pack", "helper_forward", "unpack"]
+    assert ps[2]["bytes_read"] == ps[2]["bytes_written"] == 4 * 4 * 3 * oc * E
+    assert ps[0]["bytes_read"] == (4 * 4 * 3 * oc + 12 * p.direct_g1 + 4 * seg) * E
+
+
+def test_in_place_drops_self_copies():
+    p, out_of_place = _passes(rv.ALL_GATHER, 1 << 20, rv.BF16, 4, 8)
+    _, in_place = _passes(rv.ALL_GATHER, 1 << 20, rv.BF16, 4, 8, in_place=True)
+    assert out_of_place[0]["bytes_read"] - in_place[0]["bytes_read"] == 4 * (1 << 20) * 2
+
+
+# ----------------------------------------------------------------- size contracts --
+
+def _golden_rows(name):
+    for line in open(os.path.join(GOLDEN, name)):
+        line = line.split("#", 1)[0].strip()
+        if line:
+            yield line.split()
+
+
+def test_passthrough_helper_size_literals():
+    # D115998394 / D115998388 hand-computed literals
+    for row in _golden_rows("helper_sizes.txt"):
+        if row[0] == "total":
+            groups, count, A, nc, total = (int(v) for v in row[1:])
+            assert groups * rv.relay_passthrough_helper_size(count, A, nc) == total
+        else:
+            count, A, nc, exp = (int(v) for v in row)
+            assert rv.relay_passthrough_helper_size(count, A, nc) == exp
+
+
+@pytest.mark.parametrize("count", [1024, 65536, 1 << 20, 12_002_982_488 // 64, 777_777])
+def test_helper_need_fits_page_contract(orc, count):
+    for coll in range(4):
+        for A in (2, 4):
+            p = rv.relay_plan(coll, count, rv.BF16, A, 8, rv.make_opts(schedule=rv.SCHEDULE_RELAY))
+            contract = orc.relay_helper_contract(coll, A, 8, count)
+            if A == 4 and coll == rv.ALL_TO_ALL:
+                continue   # the page's A=4 all-to-all never relays (size-1 placeholder)
+            assert p.helper_elems <= contract, (coll, A, count)
+    # item 6: the 4-active reduce-scatter helper needs A*(A-1)*chunk = 1.5x recvCount
+    m = 1 << 20
+    p = rv.relay_plan(rv.REDUCE_SCATTER, m, rv.BF16, 4, 8, rv.make_opts(schedule=rv.SCHEDULE_RELAY))
+    assert p.helper_elems * 2 == 3 * m
+
+
+# -------------------------------------------------------------------- validation --
+
+def _call(coll, send, recv, scratch, count, dt=rv.F32, A=2, R=8, scale=1.0):
+    fn = rv.lib()
+    arr = lambda xs: (ctypes.c_void_p * R)(*(xs + [None] * (R - len(xs))))
+    if coll in (rv.ALLREDUCE, rv.REDUCE_SCATTER):
+        f = fn.relay_allreduce if coll == rv.ALLREDUCE else fn.relay_reduce_scatter
+        return f(arr(send), arr(recv), arr(scratch), count, dt, A, R, scale, None, None)
+    f = fn.relay_all_gather if coll == rv.ALL_GATHER else fn.relay_all_to_all
+    return f(arr(send), arr(recv), arr(scratch), count, dt, A, R, None, None)
+
+
+GB = 1 << 30
+
+
+def _fake(i):
+    return (i + 1) * 64 * GB   # widely spaced, never dereferenced
+
+
+def test_validation_rejects_before_launch():
+    inval = rv.ERR_INVALID_ARGUMENT
+    ok_scratch = [_fake(10 + r) for r in range(8)]
+    # A and R (D115998382)
+    for A, R in [(3, 8), (1, 8), (2, 2), (4, 4), (2, 65)]:
+        p = rv.RelayPlan()
+        assert rv.lib().relay_plan(0, 1024, 0, A, R, None, ctypes.byref(p)) == inval
+    # int32 reductions are SUM only
+    assert _call(rv.ALLREDUCE, [_fake(0), _fake(1)], [_fake(2), _fake(3)], ok_scratch, 4096,
+                 rv.I32, scale=0.5) == inval
+    # NULL active buffers
+    assert _call(rv.ALLREDUCE, [_fake(0), None], [_fake(2), _fake(3)], ok_scratch, 4096) == inval
+    # overlapping outputs
+    assert _call(rv.ALLREDUCE, [_fake(0), _fake(1)], [_fake(2), _fake(2) + 64], ok_scratch,
+                 4096) == inval
+    # element alignment
+    assert _call(rv.ALLREDUCE, [_fake(0) + 2, _fake(1)], [_fake(2), _fake(3)], ok_scratch,
+                 4096) == inval
+    # all-to-all is out-of-place only (D115998370)
+    assert _call(rv.ALL_TO_ALL, [_fake(0), _fake(1)], [_fake(0), _fake(3)], ok_scratch,
+                 4096) == inval
+    # reduce-scatter in-place must be at the own block offset (D115998376)
+    assert _call(rv.REDUCE_SCATTER, [_fake(0), _fake(1)], [_fake(0) + 4, _fake(3)],
+                 ok_scratch, 4096) == inval
+    # every rejection leaves a message
+    assert b"overlap" in rv.lib().relay_last_error() or rv.lib().relay_last_error()
+
+
+def test_count_zero_is_a_noop():
+    for coll in range(4):
+        assert _call(coll, [None, None], [None, None], [None] * 8, 0) == rv.OK
+
+
+def test_missing_scratch_is_rejected():
+    opts = rv.make_opts(schedule=rv.SCHEDULE_RELAY)
+    arr = lambda xs: (ctypes.c_void_p * 8)(*(xs + [None] * (8 - len(xs))))
+    st = rv.lib().relay_allreduce(arr([_fake(0), _fake(1)]), arr([_fake(2), _fake(3)]),
+                                  arr([_fake(4), _fake(5)]), 1 << 20, rv.F32, 2, 8, 1.0,
+                                  ctypes.byref(opts), None)
+    assert st == rv.ERR_INVALID_ARGUMENT
+    assert b"helper" in rv.lib().relay_last_error()
+
+
+def test_legacy_only_at_two_actives():
+    with pytest.raises(rv.RelayError):
+        rv.relay_plan(rv.ALLREDUCE, 1 << 20, rv.F32, 4, 8, rv.make_opts(schedule=rv.SCHEDULE_LEGACY))
+    p = rv.relay_plan(rv.ALLREDUCE, 1 << 20, rv.F32, 2, 8, rv.make_opts(schedule=rv.SCHEDULE_LEGACY))
+    assert p.kind == rv.KIND_LEGACY and p.num_groups == 3
+
+
+def test_pass_names():
+    assert [rv.relay_pass_name(k) for k in range(7)] == list(rv.PASS_NAMES)
+
+
+# ------------------------------------------- bounds and races of every program (dry) --
+
+def _dry(coll, count, dt, A, R, sched, in_place):
+    """Run a collective in dry-run mode over fake, disjoint buffers of exactly the
+    declared sizes: the library builds every pass and checks that each segment stays
+    inside a declared buffer and that no launch races with itself; nothing launches."""
+    opts = rv.make_opts(schedule=sched, flags=rv.FLAG_CHECK_HAZARDS | rv.FLAG_DRY_RUN)
+    p = rv.relay_plan(coll, count, dt, A, R, opts)
+    E = rv.ESIZE[dt]
+    base = lambda r, k: ((4 * r + k + 1) << 40) + 256 * (r % 3)
+    send, recv, scratch = [], [], []
+    for a in range(A):
+        s, r = base(a, 0), base(a, 1)
+        if in_place and coll == rv.ALLREDUCE:
+            r = s
+        elif in_place and coll == rv.REDUCE_SCATTER:
+            r = s + a * count * E
+        elif in_place and coll == rv.ALL_GATHER:
+            s = r + a * count * E
+        send.append(s)
+        recv.append(r)
+    for r_ in range(R):
+        scratch.append(base(r_, 2))
+    arr = lambda xs: (ctypes.c_void_p * R)(*(xs + [None] * (R - len(xs))))
+    L = rv.lib()
+    if coll in (rv.ALLREDUCE, rv.REDUCE_SCATTER):
+        f = L.relay_allreduce if coll == rv.ALLREDUCE else L.relay_reduce_scatter
+        scale = 1.0 if dt == rv.I32 else 0.5
+        st = f(arr(send), arr(recv), arr(scratch), count, dt, A, R, scale, ctypes.byref(opts), None)
+    else:
+        f = L.relay_all_gather if coll == rv.ALL_GATHER else L.relay_all_to_all
+        st = f(arr(send), arr(recv), arr(scratch), count, dt, A, R, ctypes.byref(opts), None)
+    return st
+
+
+@pytest.mark.parametrize("coll", range(4))
+def test_every_program_stays_in_bounds_and_race_free(coll):
+    n = 0
+    for A in (2, 4):
+        for R in (A + 1, 8, 40):
+            for dt in (rv.F32, rv.BF16, rv.I32):
+                for count in (1, 127, 1024, 1025, 4109, 65536 + 77, 1 << 22, (3 << 20) + 5):
+                    for sched in (0, 1, 2, 3):
+                        if sched == 3 and A == 4:
+                            continue
+                        for in_place in (False, True):
+                            if in_place and coll == rv.ALL_TO_ALL:
+                                continue
+                            try:
+                                rv.relay_plan(coll, count, dt, A, R, rv.make_opts(schedule=sched))
+                            except rv.RelayError:
+                                continue
+                            st = _dry(coll, count, dt, A, R, sched, in_place)
+                            assert st == rv.OK, rv.lib().relay_last_error()
+                            n += 1
+    assert n > 200

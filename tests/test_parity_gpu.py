@@ -1,0 +1,159 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Every output element is compared bit for bit with the oracle (the kernels sum in the
+oracle's order, so fp32 and bf16 results are bit-identical, and the stated
+tolerances -- fp32 relative error 1e-6 against the fp64 sum, bf16 within one ulp of
+the fp32 sum -- are checked on top); int32, all-gather and all-to-all are bit-exact.
+Canary bands around every buffer must stay untouched, inputs must be unchanged
+out-of-place, and no launch may hold two segments that race (checked on the host).
+
+Page: "Link-balance the sharded relay schedules (up to 3.2x vs NCCL)".
+"""
+import numpy as np
+import pytest
+import torch
+
+import harness as hz
+import pack_virtual_rank_gb300 as rv
+
+pytestmark = pytest.mark.gpu
+
+SMALL_COUNTS = [1, 2, 127, 128, 129, 1000, 1023, 1024, 1025, 1792, 2047, 2048, 4109, 9000,
+                65536 + 77]
+SCHEDULES = [rv.SCHEDULE_AUTO, rv.SCHEDULE_RELAY, rv.SCHEDULE_DIRECT, rv.SCHEDULE_LEGACY]
+
+
+def _scale(coll, A, dtype):
+    if coll not in (rv.ALLREDUCE, rv.REDUCE_SCATTER) or dtype == rv.I32:
+        return 1.0
+    return 1.0 / A
+
+
+@pytest.mark.parametrize("dtype", [rv.F32, rv.BF16, rv.I32])
+@pytest.mark.parametrize("A", [2, 4])
+@pytest.mark.parametrize("coll", [rv.ALLREDUCE, rv.REDUCE_SCATTER, rv.ALL_GATHER, rv.ALL_TO_ALL])
+def test_small_sizes_every_schedule(coll, A, dtype):
+    """Every count around the 128-element alignment and chunk boundaries, every
+    schedule, R = A+1 (one helper) and R = 8, in-place and out-of-place."""
+    n = 0
+    for R in (A + 1, 8):
+        for count in SMALL_COUNTS:
+            for sched in SCHEDULES:
+                if sched == rv.SCHEDULE_LEGACY and A != 2:
+                    continue
+                for in_place in (False, True):
+                    if in_place and coll == rv.ALL_TO_ALL:
+                        continue
+                    try:
+                        rv.relay_plan(coll, count, dtype, A, R, rv.make_opts(schedule=sched))
+                    except rv.RelayError:
+                        assert sched == rv.SCHEDULE_LEGACY   # chunk aligns down to 0
+                        continue
+                    c = hz.run(coll, A, R, count, dtype, _scale(coll, A, dtype), config=7,
+                               schedule=sched, in_place=in_place)
+                    hz.check_all(c)
+                    n += 1
+    assert n > 50
+
+
+@pytest.mark.parametrize("coll", [rv.ALLREDUCE, rv.REDUCE_SCATTER, rv.ALL_GATHER, rv.ALL_TO_ALL])
+@pytest.mark.parametrize("dtype", [rv.F32, rv.BF16])
+@pytest.mark.parametrize("shift", [1, 3])
+def test_unaligned_buffers(coll, dtype, shift):
+    """Buffers that are element- but not 16-byte-aligned: all sharing one offset
+    (vector path after a peeled prologue) and with mixed offsets (per-element path)."""
+    for A in (2, 4):
+        count = 5000 + 3
+        sched = rv.SCHEDULE_RELAY
+        opts = rv.make_opts(schedule=sched, flags=rv.FLAG_CHECK_HAZARDS)
+        plan = rv.relay_plan(coll, count, dtype, A, 8, opts)
+        xs = hz.make_inputs(11, A, plan.input_elems, dtype, "cuda")
+        td = hz.TORCH[dtype]
+
+        def buf(n, s):
+            full = torch.zeros(n + 64, dtype=td, device="cuda")
+            return full[s:s + n]
+        mixed = shift == 3
+        send = [buf(plan.input_elems, 1) for _ in range(A)]
+        for a in range(A):
+            send[a].copy_(xs[a])
+        recv = [buf(plan.output_elems, 3 if mixed else 1) for _ in range(A)]
+        scratch = [buf(plan.active_scratch_elems, 1) if plan.active_scratch_elems else None
+                   for _ in range(A)]
+        scratch += [buf(plan.helper_elems, 5 if mixed else 1) for _ in range(8 - A)]
+        fn = rv.COLLECTIVES[coll]
+        args = (send + [None] * (8 - A), recv + [None] * (8 - A), scratch, count, dtype, A, 8)
+        if coll in (rv.ALLREDUCE, rv.REDUCE_SCATTER):
+            fn(*args, _scale(coll, A, dtype), opts)
+        else:
+            fn(*args, opts)
+        torch.cuda.synchronize()
+        c = hz.Call()
+        c.plan, c.coll, c.A, c.R, c.count, c.dtype = plan, coll, A, 8, count, dtype
+        c.scale, c.inputs, c.recv = _scale(coll, A, dtype), xs, recv
+        xs_host = [hz.host(x) for x in xs]
+        for a in range(A):
+            hz.check_window(c, a, 0, plan.output_elems, xs_host)
+
+
+def test_many_helpers_split_launches():
+    """R large enough that one group's segment table spans several launches."""
+    for coll in (rv.REDUCE_SCATTER, rv.ALL_TO_ALL):
+        c = hz.run(coll, 4, 40, 36 * 1024 + 5, rv.BF16, _scale(coll, 4, rv.BF16),
+                   schedule=rv.SCHEDULE_RELAY)
+        hz.check_all(c)
+
+
+def test_repeat_calls_reuse_scratch():
+    """Scratch keeps the previous call's contents; results must not depend on them."""
+    c = hz.run(rv.ALLREDUCE, 4, 8, 300_000, rv.BF16, 0.25, schedule=rv.SCHEDULE_RELAY)
+    hz.check_all(c)
+    xs2 = hz.make_inputs(99, 4, c.plan.input_elems, rv.BF16, "cuda")
+    for a in range(4):
+        c.send[a].copy_(xs2[a])
+    rv.relay_allreduce(c.send + [None] * 4, c.recv + [None] * 4, c.scratch, c.count, rv.BF16, 4,
+                       8, 0.25, rv.make_opts(schedule=rv.SCHEDULE_RELAY))
+    torch.cuda.synchronize()
+    c.inputs = xs2
+    hz.check_all(c)
+
+
+def test_special_values():
+    """Signed zeros, infinities and values whose sums round to ties survive the path
+    exactly as the oracle computes them."""
+    n = 4096
+    vals = torch.tensor([0.0, -0.0, 1.0, -1.0, float("inf"), 2.0 ** -130, 3.0e38, -3.0e38,
+                         1.0 + 2.0 ** -8, 2.0 ** -8], dtype=torch.float32)
+    g = torch.Generator().manual_seed(3)
+    for dtype in (rv.F32, rv.BF16):
+        xs = []
+        for a in range(4):
+            idx = torch.randint(0, len(vals), (n,), generator=g)
+            x = vals[idx]
+            xs.append((x if dtype == rv.F32 else x.to(torch.bfloat16)).cuda())
+        for coll, A in ((rv.ALLREDUCE, 2), (rv.ALLREDUCE, 4), (rv.REDUCE_SCATTER, 4)):
+            ins = [x[: n if coll == rv.ALLREDUCE else n] for x in xs[:A]]
+            count = n if coll == rv.ALLREDUCE else n // A
+            c = hz.run(coll, A, 8, count, dtype, 0.5, schedule=rv.SCHEDULE_RELAY, inputs=ins)
+            xs_host = [hz.host(x) for x in ins]
+            for a in range(A):
+                got = hz.host(c.recv[a])
+                q = hz.expected(c, xs_host, a, 0, c.plan.output_elems)[0]
+                # the mix holds +inf but no -inf, so no sum is NaN
+                assert np.array_equal(got, q)
+
+
+def test_pass_events_time_every_pass():
+    plan = rv.relay_plan(rv.ALLREDUCE, 1 << 22, rv.BF16, 2, 8)
+    npass = len(rv.relay_plan_passes(plan))
+    events = [torch.cuda.Event(enable_timing=True) for _ in range(npass + 1)]
+    opts = rv.make_opts(pass_events=events)
+    c = hz.run(rv.ALLREDUCE, 2, 8, 1 << 22, rv.BF16, 0.5, config=2)
+    rv.relay_allreduce(c.send + [None] * 6, c.recv + [None] * 6, c.scratch, 1 << 22, rv.BF16, 2, 8,
+                       0.5, opts)
+    torch.cuda.synchronize()
+    ms = [events[i].elapsed_time(events[i + 1]) for i in range(npass)]
+    assert all(t > 0 for t in ms)
+    with pytest.raises(rv.RelayError):
+        rv.relay_allreduce(c.send + [None] * 6, c.recv + [None] * 6, c.scratch, 1 << 22, rv.BF16,
+                           2, 8, 0.5, rv.make_opts(pass_events=events[:npass]))

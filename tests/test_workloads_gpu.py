@@ -1,0 +1,118 @@
+"""GPU parity at the full sizes of the five reference workloads.
+
+Outputs up to 16 MiB per rank are compared element by element with the oracle; larger
+ones are compared on windows around every chunk, slice and direct-region boundary
+plus random windows (the oracle computes each window from just the inputs it reads),
+and their canaries and untouched inputs are checked in full.
+
+Workloads (seeded N(0,1) fp32/bf16 and U[-2^20, 2^20] int32, seed 1000*w + rank):
+  1. allreduce A=2 of R=8, 65536 fp32, scale 1/2, relay forced (numChunks 8, d = n/4)
+  2. allreduce A=2 of R=8, bf16, scale 1/2, 64 KB .. 1 GB per rank (x2 steps); below
+     2 MB one full direct exchange
+  3. reduce-scatter A=2 of R=8, passthrough helpers, recvCount = count/2, input 2 MB ..
+     512 MB per rank; fp32 scale 1/2 and int32 scale 1
+  4. allreduce A=4 of R=8 at 500 permille with a 2 MB floor, and reduce-scatter A=4 flat
+     reduce-at-helper, bf16, scale 1/4, 1 MB .. 1 GB per rank
+  5. all-gather A=4 of R=8 and coalesced all-to-all (segmentCount = count/(A(A-1))),
+     bf16 and int32, 13.5 MB .. 1 GB per rank
+"""
+import pytest
+import torch
+
+import harness as hz
+import pack_virtual_rank_gb300 as rv
+
+pytestmark = pytest.mark.gpu
+
+MB = 1 << 20
+FULL_CHECK_BYTES = 16 * MB
+
+
+def _check(c):
+    if c.plan.output_elems * rv.ESIZE[c.dtype] <= FULL_CHECK_BYTES:
+        hz.check_all(c)
+    else:
+        hz.check_sampled(c)
+        for g in c.bufs:
+            assert g.guards_intact()
+    del c
+    torch.cuda.empty_cache()
+
+
+def _big(nbytes):
+    return nbytes > 256 * MB
+
+
+def test_allreduce_a2_fp32_65536_relay():
+    c = hz.run(rv.ALLREDUCE, 2, 8, 65536, rv.F32, 0.5, config=1, schedule=rv.SCHEDULE_RELAY)
+    p = c.plan
+    assert (p.kind, p.chunk, p.dirA_size + p.dirB_size) == (rv.KIND_RELAY, 8192, 65536 // 4)
+    t = rv.relay_plan_link_bytes(p)
+    assert t[:, 0, 1].sum() == 65536 // 4 * 4          # 0.25 * count on the direct link
+    hz.check_all(c)
+
+
+@pytest.mark.parametrize("nbytes", [64 * 1024 << k for k in range(15)])
+def test_allreduce_a2_bf16_sweep(nbytes):
+    n = nbytes // 2
+    c = hz.run(rv.ALLREDUCE, 2, 8, n, rv.BF16, 0.5, config=2, gpu_generator=_big(nbytes))
+    assert c.plan.kind == (rv.KIND_RELAY if nbytes >= 2 * MB else rv.KIND_DIRECT)
+    if nbytes < 2 * MB:
+        assert c.plan.num_groups == 1
+    _check(c)
+
+
+@pytest.mark.parametrize("nbytes", [2 * MB << k for k in range(9)])
+@pytest.mark.parametrize("dtype", [rv.F32, rv.I32])
+def test_reduce_scatter_a2_passthrough_sweep(nbytes, dtype):
+    count = nbytes // 4
+    m = count // 2
+    scale = 0.5 if dtype == rv.F32 else 1.0
+    c = hz.run(rv.REDUCE_SCATTER, 2, 8, m, dtype, scale, config=3, gpu_generator=_big(nbytes))
+    assert c.plan.kind == rv.KIND_RELAY
+    _check(c)
+
+
+@pytest.mark.parametrize("nbytes", [MB << k for k in range(11)])
+def test_allreduce_a4_bf16_sweep(nbytes):
+    n = nbytes // 2
+    c = hz.run(rv.ALLREDUCE, 4, 8, n, rv.BF16, 0.25, config=4, gpu_generator=_big(nbytes))
+    assert c.plan.kind == (rv.KIND_RELAY if nbytes >= 2 * MB else rv.KIND_DIRECT)
+    _check(c)
+
+
+@pytest.mark.parametrize("nbytes", [MB << k for k in range(11)])
+def test_reduce_scatter_a4_flat_sweep(nbytes):
+    m = nbytes // 2 // 4
+    c = hz.run(rv.REDUCE_SCATTER, 4, 8, m, rv.BF16, 0.25, config=4, gpu_generator=_big(nbytes))
+    assert c.plan.kind == (rv.KIND_RELAY if nbytes > 48 * MB else rv.KIND_DIRECT)
+    if c.plan.kind == rv.KIND_RELAY:
+        # item 6: the helper needs 1.5x recvCount, within the 2x recvCount contract
+        assert c.plan.helper_elems * 2 == 3 * m
+    _check(c)
+
+
+AG_SIZES = [int(13.5 * MB), 27 * MB, 54 * MB, 108 * MB, 135 * MB, 256 * MB, 512 * MB, 1024 * MB]
+
+
+@pytest.mark.parametrize("nbytes", AG_SIZES)
+@pytest.mark.parametrize("dtype", [rv.BF16, rv.I32])
+def test_all_gather_a4_sweep(nbytes, dtype):
+    S = nbytes // rv.ESIZE[dtype]
+    c = hz.run(rv.ALL_GATHER, 4, 8, S, dtype, config=5, schedule=rv.SCHEDULE_RELAY,
+               gpu_generator=_big(nbytes))
+    p = c.plan
+    assert p.direct_g2 >= 3 * p.direct_g1     # direct region split 1:(A-1)
+    _check(c)
+
+
+@pytest.mark.parametrize("nbytes", AG_SIZES)
+@pytest.mark.parametrize("dtype", [rv.BF16, rv.I32])
+def test_all_to_all_a4_coalesced_sweep(nbytes, dtype):
+    count = nbytes // rv.ESIZE[dtype]
+    seg = count // 12
+    c = hz.run(rv.ALL_TO_ALL, 4, 8, seg, dtype, config=5, schedule=rv.SCHEDULE_RELAY,
+               gpu_generator=_big(nbytes))
+    assert [q["name"] for q in rv.relay_plan_passes(c.plan)] == ["pack", "helper_forward",
+                                                                  "unpack"]
+    _check(c)
