@@ -81,12 +81,15 @@ class Clocks:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, enabled: bool = True):
         self.proc = None
+        self.enabled = enabled
         self.gpu = gpu_index
         self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
 
     def __enter__(self):
+        if not self.enabled:
+            return self
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
@@ -107,6 +110,8 @@ class Clocks:
 
     def summary(self):
         if self.proc is None:
+            self.out.close()
+            os.unlink(self.out.name)
             return None
         self.out.seek(0)
         sm, mx, reasons = [], [], set()
@@ -145,6 +150,22 @@ def _bytes_per_step(plan, rv, count=None):
         plan = rv.relay_plan(rv.ALLREDUCE, count, rv.BF16, A, R)
     ps = rv.relay_plan_passes(plan)
     return sum(p["bytes_read"] + p["bytes_written"] for p in ps), ps
+
+
+def slowest_rank(times_ms, world):
+    """Max over ranks of each timing (replicas finish when the slowest one does)."""
+    if world <= 1:
+        return list(times_ms)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(list(times_ms), dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t]
+
+
+def whole_job_gbs(bytes_per_step, steps, world, ms):
+    """Whole-job throughput: every replica's bytes over the slowest replica's time."""
+    return bytes_per_step * steps * world / (ms / 1e3) / 1e9
 
 
 def run_reference(args):
@@ -196,12 +217,13 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream()
-    plan = rv.relay_plan(rv.ALLREDUCE, COUNT, rv.BF16, A, R)
+    count = args.count
+    plan = rv.relay_plan(rv.ALLREDUCE, count, rv.BF16, A, R)
     nbytes, passes = _bytes_per_step(plan, rv)
     npass = len(passes)
     launches_per_step = sum((p["num_segments"] + 383) // 384 for p in passes)
 
-    xs = [synth.rank_input(2, r, COUNT, "bf16", device=dev) for r in range(A)]
+    xs = [synth.rank_input(2, r, count, "bf16", device=dev) for r in range(A)]
     ys = [torch.empty_like(x) for x in xs]
     scratch = rv.alloc_scratch(plan, dev)
     send = xs + [None] * (R - A)
@@ -213,18 +235,18 @@ def run_ours(args):
             dist.barrier()
 
     for _ in range(args.warmup):
-        rv.relay_allreduce(send, recv, scratch, COUNT, rv.BF16, A, R, SCALE)
+        rv.relay_allreduce(send, recv, scratch, count, rv.BF16, A, R, SCALE)
     # per-pass events of every timed step
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(npass + 1)]
           for _ in range(args.steps)]
     opts = [rv.make_opts(pass_events=e) for e in ev]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
-    with Clocks(local) as clk:
+    with Clocks(local, enabled=not args.kernel_only) as clk:
         barrier()
         start.record(stream)
         for k in range(args.steps):
-            rv.relay_allreduce(send, recv, scratch, COUNT, rv.BF16, A, R, SCALE, opts[k])
+            rv.relay_allreduce(send, recv, scratch, count, rv.BF16, A, R, SCALE, opts[k])
         stop.record(stream)
         barrier()
     ms = start.elapsed_time(stop)
@@ -233,46 +255,46 @@ def run_ours(args):
                 for i in range(npass)]
 
     # end to end: pinned host inputs in, results out, through the same call
-    hx = [x.cpu().pin_memory() for x in xs]
-    hy = [torch.empty(COUNT, dtype=torch.bfloat16).pin_memory() for _ in range(A)]
-    e2e_steps = max(1, min(args.steps, 5))
-    barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        for a in range(A):
-            xs[a].copy_(hx[a], non_blocking=True)
-        rv.relay_allreduce(send, recv, scratch, COUNT, rv.BF16, A, R, SCALE)
-        for a in range(A):
-            hy[a].copy_(ys[a], non_blocking=True)
-    e1.record(stream)
-    barrier()
-    e2e_ms = e0.elapsed_time(e1)
+    e2e_ms, e2e_steps = None, max(1, min(args.steps, 5))
+    if not args.kernel_only:
+        hx = [x.cpu().pin_memory() for x in xs]
+        hy = [torch.empty(count, dtype=torch.bfloat16).pin_memory() for _ in range(A)]
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            for a in range(A):
+                xs[a].copy_(hx[a], non_blocking=True)
+            rv.relay_allreduce(send, recv, scratch, count, rv.BF16, A, R, SCALE)
+            for a in range(A):
+                hy[a].copy_(ys[a], non_blocking=True)
+        e1.record(stream)
+        barrier()
+        e2e_ms = e0.elapsed_time(e1)
 
-    if world > 1:
-        t = torch.tensor([ms, e2e_ms], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, e2e_ms = float(t[0]), float(t[1])
+    ms, e2e_ms = slowest_rank([ms, e2e_ms if e2e_ms is not None else 0.0], world)
 
     if rank == 0:
         peak, peak_kind = _peaks()
-        value = nbytes * args.steps * world / (ms / 1e3) / 1e9
-        e2e = nbytes * e2e_steps * world / (e2e_ms / 1e3) / 1e9
+        value = whole_job_gbs(nbytes, args.steps, world, ms)
+        e2e = whole_job_gbs(nbytes, e2e_steps, world, e2e_ms) if e2e_ms else None
         top = max(range(npass), key=lambda i: per_pass[i])
         top_bytes = passes[top]["bytes_read"] + passes[top]["bytes_written"]
         achieved = top_bytes / (per_pass[top] / 1e3) / 1e9
         traffic, _sha = _profiled_traffic()
         tr = traffic.get(passes[top]["name"]) if traffic else None
-        cpu_t = _cpu_oracle(CPU_SAMPLE)
+        cpu_t = None if args.kernel_only else _cpu_oracle(CPU_SAMPLE)
         cpu_bytes, _ = _bytes_per_step(plan, rv, CPU_SAMPLE)
-        cpu_val = cpu_bytes / cpu_t / 1e9
+        cpu_val = cpu_bytes / cpu_t / 1e9 if cpu_t else None
         line = {
             "metric": "relay-pass HBM GB/s (allreduce A=2 of R=8, bf16)",
             "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded N(0,1) bf16, generated on the device)",
-            "config": {"workload": WORKLOAD, "count": COUNT, "A": A, "R": R,
+            "config": {"workload": WORKLOAD if count == COUNT else
+                       f"allreduce A=2 of R=8, bf16, {count} elements per rank (profiling case)",
+                       "count": count, "A": A, "R": R,
                        "schedule": ["relay", "zero_chunk", "direct", "legacy"][plan.kind],
                        "numChunks": plan.H + 2, "chunk": plan.chunk,
                        "l2": "inputs larger than L2 (1 GiB per rank); no flush",
@@ -287,13 +309,13 @@ def run_ours(args):
                          "frac": round(achieved / peak, 4), "traffic": tr,
                          "peak_source": f"{peak_kind} hbm_gbs (copy, burst)",
                          "algorithmic_bytes_per_launch": top_bytes},
-            "cpu_baseline": {"value": round(cpu_val, 3), "unit": "GB/s", "cores": 1,
-                             "kind": "oracle",
-                             "sample": f"oracle allreduce on {CPU_SAMPLE} elements per rank "
-                                       f"({cpu_t:.2f} s); GB/s counts the relay schedule's "
-                                       "algorithmic bytes for that count"},
-            "e2e": {"value": round(e2e, 2), "unit": "GB/s",
-                    "h2d_bytes_per_step": A * COUNT * 2, "d2h_bytes_per_step": A * COUNT * 2},
+            "cpu_baseline": None if cpu_t is None else {
+                "value": round(cpu_val, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                "sample": f"oracle allreduce on {CPU_SAMPLE} elements per rank ({cpu_t:.2f} s); "
+                          "GB/s counts the relay schedule's algorithmic bytes for that count"},
+            "e2e": None if e2e is None else {
+                "value": round(e2e, 2), "unit": "GB/s", "h2d_bytes_per_step": A * count * 2,
+                "d2h_bytes_per_step": A * count * 2},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks,
         }
@@ -310,6 +332,11 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--count", type=int, default=COUNT,
+                    help="elements per rank (default 2^29 = 1 GiB of bf16); smaller counts are "
+                         "for profiling captures, not bench lines")
+    ap.add_argument("--kernel-only", action="store_true",
+                    help="time the device passes only (no end-to-end leg, no CPU baseline)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)   # at least 3 untimed steps before timing
     if args.impl == "reference":

@@ -213,6 +213,36 @@ relay_status_t relay_all_to_all(void* const* send, void* const* recv, void* cons
                                 size_t segment_count, relay_dtype_t dtype, int A, int R,
                                 const relay_opts_t* opts, cudaStream_t stream);
 
+/*
+ * Fused multi-group call (D115998367, D115998376, D115998378): the R = num_groups*A
+ * ranks form num_groups sparse groups of A consecutive ranks (group g = ranks g*A ..
+ * g*A+A-1, D115998382). Every rank is active in its own group and a relay helper in
+ * every other group; each group plans its own schedule from counts[g] (a group whose
+ * chunk aligns down to zero takes the direct fallback while the others relay). The
+ * groups run phase-synchronized: one launch carries every group's group-1 transfers,
+ * the next every group's group-2 transfers, and so on, then every group's closing
+ * reductions.
+ *   send[r], recv[r]   (r < R): rank r's input and output for its own group;
+ *   scratch[g*R + r]   rank r's scratch for group g: its active scratch when r is in
+ *                      group g (plan.active_scratch_elems), its helper scratch otherwise
+ *                      (plan.helper_elems); NULL where the size is 0.
+ * Sizes, dtypes, in-place forms and scale are as for the single-group calls; scale is
+ * ignored for all-gather and all-to-all. Every buffer must be disjoint from every other
+ * except the in-place forms.
+ */
+relay_status_t relay_multi_group(relay_coll_t coll, int num_groups, const size_t* counts,
+                                 void* const* send, void* const* recv, void* const* scratch,
+                                 relay_dtype_t dtype, int A, float scale,
+                                 const relay_opts_t* opts, cudaStream_t stream);
+
+/* Link-byte accountant of a fused call: out[(p*R + src)*R + dst] = payload BYTES moved
+ * from rank src to rank dst in phase p (the groups' serialized group p, summed over
+ * groups). *num_phases receives the number of phases; cap >= num_phases*R*R. */
+relay_status_t relay_multi_group_link_bytes(relay_coll_t coll, int num_groups,
+                                            const size_t* counts, relay_dtype_t dtype, int A,
+                                            const relay_opts_t* opts, uint64_t* out, size_t cap,
+                                            int* num_phases);
+
 /* Human-readable text of the last error this thread's calls produced. */
 const char* relay_last_error(void);
 int relay_abi_version(void);

@@ -7,6 +7,13 @@
  * table or helper with the CUDA library in pack_virtual_rank_gb300/, and the library
  * never calls it.
  *
+ * Parity unpinned (readings the page does not fix; the tests hold them to the stated
+ * reading only): the crossover values the page gives no figure for (A=2 allreduce full
+ * exchange, A=2 all-gather and all-to-all, A=4 all-to-all), the A=2 chunk-to-helper
+ * mapping and direct-region placement, the A=4 owner-slice alignment, and the value of
+ * orc_passthrough_helper_size when the aligned chunk is zero.  Everything else here is
+ * pinned by tests/test_oracle_pins.py.
+ *
  * Citations name the page "Link-balance the sharded relay schedules (up to 3.2x vs
  * NCCL)" (torchrec pull request #4570).  "Sk" is item k of that page's summary;
  * "cost model" is the paragraph before item 1; "Dnnnnnnnnn" is the commit of the

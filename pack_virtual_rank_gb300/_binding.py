@@ -98,6 +98,11 @@ def lib():
         fn = getattr(L, name)
         fn.argtypes = [arr, arr, arr, sz, i32, i32, i32, P(RelayOpts), vp]
         fn.restype = i32
+    L.relay_multi_group.argtypes = [i32, i32, P(sz), arr, arr, arr, i32, i32, f32, P(RelayOpts), vp]
+    L.relay_multi_group.restype = i32
+    L.relay_multi_group_link_bytes.argtypes = [i32, i32, P(sz), i32, i32, P(RelayOpts),
+                                               P(ctypes.c_uint64), sz, P(ctypes.c_int)]
+    L.relay_multi_group_link_bytes.restype = i32
     if L.relay_abi_version() != 1:
         raise RuntimeError("librelay.so ABI version mismatch")
     _lib = L
@@ -262,4 +267,61 @@ def alloc_scratch(plan: RelayPlan, device, torch_dtype=None):
     for r in range(plan.R):
         n = plan.active_scratch_elems if r < plan.A else plan.helper_elems
         out.append(torch.empty(n, dtype=td, device=device) if n > 0 else None)
+    return out
+
+
+# -------------------------------------------------------------- fused multi-group --
+
+def group_ranks(g: int, A: int, R: int) -> list:
+    """Global ranks of group g's local ranks: its A actives, then its helpers."""
+    return [g * A + a for a in range(A)] + [r for r in range(R) if r // A != g]
+
+
+def relay_multi_group(coll: int, counts: Sequence[int], send, recv, scratch, dtype, A: int,
+                      scale: float = 1.0, opts: Optional[RelayOpts] = None, stream=None) -> None:
+    """Fused call over len(counts) groups of A consecutive ranks (R = groups * A).
+    send/recv: R entries (rank r's buffers for its own group); scratch: one list of R
+    entries per group (rank r's scratch for that group)."""
+    G = len(counts)
+    R = G * A
+    flat = [x for per_group in scratch for x in _pad(per_group, R)]
+    if len(flat) != G * R:
+        raise ValueError("scratch needs one list of R entries per group")
+    c = (ctypes.c_size_t * G)(*counts)
+    _check(lib().relay_multi_group(coll, G, c, _ptr_array(send, R), _ptr_array(recv, R),
+                                   (ctypes.c_void_p * (G * R))(*[_ptr(x) for x in flat]),
+                                   dtype_code(dtype), A, scale,
+                                   ctypes.byref(opts) if opts is not None else None,
+                                   _stream(stream)))
+
+
+def relay_multi_group_link_bytes(coll: int, counts: Sequence[int], dtype, A: int,
+                                 opts: Optional[RelayOpts] = None) -> np.ndarray:
+    G = len(counts)
+    R = G * A
+    out = np.zeros(3 * R * R, np.uint64)
+    phases = ctypes.c_int(0)
+    c = (ctypes.c_size_t * G)(*counts)
+    _check(lib().relay_multi_group_link_bytes(
+        coll, G, c, dtype_code(dtype), A, ctypes.byref(opts) if opts is not None else None,
+        out.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64)), out.size, ctypes.byref(phases)))
+    return out[: phases.value * R * R].reshape(phases.value, R, R)
+
+
+def alloc_multi_scratch(coll: int, counts: Sequence[int], dtype, A: int, device,
+                        opts: Optional[RelayOpts] = None):
+    """Per group, R scratch buffers sized by that group's plan (None where not needed)."""
+    import torch
+    G = len(counts)
+    R = G * A
+    td = {F32: torch.float32, BF16: torch.bfloat16, I32: torch.int32}[dtype_code(dtype)]
+    out = []
+    for g in range(G):
+        p = relay_plan(coll, counts[g], dtype, A, R, opts)
+        row = [None] * R
+        for l, r in enumerate(group_ranks(g, A, R)):
+            n = p.active_scratch_elems if l < A else p.helper_elems
+            if n > 0:
+                row[r] = torch.empty(n, dtype=td, device=device)
+        out.append(row)
     return out

@@ -26,12 +26,15 @@ relay_status_t fail(relay_status_t st, const std::string& msg) {
 // whose segment lengths and ranks can be counted without touching memory.
 struct FakeBuffers {
   std::vector<void*> send, recv, scratch;
-  FakeBuffers(const relay_plan_t& p, bool in_place) {
+  FakeBuffers(const relay_plan_t& p, bool in_place, int salt = 0) {
     send.resize(p.R);
     recv.resize(p.R);
     scratch.resize(p.R);
     for (int r = 0; r < p.R; ++r) {
-      auto base = [&](int k) { return reinterpret_cast<void*>((uintptr_t)(4 * r + k + 1) << 42); };
+      auto base = [&](int k) {
+        return reinterpret_cast<void*>(((uintptr_t)(4 * r + k + 1) << 42) +
+                                       ((uintptr_t)salt << 36));
+      };
       send[r] = base(0);
       recv[r] = base(1);
       scratch[r] = base(2);
@@ -109,78 +112,70 @@ bool find_out_of_bounds(const Pass& pass, int E, const std::vector<Range>& bufs,
   return false;
 }
 
-relay_status_t run_collective(relay_coll_t coll, void* const* send, void* const* recv,
-                              void* const* scratch, size_t count, relay_dtype_t dtype, int A,
-                              int R, float scale, const relay_opts_t* opts, cudaStream_t stream) {
-  if (count > (size_t)INT64_MAX) return fail(RELAY_ERR_INVALID_ARGUMENT, "count too large");
-  relay_plan_t p;
-  std::string why;
-  relay_status_t st = make_plan(coll, (int64_t)count, dtype, A, R, opts, &p, &why);
-  if (st != RELAY_OK) return fail(st, why);
-  const bool reduces = coll == RELAY_ALLREDUCE || coll == RELAY_REDUCE_SCATTER;
-  // D115998376: SUM (scale 1) and AVG (scale 1/A) only; an integer average is not
-  // defined on the page, so int32 takes scale 1 only
-  if (reduces && dtype == RELAY_I32 && scale != 1.0f)
-    return fail(RELAY_ERR_INVALID_ARGUMENT, "int32 reductions take scale == 1 only");
-  if (p.count == 0) return RELAY_OK;
-  if (send == nullptr || recv == nullptr || scratch == nullptr)
-    return fail(RELAY_ERR_INVALID_ARGUMENT, "pointer arrays must not be NULL");
-
+// Validate one group's buffers (R local entries: actives first, then its helpers) and
+// append their ranges. In-place forms are recognised and not counted twice.
+relay_status_t validate_group(const relay_plan_t& p, void* const* send, void* const* recv,
+                              void* const* scratch, const int* global_rank,
+                              std::vector<Range>* ranges) {
+  const int A = p.A;
   const int64_t E = p.esize;
-  std::vector<Range> ranges;
-  auto add = [&](const void* ptr, int64_t elems, const std::string& what) -> bool {
-    if (ptr == nullptr) return false;
+  auto name = [&](const char* what, int local) {
+    return std::string(what) + "[" + std::to_string(global_rank[local]) + "]";
+  };
+  auto add = [&](const void* ptr, int64_t elems, const std::string& what) {
     const uintptr_t lo = reinterpret_cast<uintptr_t>(ptr);
-    ranges.push_back(Range{lo, lo + (uintptr_t)(elems * E), what});
-    return true;
+    ranges->push_back(Range{lo, lo + (uintptr_t)(elems * E), what});
   };
   for (int a = 0; a < A; ++a) {
-    const std::string ra = std::to_string(a);
     if (send[a] == nullptr || recv[a] == nullptr)
-      return fail(RELAY_ERR_INVALID_ARGUMENT, "active " + ra + ": send/recv is NULL");
+      return fail(RELAY_ERR_INVALID_ARGUMENT, "active " + name("rank", a) + ": send/recv is NULL");
     if ((reinterpret_cast<uintptr_t>(send[a]) | reinterpret_cast<uintptr_t>(recv[a])) % E)
-      return fail(RELAY_ERR_INVALID_ARGUMENT, "active " + ra + ": buffer not element-aligned");
+      return fail(RELAY_ERR_INVALID_ARGUMENT,
+                  "active " + name("rank", a) + ": buffer not element-aligned");
     const char* s = static_cast<const char*>(send[a]);
     const char* r = static_cast<const char*>(recv[a]);
     bool send_in_recv = false, recv_in_send = false;
-    switch (coll) {
-      case RELAY_ALLREDUCE: recv_in_send = r == s; break;                                // D115998369
-      case RELAY_REDUCE_SCATTER: recv_in_send = r == s + a * p.count * E; break;        // D115998376
-      case RELAY_ALL_GATHER: send_in_recv = s == r + a * p.count * E; break;            // D115998385
-      default: break;                                                                     // D115998370
+    switch (p.coll) {
+      case RELAY_ALLREDUCE: recv_in_send = r == s; break;                          // D115998369
+      case RELAY_REDUCE_SCATTER: recv_in_send = r == s + a * p.count * E; break;  // D115998376
+      case RELAY_ALL_GATHER: send_in_recv = s == r + a * p.count * E; break;      // D115998385
+      default: break;                                                               // D115998370
     }
-    if (!send_in_recv) add(send[a], p.input_elems, "send[" + ra + "]");
-    if (!recv_in_send) add(recv[a], p.output_elems, "recv[" + ra + "]");
-    if (p.active_scratch_elems > 0) {
-      if (scratch[a] == nullptr)
-        return fail(RELAY_ERR_INVALID_ARGUMENT, "active " + ra + " needs scratch");
-      if (reinterpret_cast<uintptr_t>(scratch[a]) % E)
-        return fail(RELAY_ERR_INVALID_ARGUMENT, "scratch[" + ra + "] not element-aligned");
-      add(scratch[a], p.active_scratch_elems, "scratch[" + ra + "]");
-    }
+    if (!send_in_recv) add(send[a], p.input_elems, name("send", a));
+    if (!recv_in_send) add(recv[a], p.output_elems, name("recv", a));
   }
-  if (p.helper_elems > 0)
-    for (int h = 0; h < p.H; ++h) {
-      const std::string rh = std::to_string(A + h);
-      if (scratch[A + h] == nullptr)
-        return fail(RELAY_ERR_INVALID_ARGUMENT, "helper rank " + rh + " needs scratch");
-      if (reinterpret_cast<uintptr_t>(scratch[A + h]) % E)
-        return fail(RELAY_ERR_INVALID_ARGUMENT, "scratch[" + rh + "] not element-aligned");
-      add(scratch[A + h], p.helper_elems, "scratch[" + rh + "]");
-    }
+  for (int l = 0; l < p.R; ++l) {
+    const int64_t need = l < A ? p.active_scratch_elems : p.helper_elems;
+    if (need <= 0) continue;
+    if (scratch[l] == nullptr)
+      return fail(RELAY_ERR_INVALID_ARGUMENT,
+                  std::string(l < A ? "active " : "helper ") + name("rank", l) + " needs scratch");
+    if (reinterpret_cast<uintptr_t>(scratch[l]) % E)
+      return fail(RELAY_ERR_INVALID_ARGUMENT, name("scratch", l) + " not element-aligned");
+    add(scratch[l], need, name("scratch", l));
+  }
+  return RELAY_OK;
+}
+
+relay_status_t check_disjoint(const std::vector<Range>& ranges) {
   for (size_t i = 0; i < ranges.size(); ++i)
     for (size_t j = i + 1; j < ranges.size(); ++j)
       if (overlaps(ranges[i], ranges[j]))
         return fail(RELAY_ERR_INVALID_ARGUMENT,
                     ranges[i].what + " overlaps " + ranges[j].what + " (not an in-place form)");
+  return RELAY_OK;
+}
 
-  std::vector<Pass> passes;
-  build_program(p, Buffers{send, recv, scratch}, false, &passes);
-
+// Optional host checks, then the passes in order on `stream`.
+relay_status_t execute(const std::vector<Pass>& passes, const std::vector<Range>& ranges,
+                       relay_dtype_t dtype, float scale, const relay_opts_t* opts,
+                       cudaStream_t stream) {
+  const int E = esize_of(dtype);
+  std::string why;
   const int flags = opts ? opts->flags : 0;
   if (flags & RELAY_FLAG_CHECK_HAZARDS)
     for (const Pass& ps : passes) {
-      if (find_out_of_bounds(ps, (int)E, ranges, &why) || find_hazard(ps, (int)E, &why))
+      if (find_out_of_bounds(ps, E, ranges, &why) || find_hazard(ps, E, &why))
         return fail(RELAY_ERR_UNSUPPORTED, "internal: " + why);
     }
   if (flags & RELAY_FLAG_DRY_RUN) return RELAY_OK;
@@ -200,6 +195,88 @@ relay_status_t run_collective(relay_coll_t coll, void* const* send, void* const*
   if (events && cudaEventRecord(events[passes.size()], stream) != cudaSuccess)
     return fail(RELAY_ERR_CUDA, "cudaEventRecord failed");
   return RELAY_OK;
+}
+
+relay_status_t check_scale(relay_coll_t coll, relay_dtype_t dtype, float scale) {
+  // D115998376: SUM (scale 1) and AVG (scale 1/A) only; an integer average is not
+  // defined on the page, so int32 takes scale 1 only
+  const bool reduces = coll == RELAY_ALLREDUCE || coll == RELAY_REDUCE_SCATTER;
+  if (reduces && dtype == RELAY_I32 && scale != 1.0f)
+    return fail(RELAY_ERR_INVALID_ARGUMENT, "int32 reductions take scale == 1 only");
+  return RELAY_OK;
+}
+
+relay_status_t run_collective(relay_coll_t coll, void* const* send, void* const* recv,
+                              void* const* scratch, size_t count, relay_dtype_t dtype, int A,
+                              int R, float scale, const relay_opts_t* opts, cudaStream_t stream) {
+  if (count > (size_t)INT64_MAX) return fail(RELAY_ERR_INVALID_ARGUMENT, "count too large");
+  relay_plan_t p;
+  std::string why;
+  relay_status_t st = make_plan(coll, (int64_t)count, dtype, A, R, opts, &p, &why);
+  if (st != RELAY_OK) return fail(st, why);
+  if ((st = check_scale(coll, dtype, scale)) != RELAY_OK) return st;
+  if (p.count == 0) return RELAY_OK;
+  if (send == nullptr || recv == nullptr || scratch == nullptr)
+    return fail(RELAY_ERR_INVALID_ARGUMENT, "pointer arrays must not be NULL");
+  std::vector<int> ident(R);
+  for (int r = 0; r < R; ++r) ident[r] = r;
+  std::vector<Range> ranges;
+  if ((st = validate_group(p, send, recv, scratch, ident.data(), &ranges)) != RELAY_OK) return st;
+  if ((st = check_disjoint(ranges)) != RELAY_OK) return st;
+  std::vector<Pass> passes;
+  build_program(p, Buffers{send, recv, scratch}, false, &passes);
+  return execute(passes, ranges, dtype, scale, opts, stream);
+}
+
+// Fused multi-group call (D115998367, D115998376): R/A sparse groups of A consecutive
+// ranks; every rank is active in its own group and a helper in every other group.
+// send/recv are indexed by global rank; scratch[g*R + r] is rank r's scratch for group
+// g. Each group plans its own schedule from its own count.
+relay_status_t run_multi(relay_coll_t coll, int num_groups, const size_t* counts,
+                         void* const* send, void* const* recv, void* const* scratch,
+                         relay_dtype_t dtype, int A, float scale, const relay_opts_t* opts,
+                         cudaStream_t stream) {
+  if (num_groups < 2 || counts == nullptr)
+    return fail(RELAY_ERR_INVALID_ARGUMENT, "a fused call needs at least 2 groups and counts");
+  const int R = num_groups * A;
+  if (A != 2 && A != 4) return fail(RELAY_ERR_INVALID_ARGUMENT, "A must be 2 or 4");
+  if (R > RELAY_MAX_RANKS) return fail(RELAY_ERR_INVALID_ARGUMENT, "num_groups*A exceeds RELAY_MAX_RANKS");
+  relay_status_t st = check_scale(coll, dtype, scale);
+  if (st != RELAY_OK) return st;
+  if (send == nullptr || recv == nullptr || scratch == nullptr)
+    return fail(RELAY_ERR_INVALID_ARGUMENT, "pointer arrays must not be NULL");
+  std::vector<relay_plan_t> plans(num_groups);
+  std::vector<std::vector<int>> gmap(num_groups);
+  std::vector<std::vector<void*>> ls(num_groups), lr(num_groups), lw(num_groups);
+  std::vector<Range> ranges;
+  std::string why;
+  for (int g = 0; g < num_groups; ++g) {
+    if (counts[g] > (size_t)INT64_MAX) return fail(RELAY_ERR_INVALID_ARGUMENT, "count too large");
+    st = make_plan(coll, (int64_t)counts[g], dtype, A, R, opts, &plans[g], &why);
+    if (st != RELAY_OK) return fail(st, "group " + std::to_string(g) + ": " + why);
+    gmap[g] = group_ranks(g, A, R);
+    ls[g].assign(R, nullptr);
+    lr[g].assign(R, nullptr);
+    lw[g].assign(R, nullptr);
+    for (int l = 0; l < R; ++l) {
+      const int r = gmap[g][l];
+      if (l < A) {
+        ls[g][l] = send[r];
+        lr[g][l] = recv[r];
+      }
+      lw[g][l] = scratch[(size_t)g * R + r];
+    }
+    if (plans[g].count == 0) continue;
+    st = validate_group(plans[g], ls[g].data(), lr[g].data(), lw[g].data(), gmap[g].data(),
+                        &ranges);
+    if (st != RELAY_OK) return fail(st, "group " + std::to_string(g) + ": " + relay_last_error());
+  }
+  if ((st = check_disjoint(ranges)) != RELAY_OK) return st;
+  std::vector<Buffers> bufs(num_groups);
+  for (int g = 0; g < num_groups; ++g) bufs[g] = Buffers{ls[g].data(), lr[g].data(), lw[g].data()};
+  std::vector<Pass> passes;
+  build_multi_program(plans, bufs, gmap, &passes);
+  return execute(passes, ranges, dtype, scale, opts, stream);
 }
 
 }  // namespace
@@ -331,6 +408,57 @@ relay_status_t relay_all_to_all(void* const* send, void* const* recv, void* cons
                                 const relay_opts_t* opts, cudaStream_t stream) {
   return run_collective(RELAY_ALL_TO_ALL, send, recv, scratch, segment_count, dtype, A, R, 1.0f,
                         opts, stream);
+}
+
+relay_status_t relay_multi_group(relay_coll_t coll, int num_groups, const size_t* counts,
+                                 void* const* send, void* const* recv, void* const* scratch,
+                                 relay_dtype_t dtype, int A, float scale,
+                                 const relay_opts_t* opts, cudaStream_t stream) {
+  if (coll < RELAY_ALLREDUCE || coll > RELAY_ALL_TO_ALL)
+    return fail(RELAY_ERR_INVALID_ARGUMENT, "unknown collective");
+  if (coll == RELAY_ALL_GATHER || coll == RELAY_ALL_TO_ALL) scale = 1.0f;
+  return run_multi(coll, num_groups, counts, send, recv, scratch, dtype, A, scale, opts, stream);
+}
+
+relay_status_t relay_multi_group_link_bytes(relay_coll_t coll, int num_groups,
+                                            const size_t* counts, relay_dtype_t dtype, int A,
+                                            const relay_opts_t* opts, uint64_t* out, size_t cap,
+                                            int* num_phases) {
+  if (!counts || !out || num_groups < 2 || (A != 2 && A != 4) || num_groups * A > RELAY_MAX_RANKS)
+    return fail(RELAY_ERR_INVALID_ARGUMENT, "bad fused-call description");
+  const int R = num_groups * A;
+  std::vector<relay_plan_t> plans(num_groups);
+  std::vector<std::vector<int>> gmap(num_groups);
+  std::vector<FakeBuffers> fakes;
+  fakes.reserve(num_groups);
+  std::string why;
+  int G = 0;
+  for (int g = 0; g < num_groups; ++g) {
+    const relay_status_t st =
+        make_plan(coll, (int64_t)counts[g], dtype, A, R, opts, &plans[g], &why);
+    if (st != RELAY_OK) return fail(st, why);
+    G = std::max(G, plans[g].num_groups);
+    gmap[g] = group_ranks(g, A, R);
+    fakes.emplace_back(plans[g], false, g);
+  }
+  const size_t need = (size_t)G * R * R;
+  if (num_phases) *num_phases = G;
+  if (cap < need) return fail(RELAY_ERR_INVALID_ARGUMENT, "link table too small");
+  std::fill(out, out + need, 0);
+  std::vector<Buffers> bufs;
+  for (auto& f : fakes) bufs.push_back(f.view());
+  std::vector<Pass> passes;
+  build_multi_program(plans, bufs, gmap, &passes);
+  for (const Pass& ps : passes)
+    for (size_t i = 0; i < ps.segs.size(); ++i) {
+      const SegMeta& m = ps.meta[i];
+      if (m.group < 0) continue;
+      for (int d = 0; d < ps.segs[i].ndst; ++d)
+        if (m.dst_rank[d] != m.exec_rank)
+          out[((size_t)m.group * R + m.exec_rank) * R + m.dst_rank[d]] +=
+              (uint64_t)ps.segs[i].n * esize_of(dtype);
+    }
+  return RELAY_OK;
 }
 
 }  // extern "C"

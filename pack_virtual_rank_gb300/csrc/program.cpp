@@ -403,4 +403,54 @@ void build_program(const relay_plan_t& p, const Buffers& b, bool in_place,
              out->end());
 }
 
+std::vector<int> group_ranks(int g, int A, int R) {
+  std::vector<int> m;
+  m.reserve(R);
+  for (int a = 0; a < A; ++a) m.push_back(g * A + a);
+  for (int r = 0; r < R; ++r)
+    if (r / A != g) m.push_back(r);
+  return m;
+}
+
+namespace {
+// Order of a pass within a phase-synchronized fused call.
+int phase_of(relay_pass_kind_t k) {
+  switch (k) {
+    case RELAY_PASS_G1:
+    case RELAY_PASS_PACK: return 0;
+    case RELAY_PASS_G2:
+    case RELAY_PASS_HELPER_FORWARD: return 1;
+    case RELAY_PASS_G3: return 2;
+    default: return 3;
+  }
+}
+}  // namespace
+
+void build_multi_program(const std::vector<relay_plan_t>& plans, const std::vector<Buffers>& bufs,
+                         const std::vector<std::vector<int>>& global_rank, std::vector<Pass>* out) {
+  out->clear();
+  std::vector<Pass> merged(4);
+  for (int ph = 0; ph < 4; ++ph) merged[ph].kind = RELAY_PASS_G1;
+  std::vector<bool> used(4, false);
+  for (size_t g = 0; g < plans.size(); ++g) {
+    std::vector<Pass> one;
+    build_program(plans[g], bufs[g], false, &one);
+    for (Pass& ps : one) {
+      const int ph = phase_of(ps.kind);
+      if (!used[ph]) merged[ph].kind = ps.kind;
+      used[ph] = true;
+      for (size_t i = 0; i < ps.segs.size(); ++i) {
+        SegMeta m = ps.meta[i];
+        m.exec_rank = (int8_t)global_rank[g][m.exec_rank];
+        for (int d = 0; d < kMaxDst; ++d)
+          if (m.dst_rank[d] >= 0) m.dst_rank[d] = (int8_t)global_rank[g][m.dst_rank[d]];
+        merged[ph].segs.push_back(ps.segs[i]);
+        merged[ph].meta.push_back(m);
+      }
+    }
+  }
+  for (int ph = 0; ph < 4; ++ph)
+    if (used[ph] && !merged[ph].segs.empty()) out->push_back(std::move(merged[ph]));
+}
+
 }  // namespace relay

@@ -63,6 +63,16 @@ struct Buffers {
 void build_program(const relay_plan_t& p, const Buffers& b, bool in_place,
                    std::vector<Pass>* out);
 
+// Global ranks of group g's local ranks in a fused multi-group call: its A actives
+// (ranks g*A .. g*A+A-1, D115998382) first, then every other rank ascending as its
+// helpers.
+std::vector<int> group_ranks(int g, int A, int R);
+
+// Programs of several groups merged phase by phase (every group's group-1 transfers in
+// one launch, then group 2, ...), local ranks renamed to global ones -- program.cpp.
+void build_multi_program(const std::vector<relay_plan_t>& plans, const std::vector<Buffers>& bufs,
+                         const std::vector<std::vector<int>>& global_rank, std::vector<Pass>* out);
+
 // Launch one pass on `stream` -- passes.cu. Splits into several launches when the
 // segment table exceeds one launch's parameter capacity.
 cudaError_t launch_pass(int dtype, const Pass& pass, float scale, cudaStream_t stream);

@@ -317,3 +317,92 @@ def test_every_program_stays_in_bounds_and_race_free(coll):
                             assert st == rv.OK, rv.lib().relay_last_error()
                             n += 1
     assert n > 200
+
+
+# ------------------------------------------------------------ fused multi-group call --
+
+def _dry_multi(coll, counts, dt, A, sched, in_place=False):
+    G = len(counts)
+    R = G * A
+    opts = rv.make_opts(schedule=sched, flags=rv.FLAG_CHECK_HAZARDS | rv.FLAG_DRY_RUN)
+    E = rv.ESIZE[dt]
+    send, recv = [], []
+    for r in range(R):
+        s, rr = (r + 1) << 40, ((r + 1) << 40) + (1 << 38)
+        if in_place and coll == rv.ALLREDUCE:
+            rr = s
+        elif in_place and coll == rv.REDUCE_SCATTER:
+            rr = s + (r % A) * counts[r // A] * E
+        elif in_place and coll == rv.ALL_GATHER:
+            s = rr + (r % A) * counts[r // A] * E
+        send.append(s)
+        recv.append(rr)
+    scratch = [((100 + g * R + r) << 40) for g in range(G) for r in range(R)]
+    c = (ctypes.c_size_t * G)(*counts)
+    arr = lambda xs: (ctypes.c_void_p * len(xs))(*xs)
+    scale = 1.0 if dt == rv.I32 else 0.5
+    return rv.lib().relay_multi_group(coll, G, c, arr(send), arr(recv), arr(scratch), dt, A, scale,
+                                      ctypes.byref(opts), None)
+
+
+@pytest.mark.parametrize("coll", range(4))
+def test_fused_programs_stay_in_bounds_and_race_free(coll):
+    mixes = {2: [[65536, 1000, 300_000, 4097], [1 << 20] * 4, [0, 5, 1024, 129]],
+             4: [[65536, 3000], [1 << 20, 1 << 20], [0, 70_000]]}
+    n = 0
+    for A, lists in mixes.items():
+        for counts in lists:
+            for dt in (rv.F32, rv.BF16, rv.I32):
+                for sched in (0, 1, 2):
+                    for in_place in (False, True):
+                        if in_place and coll == rv.ALL_TO_ALL:
+                            continue
+                        st = _dry_multi(coll, counts, dt, A, sched, in_place)
+                        assert st == rv.OK, rv.lib().relay_last_error()
+                        n += 1
+    assert n > 50
+
+
+def test_fused_uniform_relay_puts_one_chunk_on_every_link():
+    # 4 groups of 2 on 8 ranks: each rank is active once and a helper 3 times; with the
+    # same count everywhere every directed link carries exactly one chunk per phase, so
+    # all four allreduces finish in the time of one (cost model, item 1)
+    n = 1 << 20
+    t = rv.relay_multi_group_link_bytes(rv.ALLREDUCE, [n] * 4, rv.BF16, 2,
+                                        rv.make_opts(schedule=rv.SCHEDULE_RELAY))
+    cs = n // 8
+    assert t.shape == (2, 8, 8)
+    for ph in range(2):
+        off = t[ph][~np.eye(8, dtype=bool)]
+        assert np.all(off == cs * 2)
+        assert np.all(np.diag(t[ph]) == 0)
+
+
+@pytest.mark.parametrize("coll", range(4))
+def test_fused_table_is_sum_of_group_tables(orc, coll):
+    # the fused table equals each group's oracle table, local ranks renamed to global
+    counts, A = [65536, 1000, 300_000, 4097], 2
+    if coll in (rv.REDUCE_SCATTER, rv.ALL_TO_ALL):
+        counts = [c // 2 for c in counts]
+    opts = rv.make_opts(schedule=rv.SCHEDULE_RELAY)
+    got = rv.relay_multi_group_link_bytes(coll, counts, rv.F32, A, opts)
+    R = len(counts) * A
+    exp = np.zeros((3, R, R), np.uint64)
+    for g, c in enumerate(counts):
+        _, gv = orc.plan(coll, A, R, c, 4, force=rv.SCHEDULE_RELAY)
+        t = orc.link_elems(gv).astype(np.uint64) * np.uint64(4)
+        m = rv.group_ranks(g, A, R)
+        for ph in range(t.shape[0]):
+            for s in range(R):
+                for d in range(R):
+                    exp[ph, m[s], m[d]] += t[ph, s, d]
+    assert np.array_equal(got, exp[: got.shape[0]])
+    assert not exp[got.shape[0]:].any()
+
+
+def test_fused_validation():
+    arr = lambda xs: (ctypes.c_void_p * len(xs))(*xs)
+    c = (ctypes.c_size_t * 1)(1024)
+    # a single group is not a fused call
+    assert rv.lib().relay_multi_group(0, 1, c, arr([1 << 40, 2 << 40]), arr([3 << 40, 4 << 40]),
+                                      arr([None] * 2), 0, 2, 1.0, None, None) == rv.ERR_INVALID_ARGUMENT
