@@ -243,6 +243,18 @@ relay_status_t relay_multi_group_link_bytes(relay_coll_t coll, int num_groups,
                                             const relay_opts_t* opts, uint64_t* out, size_t cap,
                                             int* num_phases);
 
+/*
+ * Flat packing of a caller's tensor list (D115998366: the distributed layer packs the
+ * tensors into the active flat buffer and unpacks the result, one launch each).
+ * relay_pack_flat copies tensors srcs[0..n-1] (counts[i] elements each) end to end
+ * into `flat`; relay_unpack_flat copies them back out into dsts. One launch for up to
+ * 384 non-empty tensors. `flat` must hold sum(counts) elements and overlap no tensor.
+ */
+relay_status_t relay_pack_flat(const void* const* srcs, const size_t* counts, int n, void* flat,
+                               relay_dtype_t dtype, cudaStream_t stream);
+relay_status_t relay_unpack_flat(const void* flat, void* const* dsts, const size_t* counts, int n,
+                                 relay_dtype_t dtype, cudaStream_t stream);
+
 /* Human-readable text of the last error this thread's calls produced. */
 const char* relay_last_error(void);
 int relay_abi_version(void);

@@ -103,6 +103,10 @@ def lib():
     L.relay_multi_group_link_bytes.argtypes = [i32, i32, P(sz), i32, i32, P(RelayOpts),
                                                P(ctypes.c_uint64), sz, P(ctypes.c_int)]
     L.relay_multi_group_link_bytes.restype = i32
+    L.relay_pack_flat.argtypes = [arr, P(sz), i32, vp, i32, vp]
+    L.relay_pack_flat.restype = i32
+    L.relay_unpack_flat.argtypes = [vp, arr, P(sz), i32, i32, vp]
+    L.relay_unpack_flat.restype = i32
     if L.relay_abi_version() != 1:
         raise RuntimeError("librelay.so ABI version mismatch")
     _lib = L
@@ -325,3 +329,23 @@ def alloc_multi_scratch(coll: int, counts: Sequence[int], dtype, A: int, device,
                 row[r] = torch.empty(n, dtype=td, device=device)
         out.append(row)
     return out
+
+
+# ------------------------------------------------------------ flat pack / unpack --
+
+def relay_pack_flat(tensors: Sequence, flat, dtype=None, stream=None) -> None:
+    """Copy `tensors` end to end into `flat` (one launch)."""
+    n = len(tensors)
+    dt = dtype_code(dtype if dtype is not None else flat.dtype)
+    counts = (ctypes.c_size_t * max(n, 1))(*[t.numel() for t in tensors])
+    _check(lib().relay_pack_flat((ctypes.c_void_p * max(n, 1))(*[_ptr(t) for t in tensors]),
+                                 counts, n, _ptr(flat), dt, _stream(stream)))
+
+
+def relay_unpack_flat(flat, tensors: Sequence, dtype=None, stream=None) -> None:
+    """Copy consecutive pieces of `flat` back into `tensors` (one launch)."""
+    n = len(tensors)
+    dt = dtype_code(dtype if dtype is not None else flat.dtype)
+    counts = (ctypes.c_size_t * max(n, 1))(*[t.numel() for t in tensors])
+    _check(lib().relay_unpack_flat(_ptr(flat), (ctypes.c_void_p * max(n, 1))(*[_ptr(t) for t in tensors]),
+                                   counts, n, dt, _stream(stream)))

@@ -420,6 +420,60 @@ relay_status_t relay_multi_group(relay_coll_t coll, int num_groups, const size_t
   return run_multi(coll, num_groups, counts, send, recv, scratch, dtype, A, scale, opts, stream);
 }
 
+// D115998366: the distributed layer packs the caller's tensors into the active flat
+// buffer with one launch and unpacks the result with one launch; here both are a single
+// pass of copy segments (split only past 384 tensors).
+static relay_status_t flat_copy(const void* const* parts, const size_t* counts, int n,
+                                void* flat, relay_dtype_t dtype, bool pack, cudaStream_t stream) {
+  if (n < 0 || (n > 0 && (parts == nullptr || counts == nullptr)))
+    return fail(RELAY_ERR_INVALID_ARGUMENT, "bad tensor list");
+  if (dtype < RELAY_F32 || dtype > RELAY_I32) return fail(RELAY_ERR_INVALID_ARGUMENT, "unknown dtype");
+  const int E = esize_of(dtype);
+  Pass ps{pack ? RELAY_PASS_PACK : RELAY_PASS_UNPACK, {}, {}};
+  std::vector<Range> ranges;
+  int64_t off = 0;
+  for (int i = 0; i < n; ++i) {
+    if (counts[i] > (size_t)INT64_MAX / 16) return fail(RELAY_ERR_INVALID_ARGUMENT, "count too large");
+    const int64_t c = (int64_t)counts[i];
+    if (c == 0) continue;
+    if (parts[i] == nullptr || flat == nullptr)
+      return fail(RELAY_ERR_INVALID_ARGUMENT, "tensor " + std::to_string(i) + " is NULL");
+    if ((reinterpret_cast<uintptr_t>(parts[i]) | reinterpret_cast<uintptr_t>(flat)) % E)
+      return fail(RELAY_ERR_INVALID_ARGUMENT, "tensor " + std::to_string(i) + " not element-aligned");
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(parts[i]);
+    ranges.push_back(Range{lo, lo + (uintptr_t)(c * E), "tensor " + std::to_string(i)});
+    Seg sg{};
+    char* f = static_cast<char*>(flat) + off * E;
+    sg.src[0] = pack ? parts[i] : f;
+    sg.dst[0] = pack ? (void*)f : const_cast<void*>(parts[i]);
+    sg.n = c;
+    sg.op = kOpCopy;
+    sg.nsrc = sg.ndst = 1;
+    ps.segs.push_back(sg);
+    ps.meta.push_back(SegMeta{-1, 0, {0, -1, -1, -1}});
+    off += c;
+  }
+  if (off == 0) return RELAY_OK;
+  const uintptr_t lo = reinterpret_cast<uintptr_t>(flat);
+  ranges.push_back(Range{lo, lo + (uintptr_t)(off * E), "flat"});
+  relay_status_t st = check_disjoint(ranges);
+  if (st != RELAY_OK) return st;
+  const cudaError_t e = launch_pass(dtype, ps, 1.0f, stream);
+  if (e != cudaSuccess) return fail(RELAY_ERR_CUDA, cudaGetErrorString(e));
+  return RELAY_OK;
+}
+
+relay_status_t relay_pack_flat(const void* const* srcs, const size_t* counts, int n, void* flat,
+                               relay_dtype_t dtype, cudaStream_t stream) {
+  return flat_copy(srcs, counts, n, flat, dtype, true, stream);
+}
+
+relay_status_t relay_unpack_flat(const void* flat, void* const* dsts, const size_t* counts, int n,
+                                 relay_dtype_t dtype, cudaStream_t stream) {
+  return flat_copy(const_cast<const void* const*>(dsts), counts, n, const_cast<void*>(flat), dtype,
+                   false, stream);
+}
+
 relay_status_t relay_multi_group_link_bytes(relay_coll_t coll, int num_groups,
                                             const size_t* counts, relay_dtype_t dtype, int A,
                                             const relay_opts_t* opts, uint64_t* out, size_t cap,

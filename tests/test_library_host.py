@@ -406,3 +406,13 @@ def test_fused_validation():
     # a single group is not a fused call
     assert rv.lib().relay_multi_group(0, 1, c, arr([1 << 40, 2 << 40]), arr([3 << 40, 4 << 40]),
                                       arr([None] * 2), 0, 2, 1.0, None, None) == rv.ERR_INVALID_ARGUMENT
+
+
+def test_flat_pack_validation():
+    arr = lambda xs: (ctypes.c_void_p * len(xs))(*xs)
+    c = (ctypes.c_size_t * 2)(100, 100)
+    # the flat buffer overlaps a tensor
+    assert rv.lib().relay_pack_flat(arr([1 << 40, 2 << 40]), c, 2, (1 << 40) + 8, 0, None) \
+        == rv.ERR_INVALID_ARGUMENT
+    # empty list: nothing to do
+    assert rv.lib().relay_pack_flat(arr([None]), c, 0, None, 0, None) == rv.OK

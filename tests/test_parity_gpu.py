@@ -157,3 +157,24 @@ def test_pass_events_time_every_pass():
     with pytest.raises(rv.RelayError):
         rv.relay_allreduce(c.send + [None] * 6, c.recv + [None] * 6, c.scratch, 1 << 22, rv.BF16,
                            2, 8, 0.5, rv.make_opts(pass_events=events[:npass]))
+
+
+def test_flat_pack_unpack_round_trip():
+    """Caller tensor lists packed into one flat buffer and unpacked again, one launch
+    each (commit D115998366); odd sizes and offsets take the unaligned paths."""
+    g = torch.Generator().manual_seed(5)
+    sizes = [1, 7, 128, 1000, 4097, 65536 + 3, 0, 300_001]
+    for dtype in (rv.F32, rv.BF16, rv.I32):
+        td = hz.TORCH[dtype]
+        ts = [torch.randint(-1000, 1000, (n,), generator=g).to(td).cuda() for n in sizes]
+        flat = hz.Guarded(sum(sizes), dtype, "cuda")
+        rv.relay_pack_flat(ts, flat.view)
+        torch.cuda.synchronize()
+        exp = torch.cat([t.cpu() for t in ts])
+        assert torch.equal(flat.view.cpu(), exp)
+        outs = [hz.Guarded(n, dtype, "cuda") for n in sizes]
+        rv.relay_unpack_flat(flat.view, [o.view for o in outs])
+        torch.cuda.synchronize()
+        for t, o in zip(ts, outs):
+            assert torch.equal(o.view.cpu(), t.cpu()) and o.guards_intact()
+        assert flat.guards_intact()
