@@ -326,6 +326,97 @@ def run_ours(args):
     return 0
 
 
+def _sweep_points():
+    """The five reference workloads at a spread of their sizes (bytes per rank)."""
+    MB = 1 << 20
+    pts = [("allreduce", 2, "f32", 65536 * 4, "relay")]
+    pts += [("allreduce", 2, "bf16", b, "auto") for b in
+            [64 * 1024, 256 * 1024, MB, 4 * MB, 16 * MB, 64 * MB, 256 * MB, 1024 * MB]]
+    for dt in ("f32", "i32"):
+        pts += [("reduce_scatter", 2, dt, b, "auto") for b in [2 * MB, 8 * MB, 32 * MB, 128 * MB, 512 * MB]]
+    for coll in ("allreduce", "reduce_scatter"):
+        pts += [(coll, 4, "bf16", b, "auto") for b in [MB, 4 * MB, 16 * MB, 64 * MB, 256 * MB, 1024 * MB]]
+    for coll in ("all_gather", "all_to_all"):
+        for dt in ("bf16", "i32"):
+            pts += [(coll, 4, dt, b, "relay") for b in
+                    [int(13.5 * MB), 54 * MB, 135 * MB, 512 * MB, 1024 * MB]]
+    return pts
+
+
+def run_sweep(args):
+    """Per collective and count: each pass's time (CUDA events, L2 flushed before every
+    repetition), algorithmic bytes, GB/s and fraction of the measured HBM peak."""
+    import torch
+    import pack_virtual_rank_gb300.build as b
+    b.build()
+    import pack_virtual_rank_gb300 as rv
+    import synth
+    dev = torch.device("cuda", 0)
+    peak, _ = _peaks()
+    colls = {"allreduce": rv.ALLREDUCE, "reduce_scatter": rv.REDUCE_SCATTER,
+             "all_gather": rv.ALL_GATHER, "all_to_all": rv.ALL_TO_ALL}
+    dts = {"f32": rv.F32, "bf16": rv.BF16, "i32": rv.I32}
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2 // 4, dtype=torch.float32, device=dev)
+    rows = []
+    for name, A, dt, nbytes, sched in _sweep_points():
+        coll, d = colls[name], dts[dt]
+        E = rv.ESIZE[d]
+        elems = nbytes // E
+        count = {rv.ALLREDUCE: elems, rv.REDUCE_SCATTER: elems // A, rv.ALL_GATHER: elems,
+                 rv.ALL_TO_ALL: elems // (A * (A - 1))}[coll]
+        opts0 = rv.make_opts(schedule=rv.SCHEDULE_RELAY if sched == "relay" else rv.SCHEDULE_AUTO)
+        plan = rv.relay_plan(coll, count, d, A, R, opts0)
+        passes = rv.relay_plan_passes(plan)
+        xs = [synth.rank_input(9, r, plan.input_elems, dt, device=dev) for r in range(A)]
+        ys = [torch.empty(plan.output_elems, dtype=xs[0].dtype, device=dev) for _ in range(A)]
+        scratch = rv.alloc_scratch(plan, dev)
+        scale = 1.0 if (d == rv.I32 or coll in (rv.ALL_GATHER, rv.ALL_TO_ALL)) else 1.0 / A
+        fn = rv.COLLECTIVES[coll]
+
+        def call(opts):
+            a = (xs + [None] * (R - A), ys + [None] * (R - A), scratch, count, d, A, R)
+            if coll in (rv.ALLREDUCE, rv.REDUCE_SCATTER):
+                fn(*a, scale, opts)
+            else:
+                fn(*a, opts)
+        for _ in range(3):
+            call(opts0)
+        reps = args.steps
+        times = [[] for _ in passes]
+        totals = []
+        for _ in range(reps):
+            flush.fill_(1.0)
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(passes) + 1)]
+            o = rv.make_opts(schedule=opts0.schedule, pass_events=ev)
+            call(o)
+            torch.cuda.synchronize()
+            for i in range(len(passes)):
+                times[i].append(ev[i].elapsed_time(ev[i + 1]))
+            totals.append(ev[0].elapsed_time(ev[-1]))
+        prow = []
+        for p, t in zip(passes, times):
+            by = p["bytes_read"] + p["bytes_written"]
+            med = statistics.median(t)
+            prow.append({"pass": p["name"], "bytes": by, "ms_min": round(min(t), 4),
+                         "ms_median": round(med, 4), "gbs": round(by / med / 1e6, 1),
+                         "frac": round(by / med / 1e6 / peak, 3)})
+        tot_b = sum(p["bytes_read"] + p["bytes_written"] for p in passes)
+        med = statistics.median(totals)
+        row = {"collective": name, "A": A, "dtype": dt, "bytes_per_rank": nbytes, "count": count,
+               "schedule": ["relay", "zero_chunk", "direct", "legacy"][plan.kind],
+               "ms_median": round(med, 4), "gbs": round(tot_b / med / 1e6, 1),
+               "frac": round(tot_b / med / 1e6 / peak, 3), "passes": prow}
+        rows.append(row)
+        print(json.dumps(row), flush=True)
+        del xs, ys, scratch
+        torch.cuda.empty_cache()
+    if args.sweep_out:
+        with open(args.sweep_out, "w") as f:
+            json.dump({"peak_gbs": peak, "rows": rows}, f, indent=1)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -335,12 +426,18 @@ def main():
     ap.add_argument("--count", type=int, default=COUNT,
                     help="elements per rank (default 2^29 = 1 GiB of bf16); smaller counts are "
                          "for profiling captures, not bench lines")
+    ap.add_argument("--sweep", action="store_true",
+                    help="per-collective, per-count pass table of the five reference workloads "
+                         "(not a bench line)")
+    ap.add_argument("--sweep-out", default=None, help="write the sweep table as JSON here")
     ap.add_argument("--kernel-only", action="store_true",
                     help="time the device passes only (no end-to-end leg, no CPU baseline)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)   # at least 3 untimed steps before timing
     if args.impl == "reference":
         return run_reference(args)
+    if args.sweep:
+        return run_sweep(args)
     return run_ours(args)
 
 

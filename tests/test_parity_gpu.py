@@ -178,3 +178,33 @@ def test_flat_pack_unpack_round_trip():
         for t, o in zip(ts, outs):
             assert torch.equal(o.view.cpu(), t.cpu()) and o.guards_intact()
         assert flat.guards_intact()
+
+
+def test_cuda_graph_capture_and_replay():
+    """A whole collective captured into a CUDA graph (kernel parameters are captured by
+    value) replays to the same bits as a direct call, for small launch-bound sizes."""
+    for coll, A, count in ((rv.ALLREDUCE, 2, 32 * 1024), (rv.REDUCE_SCATTER, 4, 40_000),
+                           (rv.ALL_TO_ALL, 4, 30_000)):
+        scale = 0.5 if coll in (rv.ALLREDUCE, rv.REDUCE_SCATTER) else 1.0
+        c = hz.run(coll, A, 8, count, rv.BF16, scale, schedule=rv.SCHEDULE_RELAY)
+        hz.check_all(c)
+        ref = [hz.host(y).copy() for y in c.recv]
+        for y in c.recv:
+            y.zero_()
+        opts = rv.make_opts(schedule=rv.SCHEDULE_RELAY)
+        s = torch.cuda.Stream()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        fn = rv.COLLECTIVES[coll]
+        args = (c.send + [None] * (8 - A), c.recv + [None] * (8 - A), c.scratch, count, rv.BF16, A, 8)
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(graph, stream=s):
+                if coll in (rv.ALLREDUCE, rv.REDUCE_SCATTER):
+                    fn(*args, scale, opts, stream=s)
+                else:
+                    fn(*args, opts, stream=s)
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+        for y, r in zip(c.recv, ref):
+            assert np.array_equal(hz.host(y), r)
