@@ -255,6 +255,34 @@ relay_status_t relay_pack_flat(const void* const* srcs, const size_t* counts, in
 relay_status_t relay_unpack_flat(const void* flat, void* const* dsts, const size_t* counts, int n,
                                  relay_dtype_t dtype, cudaStream_t stream);
 
+/*
+ * relay_allreduce_noalloc -- an allreduce for callers that cannot allocate device
+ * memory when they call it (an allocator or memory-pool hook that would recurse into
+ * itself, a process that reserved all of HBM at start-up, a path that cannot take the
+ * synchronisation an allocation may cause). The page has no counterpart to this entry
+ * point.
+ *
+ * Arguments and results are those of relay_allreduce, without `scratch`: the helpers'
+ * relay slots and the actives' receive staging come from one file-scope device array of
+ * RELAY_NOALLOC_SCRATCH_BYTES that every GPU loading this library holds until exit.
+ * The call allocates nothing (no cudaMalloc, cudaFree or allocating library routine).
+ *   - Limit: A*round256(active_scratch_elems*esize) + H*round256(helper_elems*esize)
+ *     bytes (relay_plan gives both sizes) must fit the array; larger calls return
+ *     RELAY_ERR_INVALID_ARGUMENT with a message. For the 2-active relay that is about
+ *     2*count*esize, i.e. up to 32 MiB per rank.
+ *   - Set-up: the first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call before any
+ *     stream capture.
+ *   - Sharing: every call on a device uses the same array and leaves its contents
+ *     there. Nothing in it needs clearing (each call writes every element before it
+ *     reads it), but calls whose execution overlaps on the GPU (other streams, other
+ *     host threads) race on it: order them.
+ */
+#define RELAY_NOALLOC_SCRATCH_BYTES (64u << 20)
+relay_status_t relay_allreduce_noalloc(void* const* send, void* const* recv, size_t count,
+                                       relay_dtype_t dtype, int A, int R, float scale,
+                                       const relay_opts_t* opts, cudaStream_t stream);
+
 /* Human-readable text of the last error this thread's calls produced. */
 const char* relay_last_error(void);
 int relay_abi_version(void);

@@ -103,6 +103,8 @@ def lib():
     L.relay_multi_group_link_bytes.argtypes = [i32, i32, P(sz), i32, i32, P(RelayOpts),
                                                P(ctypes.c_uint64), sz, P(ctypes.c_int)]
     L.relay_multi_group_link_bytes.restype = i32
+    L.relay_allreduce_noalloc.argtypes = [arr, arr, sz, i32, i32, i32, f32, P(RelayOpts), vp]
+    L.relay_allreduce_noalloc.restype = i32
     L.relay_pack_flat.argtypes = [arr, P(sz), i32, vp, i32, vp]
     L.relay_pack_flat.restype = i32
     L.relay_unpack_flat.argtypes = [vp, arr, P(sz), i32, i32, vp]
@@ -257,6 +259,15 @@ def relay_all_to_all(send, recv, scratch, segment_count: int, dtype, A: int, R: 
                                   dtype_code(dtype), A, R,
                                   ctypes.byref(opts) if opts is not None else None,
                                   _stream(stream)))
+
+
+def relay_allreduce_noalloc(send, recv, count: int, dtype, A: int, R: int, scale: float = 1.0,
+                            opts: Optional[RelayOpts] = None, stream=None) -> None:
+    """Allreduce whose scratch is the library's built-in device array (see relay.h)."""
+    _check(lib().relay_allreduce_noalloc(_ptr_array(_pad(send, R), R), _ptr_array(_pad(recv, R), R),
+                                         count, dtype_code(dtype), A, R, scale,
+                                         ctypes.byref(opts) if opts is not None else None,
+                                         _stream(stream)))
 
 
 COLLECTIVES = {ALLREDUCE: relay_allreduce, REDUCE_SCATTER: relay_reduce_scatter,

@@ -280,6 +280,9 @@ relay_status_t run_multi(relay_coll_t coll, int num_groups, const size_t* counts
 }
 
 }  // namespace
+
+relay_status_t report_error(relay_status_t st, const std::string& msg) { return fail(st, msg); }
+
 }  // namespace relay
 
 using namespace relay;

@@ -77,6 +77,9 @@ void build_multi_program(const std::vector<relay_plan_t>& plans, const std::vect
 // segment table exceeds one launch's parameter capacity.
 cudaError_t launch_pass(int dtype, const Pass& pass, float scale, cudaStream_t stream);
 
+// Record `msg` as this thread's last error and return `st` -- abi.cpp.
+relay_status_t report_error(relay_status_t st, const std::string& msg);
+
 // Tile size in elements for a payload of esize bytes (shared by host tiling and the
 // kernel).
 constexpr int kThreads = 256;
