@@ -198,6 +198,115 @@ __device__ __forceinline__ void run_full_tile(const Seg& s, int64_t base, float 
   }
 }
 
+// ---------------------------------------------------------- realigned sources --
+// Destinations 16-byte aligned, sources at any element offset (an all-to-all whose
+// segmentCount is not a multiple of the vector width, an odd recvCount): each lane loads
+// the aligned 16-byte vector that holds the start of its source range, takes the next
+// one from its right neighbour by a warp shuffle (lane 31 loads it itself), and funnel-
+// shifts the pair by the source's byte offset. Reads stay inside the 16-byte blocks
+// that hold the segment's own bytes.
+
+__device__ __forceinline__ uint4 shift_pair(uint4 lo, uint4 hi, unsigned sigma) {
+  const unsigned r = (sigma & 3u) * 8u;
+  uint32_t w0 = lo.x, w1 = lo.y, w2 = lo.z, w3 = lo.w, w4 = hi.x, w5 = hi.y, w6 = hi.z, w7 = hi.w;
+  uint4 o;
+  switch (sigma >> 2) {
+    case 0:
+      o.x = __funnelshift_r(w0, w1, r); o.y = __funnelshift_r(w1, w2, r);
+      o.z = __funnelshift_r(w2, w3, r); o.w = __funnelshift_r(w3, w4, r);
+      break;
+    case 1:
+      o.x = __funnelshift_r(w1, w2, r); o.y = __funnelshift_r(w2, w3, r);
+      o.z = __funnelshift_r(w3, w4, r); o.w = __funnelshift_r(w4, w5, r);
+      break;
+    case 2:
+      o.x = __funnelshift_r(w2, w3, r); o.y = __funnelshift_r(w3, w4, r);
+      o.z = __funnelshift_r(w4, w5, r); o.w = __funnelshift_r(w5, w6, r);
+      break;
+    default:
+      o.x = __funnelshift_r(w3, w4, r); o.y = __funnelshift_r(w4, w5, r);
+      o.z = __funnelshift_r(w5, w6, r); o.w = __funnelshift_r(w6, w7, r);
+      break;
+  }
+  return o;
+}
+
+template <class P, int NSRC>
+__device__ __forceinline__ void realign_full_tile(const Seg& s, int64_t base, float scale) {
+  constexpr int L = P::kLanes;
+  // vectors per source held at once: up to 8 loads (plus lane 31's neighbours) in flight
+  constexpr int NB = NSRC == 1 ? kUnroll : 2;
+  using Acc = typename P::Acc;
+  const int64_t v0 = base / L + threadIdx.x;
+  const bool last_lane = (threadIdx.x & 31u) == 31u;
+  const bool do_scale = (s.flags & kFlagScale) != 0;
+  unsigned sig[NSRC];
+  const uint4* a[NSRC];
+#pragma unroll
+  for (int k = 0; k < NSRC; ++k) {
+    sig[k] = (unsigned)(reinterpret_cast<uintptr_t>(s.src[k]) & 15u);
+    a[k] = reinterpret_cast<const uint4*>(static_cast<const char*>(s.src[k]) - sig[k]);
+  }
+#pragma unroll 1
+  for (int u = 0; u < kUnroll; u += NB) {
+    // one round trip: every lane's aligned block, and lane 31's right neighbour
+    uint4 cur[NSRC][NB], ext[NSRC][NB];
+#pragma unroll
+    for (int j = 0; j < NB; ++j)
+#pragma unroll
+      for (int k = 0; k < NSRC; ++k) {
+        const int64_t vi = v0 + (u + j) * kThreads;
+        cur[k][j] = ld_stream_v4(a[k] + vi);
+        if (sig[k] != 0 && last_lane) ext[k][j] = ld_stream_v4(a[k] + vi + 1);
+      }
+#pragma unroll
+    for (int j = 0; j < NB; ++j) {
+      uint4 v[NSRC];
+#pragma unroll
+      for (int k = 0; k < NSRC; ++k) {
+        v[k] = cur[k][j];
+        if (sig[k] != 0) {
+          uint4 nxt;
+          nxt.x = __shfl_down_sync(0xffffffffu, cur[k][j].x, 1);
+          nxt.y = __shfl_down_sync(0xffffffffu, cur[k][j].y, 1);
+          nxt.z = __shfl_down_sync(0xffffffffu, cur[k][j].z, 1);
+          nxt.w = __shfl_down_sync(0xffffffffu, cur[k][j].w, 1);
+          if (last_lane) nxt = ext[k][j];
+          v[k] = shift_pair(cur[k][j], nxt, sig[k]);
+        }
+      }
+      uint4 r = v[0];
+      if (s.op != kOpCopy) {
+        Acc acc[L], t[L];
+        P::unpack(v[0], acc);
+#pragma unroll
+        for (int k = 1; k < NSRC; ++k) {
+          P::unpack(v[k], t);
+#pragma unroll
+          for (int i = 0; i < L; ++i) acc[i] = P::add(acc[i], t[i]);
+        }
+        if (do_scale) {
+#pragma unroll
+          for (int i = 0; i < L; ++i) acc[i] = P::scale(acc[i], scale);
+        }
+        r = P::pack(acc);
+      }
+      const int64_t vi = v0 + (u + j) * kThreads;
+#pragma unroll
+      for (int d = 0; d < kMaxDst; ++d)
+        if (d < s.ndst) st_v4(static_cast<uint4*>(s.dst[d]) + vi, r);
+    }
+  }
+}
+
+// One or two sources (the host sends segments with more sources to the per-element
+// path when their sources need realigning).
+template <class P>
+__device__ __forceinline__ void run_realign_tile(const Seg& s, int64_t base, float scale) {
+  if (s.nsrc == 1) realign_full_tile<P, 1>(s, base, scale);
+  else realign_full_tile<P, 2>(s, base, scale);
+}
+
 // The last, partial tile of a segment and every tile of a segment whose pointers are
 // not 16-byte aligned: one vector (or one element) per source at a time, with the
 // source count read at run time. Rare, so it is kept small rather than fast.
@@ -259,8 +368,11 @@ __device__ __noinline__ void run_partial_tile(const Seg& s, int64_t base, int64_
   }
 }
 
-template <class P, int CAP>
-__global__ void __launch_bounds__(kThreads) relay_pass_kernel(const __grid_constant__ PassArgs<CAP> args) {
+// REALIGN selects the variant that runs segments with realigned sources; it is its own
+// kernel so that its larger register need does not lower the occupancy of the others.
+template <class P, int CAP, bool REALIGN>
+__global__ void __launch_bounds__(kThreads, REALIGN ? 4 : 5)
+    relay_pass_kernel(const __grid_constant__ PassArgs<CAP> args) {
   constexpr int64_t kTile = kTileBytes / P::kE;
   for (int t = blockIdx.x; t < args.ntiles; t += gridDim.x) {
     // last segment whose first tile is <= t (uniform across the CTA)
@@ -272,43 +384,47 @@ __global__ void __launch_bounds__(kThreads) relay_pass_kernel(const __grid_const
     const Seg& s = args.seg[lo];
     const int64_t base = (int64_t)(t - s.tile0) * kTile;
     const int64_t len = min(kTile, s.n - base);
-    if ((s.flags & kFlagVector) && len == kTile) run_full_tile<P>(s, base, args.scale);
+    if (!REALIGN && (s.flags & kFlagVector) && len == kTile) run_full_tile<P>(s, base, args.scale);
+    else if (REALIGN && len == kTile) run_realign_tile<P>(s, base, args.scale);
     else run_partial_tile<P>(s, base, len, args.scale);
   }
 }
 
 // ------------------------------------------------------------------- host side --
 
-// Split segments so that as much as possible takes the vector path: when every
-// pointer of a segment sits at the same offset modulo 16 bytes, peel that many bytes
-// off the front as a per-element segment and vectorize the rest.
+// Split segments so that as much as possible takes a 16-byte path. When every pointer
+// of a segment sits at the same offset modulo 16 bytes, that many bytes are peeled off
+// the front as a per-element segment and the rest is vectorized. When only the
+// destinations share an offset, the head is peeled so that they are aligned and the
+// sources are realigned in registers. Destinations at different offsets leave the
+// segment to the per-element path.
 void split_for_alignment(const std::vector<Seg>& in, int E, std::vector<Seg>* out) {
   out->clear();
   out->reserve(in.size() + 8);
+  auto mis = [](const void* p) { return (unsigned)(reinterpret_cast<uintptr_t>(p) & 15u); };
   for (const Seg& s0 : in) {
     Seg s = s0;
-    auto mis = [](const void* p) { return (unsigned)(reinterpret_cast<uintptr_t>(p) & 15u); };
-    const unsigned m0 = mis(s.src[0]);
-    bool same = true;
-    for (int k = 0; k < s.nsrc; ++k) same &= mis(s.src[k]) == m0;
-    for (int d = 0; d < s.ndst; ++d) same &= mis(s.dst[d]) == m0;
-    if (!same || m0 % E != 0) {
-      s.flags &= ~kFlagVector;
+    s.flags &= ~(kFlagVector | kFlagRealign);
+    const unsigned md = mis(s.dst[0]);
+    bool dst_same = true, src_same = true;
+    for (int d = 0; d < s.ndst; ++d) dst_same &= mis(s.dst[d]) == md;
+    for (int k = 0; k < s.nsrc; ++k) src_same &= mis(s.src[k]) == md;
+    if (!dst_same || md % E != 0) {
       out->push_back(s);
       continue;
     }
-    const int64_t head = m0 == 0 ? 0 : std::min<int64_t>((16 - m0) / E, s.n);
+    const int64_t head = md == 0 ? 0 : std::min<int64_t>((16 - md) / E, s.n);
     if (head > 0) {
       Seg h = s;
       h.n = head;
-      h.flags &= ~kFlagVector;
       out->push_back(h);
       for (int k = 0; k < s.nsrc; ++k) s.src[k] = static_cast<const char*>(s.src[k]) + head * E;
       for (int d = 0; d < s.ndst; ++d) s.dst[d] = static_cast<char*>(s.dst[d]) + head * E;
       s.n -= head;
     }
     if (s.n > 0) {
-      s.flags |= kFlagVector;
+      if (src_same) s.flags |= kFlagVector;
+      else if (s.nsrc <= 2) s.flags |= kFlagRealign;
       out->push_back(s);
     }
   }
@@ -325,12 +441,12 @@ int sm_count() {
   return n;
 }
 
-template <class P, int CAP>
+template <class P, int CAP, bool REALIGN>
 int blocks_per_sm() {
   static int cached = 0;
   if (cached == 0) {
     int nb = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, relay_pass_kernel<P, CAP>, kThreads, 0) !=
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, relay_pass_kernel<P, CAP, REALIGN>, kThreads, 0) !=
             cudaSuccess ||
         nb <= 0)
       nb = 1;
@@ -339,7 +455,7 @@ int blocks_per_sm() {
   return cached;
 }
 
-template <class P, int CAP>
+template <class P, int CAP, bool REALIGN>
 cudaError_t launch_cap(const Seg* segs, int nseg, float scale, cudaStream_t stream) {
   static thread_local PassArgs<CAP> a;  // up to ~30 KiB: keep it off the stack
   constexpr int64_t kTile = kTileBytes / P::kE;
@@ -354,39 +470,52 @@ cudaError_t launch_cap(const Seg* segs, int nseg, float scale, cudaStream_t stre
   a.ntiles = (int32_t)tiles;
   a.scale = scale;
   a.pad = 0;
-  const int64_t cap = (int64_t)sm_count() * blocks_per_sm<P, CAP>();
+  const int64_t cap = (int64_t)sm_count() * blocks_per_sm<P, CAP, REALIGN>();
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, cap));
-  relay_pass_kernel<P, CAP><<<grid, kThreads, 0, stream>>>(a);
+  relay_pass_kernel<P, CAP, REALIGN><<<grid, kThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
-template <class P>
+template <class P, bool REALIGN>
 cudaError_t launch_typed(const std::vector<Seg>& segs, float scale, cudaStream_t stream) {
   constexpr int kMaxCap = 384;  // 16 + 384 * 80 bytes of parameters, under the 32 KiB limit
   size_t i = 0;
   while (i < segs.size()) {
     const int n = (int)std::min<size_t>(segs.size() - i, kMaxCap);
     cudaError_t e;
-    if (n <= 8) e = launch_cap<P, 8>(segs.data() + i, n, scale, stream);
-    else if (n <= 32) e = launch_cap<P, 32>(segs.data() + i, n, scale, stream);
-    else if (n <= 128) e = launch_cap<P, 128>(segs.data() + i, n, scale, stream);
-    else e = launch_cap<P, kMaxCap>(segs.data() + i, n, scale, stream);
+    if (n <= 8) e = launch_cap<P, 8, REALIGN>(segs.data() + i, n, scale, stream);
+    else if (n <= 32) e = launch_cap<P, 32, REALIGN>(segs.data() + i, n, scale, stream);
+    else if (n <= 128) e = launch_cap<P, 128, REALIGN>(segs.data() + i, n, scale, stream);
+    else e = launch_cap<P, kMaxCap, REALIGN>(segs.data() + i, n, scale, stream);
     if (e != cudaSuccess) return e;
     i += n;
   }
   return cudaSuccess;
 }
 
+template <class P>
+cudaError_t launch_split(const std::vector<Seg>& direct, const std::vector<Seg>& realigned,
+                         float scale, cudaStream_t stream) {
+  cudaError_t e = cudaSuccess;
+  if (!direct.empty()) e = launch_typed<P, false>(direct, scale, stream);
+  if (e == cudaSuccess && !realigned.empty()) e = launch_typed<P, true>(realigned, scale, stream);
+  return e;
+}
+
 }  // namespace
 
+// Segments with realigned sources go to their own launch after the others; the two
+// launches of such a pass touch disjoint memory, so their order does not matter.
 cudaError_t launch_pass(int dtype, const Pass& pass, float scale, cudaStream_t stream) {
-  static thread_local std::vector<Seg> segs;
+  static thread_local std::vector<Seg> segs, direct, realigned;
   split_for_alignment(pass.segs, esize_of(dtype), &segs);
-  if (segs.empty()) return cudaSuccess;
+  direct.clear();
+  realigned.clear();
+  for (const Seg& sg : segs) (sg.flags & kFlagRealign ? realigned : direct).push_back(sg);
   switch (dtype) {
-    case RELAY_F32: return launch_typed<TF32>(segs, scale, stream);
-    case RELAY_BF16: return launch_typed<TBF16>(segs, scale, stream);
-    default: return launch_typed<TI32>(segs, scale, stream);
+    case RELAY_F32: return launch_split<TF32>(direct, realigned, scale, stream);
+    case RELAY_BF16: return launch_split<TBF16>(direct, realigned, scale, stream);
+    default: return launch_split<TI32>(direct, realigned, scale, stream);
   }
 }
 

@@ -22,7 +22,7 @@ constexpr int kMaxSrc = 4;
 constexpr int kMaxDst = 4;
 
 enum SegOp : uint8_t { kOpCopy = 0, kOpReduce = 1 };
-enum SegFlag : uint8_t { kFlagScale = 1, kFlagVector = 2 };
+enum SegFlag : uint8_t { kFlagScale = 1, kFlagVector = 2, kFlagRealign = 4 };
 
 // Device-visible segment descriptor (kernel parameter space).
 struct Seg {

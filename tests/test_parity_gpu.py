@@ -217,3 +217,20 @@ def test_cuda_graph_capture_and_replay():
         torch.cuda.synchronize()
         for y, r in zip(c.recv, ref):
             assert np.array_equal(hz.host(y), r)
+
+
+@pytest.mark.parametrize("dtype", [rv.F32, rv.BF16, rv.I32])
+def test_realigned_sources_span_whole_tiles(dtype):
+    """Odd counts put sources at different offsets modulo 16 bytes from their
+    destinations over many whole tiles: the register-realigned vector path."""
+    cases = [(rv.ALL_TO_ALL, 4, 200_003), (rv.ALL_TO_ALL, 2, 300_001),
+             (rv.REDUCE_SCATTER, 2, 300_001), (rv.REDUCE_SCATTER, 4, 250_001),
+             (rv.ALL_GATHER, 4, 500_001), (rv.ALLREDUCE, 4, 1_000_001)]
+    for coll, A, count in cases:
+        scale = _scale(coll, A, dtype)
+        for in_place in (False, True):
+            if in_place and coll == rv.ALL_TO_ALL:
+                continue
+            c = hz.run(coll, A, 8, count, dtype, scale, config=13, schedule=rv.SCHEDULE_RELAY,
+                       in_place=in_place)
+            hz.check_all(c)
