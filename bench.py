@@ -344,8 +344,9 @@ def _sweep_points():
 
 
 def run_sweep(args):
-    """Per collective and count: each pass's time (CUDA events, L2 flushed before every
-    repetition), algorithmic bytes, GB/s and fraction of the measured HBM peak."""
+    """Per collective and count: each pass's time (CUDA events; before every repetition
+    a buffer twice the L2 is written and another read, so L2 holds no dirty lines),
+    algorithmic bytes, GB/s and fraction of the measured HBM peak."""
     import torch
     import pack_virtual_rank_gb300.build as b
     b.build()
@@ -358,6 +359,7 @@ def run_sweep(args):
     dts = {"f32": rv.F32, "bf16": rv.BF16, "i32": rv.I32}
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(2 * l2 // 4, dtype=torch.float32, device=dev)
+    flush_read = torch.ones(2 * l2 // 4, dtype=torch.float32, device=dev)
     rows = []
     for name, A, dt, nbytes, sched in _sweep_points():
         coll, d = colls[name], dts[dt]
@@ -385,11 +387,24 @@ def run_sweep(args):
         reps = args.steps
         times = [[] for _ in passes]
         totals = []
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(passes) + 1)]
+        o = rv.make_opts(schedule=opts0.schedule, pass_events=ev)
+        graph = None
+        if args.graph:
+            # the whole call, pass events included, replayed from a CUDA graph: no host
+            # launch gaps between the passes
+            s = torch.cuda.Stream()
+            torch.cuda.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=s):
+                call(o)
         for _ in range(reps):
             flush.fill_(1.0)
-            ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(passes) + 1)]
-            o = rv.make_opts(schedule=opts0.schedule, pass_events=ev)
-            call(o)
+            flush_read.sum()        # leaves clean lines in L2: no write-back inside the call
+            if graph is not None:
+                graph.replay()
+            else:
+                call(o)
             torch.cuda.synchronize()
             for i in range(len(passes)):
                 times[i].append(ev[i].elapsed_time(ev[i + 1]))
@@ -404,12 +419,13 @@ def run_sweep(args):
         tot_b = sum(p["bytes_read"] + p["bytes_written"] for p in passes)
         med = statistics.median(totals)
         row = {"collective": name, "A": A, "dtype": dt, "bytes_per_rank": nbytes, "count": count,
+               "timing": "cuda graph replay" if graph is not None else "direct calls",
                "schedule": ["relay", "zero_chunk", "direct", "legacy"][plan.kind],
                "ms_median": round(med, 4), "gbs": round(tot_b / med / 1e6, 1),
                "frac": round(tot_b / med / 1e6 / peak, 3), "passes": prow}
         rows.append(row)
         print(json.dumps(row), flush=True)
-        del xs, ys, scratch
+        del xs, ys, scratch, graph
         torch.cuda.empty_cache()
     if args.sweep_out:
         with open(args.sweep_out, "w") as f:
@@ -430,6 +446,8 @@ def main():
                     help="per-collective, per-count pass table of the five reference workloads "
                          "(not a bench line)")
     ap.add_argument("--sweep-out", default=None, help="write the sweep table as JSON here")
+    ap.add_argument("--graph", action="store_true",
+                    help="sweep: replay each call from a CUDA graph (device time without host gaps)")
     ap.add_argument("--kernel-only", action="store_true",
                     help="time the device passes only (no end-to-end leg, no CPU baseline)")
     args = ap.parse_args()

@@ -181,18 +181,25 @@ relay_status_t execute(const std::vector<Pass>& passes, const std::vector<Range>
   if (flags & RELAY_FLAG_DRY_RUN) return RELAY_OK;
 
   cudaEvent_t* events = nullptr;
+  unsigned record_flags = cudaEventRecordDefault;
   if (opts && opts->pass_events) {
     if (opts->n_pass_events < (int)passes.size() + 1)
       return fail(RELAY_ERR_INVALID_ARGUMENT, "pass_events holds fewer than passes + 1 events");
     events = static_cast<cudaEvent_t*>(opts->pass_events);
+    // under stream capture the records must become event nodes of the graph, so that
+    // the events can still be timed after a replay
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess)
+      return fail(RELAY_ERR_CUDA, "cudaStreamIsCapturing failed");
+    if (cs == cudaStreamCaptureStatusActive) record_flags = cudaEventRecordExternal;
   }
   for (size_t i = 0; i < passes.size(); ++i) {
-    if (events && cudaEventRecord(events[i], stream) != cudaSuccess)
+    if (events && cudaEventRecordWithFlags(events[i], stream, record_flags) != cudaSuccess)
       return fail(RELAY_ERR_CUDA, "cudaEventRecord failed");
     const cudaError_t e = launch_pass(dtype, passes[i], scale, stream);
     if (e != cudaSuccess) return fail(RELAY_ERR_CUDA, cudaGetErrorString(e));
   }
-  if (events && cudaEventRecord(events[passes.size()], stream) != cudaSuccess)
+  if (events && cudaEventRecordWithFlags(events[passes.size()], stream, record_flags) != cudaSuccess)
     return fail(RELAY_ERR_CUDA, "cudaEventRecord failed");
   return RELAY_OK;
 }

@@ -234,3 +234,21 @@ def test_realigned_sources_span_whole_tiles(dtype):
             c = hz.run(coll, A, 8, count, dtype, scale, config=13, schedule=rv.SCHEDULE_RELAY,
                        in_place=in_place)
             hz.check_all(c)
+
+
+def test_pass_events_inside_a_cuda_graph():
+    """Pass events recorded during stream capture time the passes of every replay."""
+    c = hz.run(rv.ALLREDUCE, 2, 8, 1 << 20, rv.BF16, 0.5, schedule=rv.SCHEDULE_RELAY)
+    npass = len(rv.relay_plan_passes(c.plan))
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(npass + 1)]
+    opts = rv.make_opts(schedule=rv.SCHEDULE_RELAY, pass_events=ev)
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        rv.relay_allreduce(c.send + [None] * 6, c.recv + [None] * 6, c.scratch, 1 << 20, rv.BF16,
+                           2, 8, 0.5, opts, stream=s)
+    g.replay()
+    torch.cuda.synchronize()
+    assert all(ev[i].elapsed_time(ev[i + 1]) > 0 for i in range(npass))
+    hz.check_all(c)
