@@ -36,7 +36,8 @@ A, R = 2, 8
 COUNT = 1 << 29              # elements per rank (bf16: 1 GiB)
 SCALE = 0.5
 WORKLOAD = "allreduce A=2 of R=8, bf16 (fp32 accumulate), 1 GiB per rank, scale 1/2"
-CPU_SAMPLE = 1 << 24         # elements per rank in one oracle sample
+CPU_SAMPLE = 1 << 24         # elements per rank in one step of the reference arm
+CPU_BASELINE_SAMPLE = 1 << 27  # elements per rank of the bench's own CPU-baseline leg
 PROFILE = os.path.join(ROOT, "profiles", "relay_pass_kernel_allreduce_a2_bf16_1g.md")
 KERNEL_SRC = os.path.join(ROOT, "pack_virtual_rank_gb300", "csrc", "passes.cu")
 
@@ -135,11 +136,15 @@ class Clocks:
                 "reasons": sorted(reasons)}
 
 
-def _cpu_oracle(sample: int, seed_config: int = 2):
-    """Time the oracle's allreduce on `sample` elements per rank (host cores)."""
+def _cpu_oracle(sample: int, seed_config: int = 2, inputs=None):
+    """Time the oracle's allreduce on `sample` elements per rank (host cores). `inputs`:
+    host copies of the workload's own inputs, of which the first `sample` are used."""
     import oracle as orc
     import synth
-    xs = [synth.to_numpy(synth.rank_input(seed_config, r, sample, "bf16")) for r in range(A)]
+    if inputs is None:
+        xs = [synth.to_numpy(synth.rank_input(seed_config, r, sample, "bf16")) for r in range(A)]
+    else:
+        xs = [synth.to_numpy(x[:sample]) for x in inputs]
     t0 = time.perf_counter()
     orc.allreduce(orc.BF16, xs, SCALE)
     return time.perf_counter() - t0
@@ -283,8 +288,9 @@ def run_ours(args):
         achieved = top_bytes / (per_pass[top] / 1e3) / 1e9
         traffic, _sha = _profiled_traffic()
         tr = traffic.get(passes[top]["name"]) if traffic else None
-        cpu_t = None if args.kernel_only else _cpu_oracle(CPU_SAMPLE)
-        cpu_bytes, _ = _bytes_per_step(plan, rv, CPU_SAMPLE)
+        sample = min(CPU_BASELINE_SAMPLE, count)
+        cpu_t = None if args.kernel_only else _cpu_oracle(sample, inputs=hx)
+        cpu_bytes, _ = _bytes_per_step(plan, rv, sample)
         cpu_val = cpu_bytes / cpu_t / 1e9 if cpu_t else None
         line = {
             "metric": "relay-pass HBM GB/s (allreduce A=2 of R=8, bf16)",
@@ -311,8 +317,9 @@ def run_ours(args):
                          "algorithmic_bytes_per_launch": top_bytes},
             "cpu_baseline": None if cpu_t is None else {
                 "value": round(cpu_val, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                "sample": f"oracle allreduce on {CPU_SAMPLE} elements per rank ({cpu_t:.2f} s); "
-                          "GB/s counts the relay schedule's algorithmic bytes for that count"},
+                "sample": f"oracle allreduce on the first {sample} elements of each rank's "
+                          f"bench input ({cpu_t:.2f} s); GB/s counts the relay schedule's "
+                          "algorithmic bytes for that count"},
             "e2e": None if e2e is None else {
                 "value": round(e2e, 2), "unit": "GB/s", "h2d_bytes_per_step": A * count * 2,
                 "d2h_bytes_per_step": A * count * 2},
@@ -340,6 +347,11 @@ def _sweep_points():
         for dt in ("bf16", "i32"):
             pts += [(coll, 4, dt, b, "relay") for b in
                     [int(13.5 * MB), 54 * MB, 135 * MB, 512 * MB, 1024 * MB]]
+    # the schedules the page retuned, executed for comparison: the three-group
+    # numChunks = H+1 schedule (item 1, before) and the 780-permille offload (item 4)
+    pts += [("allreduce", 2, "bf16", b, "legacy") for b in [64 * MB, 1024 * MB]]
+    pts += [("reduce_scatter", 2, "f32", b, "legacy") for b in [128 * MB, 512 * MB]]
+    pts += [("allreduce", 4, "bf16", b, "permille780") for b in [64 * MB, 1024 * MB]]
     return pts
 
 
@@ -367,7 +379,9 @@ def run_sweep(args):
         elems = nbytes // E
         count = {rv.ALLREDUCE: elems, rv.REDUCE_SCATTER: elems // A, rv.ALL_GATHER: elems,
                  rv.ALL_TO_ALL: elems // (A * (A - 1))}[coll]
-        opts0 = rv.make_opts(schedule=rv.SCHEDULE_RELAY if sched == "relay" else rv.SCHEDULE_AUTO)
+        opts0 = rv.make_opts(
+            schedule={"relay": rv.SCHEDULE_RELAY, "legacy": rv.SCHEDULE_LEGACY}.get(sched, rv.SCHEDULE_AUTO),
+            offload_permille=780 if sched == "permille780" else -1)
         plan = rv.relay_plan(coll, count, d, A, R, opts0)
         passes = rv.relay_plan_passes(plan)
         xs = [synth.rank_input(9, r, plan.input_elems, dt, device=dev) for r in range(A)]
@@ -388,7 +402,8 @@ def run_sweep(args):
         times = [[] for _ in passes]
         totals = []
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(passes) + 1)]
-        o = rv.make_opts(schedule=opts0.schedule, pass_events=ev)
+        o = rv.make_opts(schedule=opts0.schedule, offload_permille=opts0.offload_permille,
+                         pass_events=ev)
         graph = None
         if args.graph:
             # the whole call, pass events included, replayed from a CUDA graph: no host
@@ -420,7 +435,9 @@ def run_sweep(args):
         med = statistics.median(totals)
         row = {"collective": name, "A": A, "dtype": dt, "bytes_per_rank": nbytes, "count": count,
                "timing": "cuda graph replay" if graph is not None else "direct calls",
-               "schedule": ["relay", "zero_chunk", "direct", "legacy"][plan.kind],
+               "schedule": ["relay", "zero_chunk", "direct", "legacy"][plan.kind] +
+                           (" 780 permille" if sched == "permille780" else ""),
+               "link_cost_bytes": rv.relay_plan_cost_bytes(plan),
                "ms_median": round(med, 4), "gbs": round(tot_b / med / 1e6, 1),
                "frac": round(tot_b / med / 1e6 / peak, 3), "passes": prow}
         rows.append(row)

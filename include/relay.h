@@ -80,7 +80,8 @@ typedef enum {
 #define RELAY_FLAG_DRY_RUN 2       /* validate, plan, build and check; launch nothing */
 
 typedef struct relay_opts {
-  int32_t offload_permille;      /* A=4 allreduce / reduce-scatter offload share; <0: 500 (item 4) */
+  int32_t offload_permille;      /* A=4 allreduce / reduce-scatter / all-gather offload share;
+                                    <0: 500 (item 4) */
   int32_t schedule;              /* relay_schedule_t */
   int64_t relay_threshold_bytes; /* <0: per-collective default crossover (items 3, 4, 7) */
   void* pass_events;             /* NULL, or cudaEvent_t[n_pass_events]: event i is recorded on

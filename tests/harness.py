@@ -154,15 +154,20 @@ def check_window(c, rank, i0, i1, xs_host):
     # identical arithmetic order as the oracle: bit-exact
     assert np.array_equal(got, q), _first_diff(got, q, i0)
     if c.dtype == rv.F32:
-        # fp32 criterion: relative error <= 1e-6 against the fp64-accumulated sum, where
-        # the sum is not a cancellation below fp32 resolution of the terms
-        mag = np.zeros_like(r64)
-        for x in xs_host:
-            mag += np.abs(_window_terms(c, x, rank, i0, i1).astype(np.float64))
-        mag *= abs(c.scale)
+        # fp32 criterion: relative error <= 1e-6 against the fp64-accumulated sum. Two
+        # terms round once, so this holds for every element at A=2. With more terms a
+        # cancelling sum can defeat any fixed relative bound, so there the bound also
+        # admits the recursive-summation error (A-1) * 2^-24 * sum|x|.
         err = np.abs(got.astype(np.float64) - r64)
-        bound = np.maximum(1e-6 * np.abs(r64), (c.A - 1) * 2.0 ** -24 * mag)
-        assert np.all(err <= bound), "fp32 tolerance"
+        if c.A == 2:
+            assert np.all(err <= 1e-6 * np.abs(r64)), "fp32 relative error above 1e-6"
+        else:
+            mag = np.zeros_like(r64)
+            for x in xs_host:
+                mag += np.abs(_window_terms(c, x, rank, i0, i1).astype(np.float64))
+            mag *= abs(c.scale)
+            bound = np.maximum(1e-6 * np.abs(r64), (c.A - 1) * 2.0 ** -24 * mag)
+            assert np.all(err <= bound), "fp32 tolerance"
     else:
         g = orc.bf16_to_f32(got).astype(np.float64)
         assert np.all(np.abs(g - r32.astype(np.float64)) <= bf16_ulp(r32)), "bf16 1-ulp bound"
