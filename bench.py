@@ -424,6 +424,33 @@ def run_sweep(args):
             for i in range(len(passes)):
                 times[i].append(ev[i].elapsed_time(ev[i + 1]))
             totals.append(ev[0].elapsed_time(ev[-1]))
+        # the whole call under the library's default launch policy (one cooperative
+        # launch for small calls), timed around the call
+        whole = []
+        if not args.graph:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            for _ in range(reps):
+                flush.fill_(1.0)
+                flush_read.sum()
+                e0.record()
+                call(opts0)
+                e1.record()
+                torch.cuda.synchronize()
+                whole.append(e0.elapsed_time(e1))
+        # the same with the one-launch path forced at every size
+        fused = []
+        if not args.graph:
+            of = rv.make_opts(schedule=opts0.schedule, offload_permille=opts0.offload_permille,
+                              flags=rv.FLAG_FUSED_PASSES)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            for _ in range(reps):
+                flush.fill_(1.0)
+                flush_read.sum()
+                e0.record()
+                call(of)
+                e1.record()
+                torch.cuda.synchronize()
+                fused.append(e0.elapsed_time(e1))
         prow = []
         for p, t in zip(passes, times):
             by = p["bytes_read"] + p["bytes_written"]
@@ -440,6 +467,15 @@ def run_sweep(args):
                "link_cost_bytes": rv.relay_plan_cost_bytes(plan),
                "ms_median": round(med, 4), "gbs": round(tot_b / med / 1e6, 1),
                "frac": round(tot_b / med / 1e6 / peak, 3), "passes": prow}
+        if fused:
+            fm = statistics.median(fused)
+            row.update({"ms_call_fused_forced": round(fm, 4),
+                        "frac_call_fused_forced": round(tot_b / fm / 1e6 / peak, 3)})
+        if whole:
+            wm = statistics.median(whole)
+            row.update({"ms_call_default_policy": round(wm, 4),
+                        "gbs_call_default_policy": round(tot_b / wm / 1e6, 1),
+                        "frac_call_default_policy": round(tot_b / wm / 1e6 / peak, 3)})
         rows.append(row)
         print(json.dumps(row), flush=True)
         del xs, ys, scratch, graph

@@ -78,6 +78,14 @@ typedef enum {
                                       inside a declared buffer, and no launch writes what
                                       another segment of it reads or writes (O(segs^2)) */
 #define RELAY_FLAG_DRY_RUN 2       /* validate, plan, build and check; launch nothing */
+#define RELAY_FLAG_SEPARATE_PASSES 4 /* one launch per pass even for small calls */
+#define RELAY_FLAG_FUSED_PASSES 8  /* one cooperative launch for the whole call whenever it
+                                      qualifies, whatever its size */
+/* Launch policy: a call of at most RELAY_FUSED_MAX_BYTES of pass traffic that has at most
+ * 4 passes and 128 segments, needs no realigned sources and records no pass events runs
+ * as ONE cooperative launch whose passes are separated by grid-wide barriers; any other
+ * call launches each pass separately. */
+#define RELAY_FUSED_MAX_BYTES (64ll << 20)
 
 typedef struct relay_opts {
   int32_t offload_permille;      /* A=4 allreduce / reduce-scatter / all-gather offload share;

@@ -23,6 +23,8 @@ KIND_RELAY, KIND_ZERO_CHUNK, KIND_DIRECT, KIND_LEGACY = 0, 1, 2, 3
 SCHEDULE_AUTO, SCHEDULE_RELAY, SCHEDULE_DIRECT, SCHEDULE_LEGACY = 0, 1, 2, 3
 FLAG_CHECK_HAZARDS = 1
 FLAG_DRY_RUN = 2
+FLAG_SEPARATE_PASSES = 4
+FLAG_FUSED_PASSES = 8
 ESIZE = {F32: 4, BF16: 2, I32: 4}
 PASS_NAMES = ("group1", "group2", "group3", "active_reduce", "pack", "helper_forward", "unpack")
 

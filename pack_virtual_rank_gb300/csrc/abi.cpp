@@ -180,6 +180,21 @@ relay_status_t execute(const std::vector<Pass>& passes, const std::vector<Range>
     }
   if (flags & RELAY_FLAG_DRY_RUN) return RELAY_OK;
 
+  // small calls: the whole call in one cooperative launch (no pass events there)
+  const bool events_wanted = opts && opts->pass_events;
+  if (!events_wanted && !(flags & RELAY_FLAG_SEPARATE_PASSES)) {
+    int64_t bytes = 0;
+    for (const Pass& ps : passes)
+      for (const Seg& sg : ps.segs) bytes += sg.n * E * (sg.nsrc + sg.ndst);
+    if ((flags & RELAY_FLAG_FUSED_PASSES) || bytes <= RELAY_FUSED_MAX_BYTES) {
+      cudaError_t e = cudaSuccess;
+      if (launch_fused(dtype, passes, scale, stream, &e)) {
+        if (e != cudaSuccess) return fail(RELAY_ERR_CUDA, cudaGetErrorString(e));
+        return RELAY_OK;
+      }
+    }
+  }
+
   cudaEvent_t* events = nullptr;
   unsigned record_flags = cudaEventRecordDefault;
   if (opts && opts->pass_events) {

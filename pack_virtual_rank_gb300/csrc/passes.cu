@@ -12,6 +12,7 @@
 // scales once, rounds to nearest-even into the payload type and stores the result to
 // each destination. Copies move raw 16-byte vectors. Segments whose pointers are not
 // 16-byte aligned (after a host-side prologue split) take a per-element path.
+#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -33,27 +34,57 @@ struct PassArgs {
 
 // ---------------------------------------------------------------- memory access --
 
-__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
-  uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-      : "l"(p));
-  return r;
-}
+// Loads. The per-pass kernels read only what earlier launches wrote, so they use the
+// non-coherent path without allocating in L1. The fused small-call kernel reads, after a
+// grid barrier, what other CTAs of the same launch wrote: it loads through L2 only
+// (.cg), which is coherent across SMs.
+template <bool COH>
+struct Mem;
+template <>
+struct Mem<false> {
+  static __device__ __forceinline__ uint4 v4(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+  }
+  static __device__ __forceinline__ uint32_t u32(const void* p) {
+    uint32_t r;
+    asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(r) : "l"(p));
+    return r;
+  }
+  static __device__ __forceinline__ uint16_t u16(const void* p) {
+    uint16_t r;
+    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(r) : "l"(p));
+    return r;
+  }
+};
+template <>
+struct Mem<true> {
+  static __device__ __forceinline__ uint4 v4(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+  }
+  static __device__ __forceinline__ uint32_t u32(const void* p) {
+    uint32_t r;
+    asm volatile("ld.global.cg.u32 %0, [%1];" : "=r"(r) : "l"(p));
+    return r;
+  }
+  static __device__ __forceinline__ uint16_t u16(const void* p) {
+    uint16_t r;
+    asm volatile("ld.global.cg.u16 %0, [%1];" : "=h"(r) : "l"(p));
+    return r;
+  }
+};
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) { return Mem<false>::v4(p); }
 __device__ __forceinline__ void st_v4(void* p, uint4 v) {
   asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
                "r"(v.w)
                : "memory");
-}
-__device__ __forceinline__ uint32_t ld_u32(const void* p) {
-  uint32_t r;
-  asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(r) : "l"(p));
-  return r;
-}
-__device__ __forceinline__ uint16_t ld_u16(const void* p) {
-  uint16_t r;
-  asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(r) : "l"(p));
-  return r;
 }
 __device__ __forceinline__ void st_u32(void* p, uint32_t v) {
   asm volatile("st.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
@@ -85,7 +116,10 @@ struct TF32 {
   }
   static __device__ __forceinline__ float add(float x, float y) { return __fadd_rn(x, y); }
   static __device__ __forceinline__ float scale(float x, float s) { return __fmul_rn(x, s); }
-  static __device__ __forceinline__ float load1(const void* p) { return __uint_as_float(ld_u32(p)); }
+  template <bool COH>
+  static __device__ __forceinline__ float load1(const void* p) {
+    return __uint_as_float(Mem<COH>::u32(p));
+  }
   static __device__ __forceinline__ void store1(void* p, float v) { st_u32(p, __float_as_uint(v)); }
 };
 
@@ -106,8 +140,9 @@ struct TBF16 {
   }
   static __device__ __forceinline__ float add(float x, float y) { return __fadd_rn(x, y); }
   static __device__ __forceinline__ float scale(float x, float s) { return __fmul_rn(x, s); }
+  template <bool COH>
   static __device__ __forceinline__ float load1(const void* p) {
-    return __uint_as_float((uint32_t)ld_u16(p) << 16);
+    return __uint_as_float((uint32_t)Mem<COH>::u16(p) << 16);
   }
   static __device__ __forceinline__ void store1(void* p, float v) {
     st_u16(p, (uint16_t)(bf16x2_rn(v, 0.0f) & 0xffffu));
@@ -125,7 +160,8 @@ struct TI32 {
   }
   static __device__ __forceinline__ uint32_t add(uint32_t x, uint32_t y) { return x + y; }
   static __device__ __forceinline__ uint32_t scale(uint32_t x, float) { return x; }
-  static __device__ __forceinline__ uint32_t load1(const void* p) { return ld_u32(p); }
+  template <bool COH>
+  static __device__ __forceinline__ uint32_t load1(const void* p) { return Mem<COH>::u32(p); }
   static __device__ __forceinline__ void store1(void* p, uint32_t v) { st_u32(p, v); }
 };
 
@@ -134,7 +170,7 @@ struct TI32 {
 // Whole tile on the 16-byte vector path: every thread loads kUnroll vectors per
 // source (in batches that keep at most 8 loads in flight per thread), reduces and
 // stores them. base is the tile's first element.
-template <class P, int NSRC>
+template <class P, int NSRC, bool COH>
 __device__ __forceinline__ void reduce_full_tile(const Seg& s, int64_t base, float scale) {
   constexpr int L = P::kLanes;
   constexpr int UB = NSRC <= 2 ? kUnroll : kUnroll / 2;
@@ -148,7 +184,7 @@ __device__ __forceinline__ void reduce_full_tile(const Seg& s, int64_t base, flo
     for (int u = 0; u < UB; ++u)
 #pragma unroll
       for (int k = 0; k < NSRC; ++k)
-        v[k][u] = ld_stream_v4(static_cast<const uint4*>(s.src[k]) + v0 + (u0 + u) * kThreads);
+        v[k][u] = Mem<COH>::v4(static_cast<const uint4*>(s.src[k]) + v0 + (u0 + u) * kThreads);
 #pragma unroll
     for (int u = 0; u < UB; ++u) {
       Acc acc[L], t[L];
@@ -171,12 +207,13 @@ __device__ __forceinline__ void reduce_full_tile(const Seg& s, int64_t base, flo
   }
 }
 
+template <bool COH>
 __device__ __forceinline__ void copy_full_tile(const Seg& s, int64_t vbase) {
   const int64_t v0 = vbase + threadIdx.x;
   uint4 v[kUnroll];
 #pragma unroll
   for (int u = 0; u < kUnroll; ++u)
-    v[u] = ld_stream_v4(static_cast<const uint4*>(s.src[0]) + v0 + u * kThreads);
+    v[u] = Mem<COH>::v4(static_cast<const uint4*>(s.src[0]) + v0 + u * kThreads);
 #pragma unroll
   for (int u = 0; u < kUnroll; ++u)
 #pragma unroll
@@ -184,17 +221,17 @@ __device__ __forceinline__ void copy_full_tile(const Seg& s, int64_t vbase) {
       if (d < s.ndst) st_v4(static_cast<uint4*>(s.dst[d]) + v0 + u * kThreads, v[u]);
 }
 
-template <class P>
+template <class P, bool COH>
 __device__ __forceinline__ void run_full_tile(const Seg& s, int64_t base, float scale) {
   if (s.op == kOpCopy) {
-    copy_full_tile(s, base / P::kLanes);
+    copy_full_tile<COH>(s, base / P::kLanes);
     return;
   }
   switch (s.nsrc) {
-    case 1: reduce_full_tile<P, 1>(s, base, scale); break;
-    case 2: reduce_full_tile<P, 2>(s, base, scale); break;
-    case 3: reduce_full_tile<P, 3>(s, base, scale); break;
-    default: reduce_full_tile<P, 4>(s, base, scale); break;
+    case 1: reduce_full_tile<P, 1, COH>(s, base, scale); break;
+    case 2: reduce_full_tile<P, 2, COH>(s, base, scale); break;
+    case 3: reduce_full_tile<P, 3, COH>(s, base, scale); break;
+    default: reduce_full_tile<P, 4, COH>(s, base, scale); break;
   }
 }
 
@@ -310,7 +347,7 @@ __device__ __forceinline__ void run_realign_tile(const Seg& s, int64_t base, flo
 // The last, partial tile of a segment and every tile of a segment whose pointers are
 // not 16-byte aligned: one vector (or one element) per source at a time, with the
 // source count read at run time. Rare, so it is kept small rather than fast.
-template <class P>
+template <class P, bool COH>
 __device__ __noinline__ void run_partial_tile(const Seg& s, int64_t base, int64_t len,
                                               float scale) {
   using Acc = typename P::Acc;
@@ -322,13 +359,13 @@ __device__ __noinline__ void run_partial_tile(const Seg& s, int64_t base, int64_
     const int64_t vb = base / L, nvec = len / L;
 #pragma unroll 1
     for (int64_t vi = threadIdx.x; vi < nvec; vi += kThreads) {
-      uint4 r = ld_stream_v4(static_cast<const uint4*>(s.src[0]) + vb + vi);
+      uint4 r = Mem<COH>::v4(static_cast<const uint4*>(s.src[0]) + vb + vi);
       if (!copy) {
         Acc acc[L], t[L];
         P::unpack(r, acc);
 #pragma unroll 1
         for (int k = 1; k < s.nsrc; ++k) {
-          P::unpack(ld_stream_v4(static_cast<const uint4*>(s.src[k]) + vb + vi), t);
+          P::unpack(Mem<COH>::v4(static_cast<const uint4*>(s.src[k]) + vb + vi), t);
 #pragma unroll
           for (int i = 0; i < L; ++i) acc[i] = P::add(acc[i], t[i]);
         }
@@ -348,20 +385,20 @@ __device__ __noinline__ void run_partial_tile(const Seg& s, int64_t base, int64_
     const int64_t off = (base + e) * P::kE;
     if (copy) {
       if (P::kE == 4) {
-        const uint32_t x = ld_u32(static_cast<const char*>(s.src[0]) + off);
+        const uint32_t x = Mem<COH>::u32(static_cast<const char*>(s.src[0]) + off);
 #pragma unroll 1
         for (int d = 0; d < s.ndst; ++d) st_u32(static_cast<char*>(s.dst[d]) + off, x);
       } else {
-        const uint16_t x = ld_u16(static_cast<const char*>(s.src[0]) + off);
+        const uint16_t x = Mem<COH>::u16(static_cast<const char*>(s.src[0]) + off);
 #pragma unroll 1
         for (int d = 0; d < s.ndst; ++d) st_u16(static_cast<char*>(s.dst[d]) + off, x);
       }
       continue;
     }
-    Acc acc = P::load1(static_cast<const char*>(s.src[0]) + off);
+    Acc acc = P::template load1<COH>(static_cast<const char*>(s.src[0]) + off);
 #pragma unroll 1
     for (int k = 1; k < s.nsrc; ++k)
-      acc = P::add(acc, P::load1(static_cast<const char*>(s.src[k]) + off));
+      acc = P::add(acc, P::template load1<COH>(static_cast<const char*>(s.src[k]) + off));
     if (do_scale) acc = P::scale(acc, scale);
 #pragma unroll 1
     for (int d = 0; d < s.ndst; ++d) P::store1(static_cast<char*>(s.dst[d]) + off, acc);
@@ -386,9 +423,46 @@ __global__ void __launch_bounds__(kThreads, 5)
     const Seg& s = args.seg[lo];
     const int64_t base = (int64_t)(t - s.tile0) * kTile;
     const int64_t len = min(kTile, s.n - base);
-    if (!REALIGN && (s.flags & kFlagVector) && len == kTile) run_full_tile<P>(s, base, args.scale);
+    if (!REALIGN && (s.flags & kFlagVector) && len == kTile) run_full_tile<P, false>(s, base, args.scale);
     else if (REALIGN && len == kTile) run_realign_tile<P>(s, base, args.scale);
-    else run_partial_tile<P>(s, base, len, args.scale);
+    else run_partial_tile<P, false>(s, base, len, args.scale);
+  }
+}
+
+// ----------------------------------------------------- fused small-call kernel --
+// A whole call in one cooperative launch: the passes run one after another, separated
+// by grid-wide barriers (every CTA takes part in every barrier: the pass loop is
+// uniform). For calls small enough that the fixed cost of a launch per pass dominates.
+
+constexpr int kMaxFusedPasses = 4;
+constexpr int kFusedCap = 128;
+
+struct FusedArgs {
+  int32_t npass;
+  float scale;
+  int32_t seg0[kMaxFusedPasses + 1];  // segments of pass p: [seg0[p], seg0[p+1])
+  int32_t ntiles[kMaxFusedPasses];
+  Seg seg[kFusedCap];                  // tile0 counts from the start of its pass
+};
+
+template <class P>
+__global__ void __launch_bounds__(kThreads, 5) relay_fused_kernel(const __grid_constant__ FusedArgs args) {
+  namespace cg = cooperative_groups;
+  constexpr int64_t kTile = kTileBytes / P::kE;
+  for (int p = 0; p < args.npass; ++p) {
+    for (int t = blockIdx.x; t < args.ntiles[p]; t += gridDim.x) {
+      int lo = args.seg0[p], hi = args.seg0[p + 1] - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (args.seg[mid].tile0 <= t) lo = mid; else hi = mid - 1;
+      }
+      const Seg& s = args.seg[lo];
+      const int64_t base = (int64_t)(t - s.tile0) * kTile;
+      const int64_t len = min(kTile, s.n - base);
+      if ((s.flags & kFlagVector) && len == kTile) run_full_tile<P, true>(s, base, args.scale);
+      else run_partial_tile<P, true>(s, base, len, args.scale);
+    }
+    if (p + 1 < args.npass) cg::this_grid().sync();
   }
 }
 
@@ -504,7 +578,79 @@ cudaError_t launch_split(const std::vector<Seg>& direct, const std::vector<Seg>&
   return e;
 }
 
+template <class P>
+int fused_blocks_per_sm() {
+  static int cached = 0;
+  if (cached == 0) {
+    int nb = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, relay_fused_kernel<P>, kThreads, 0) !=
+            cudaSuccess ||
+        nb <= 0)
+      nb = 1;
+    cached = nb;
+  }
+  return cached;
+}
+
+bool cooperative_supported() {
+  static int cached[RELAY_MAX_RANKS] = {0};  // 0 unknown, 1 yes, 2 no
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= RELAY_MAX_RANKS) return false;
+  if (cached[dev] == 0) {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrCooperativeLaunch, dev);
+    cached[dev] = v ? 1 : 2;
+  }
+  return cached[dev] == 1;
+}
+
+template <class P>
+cudaError_t launch_fused_typed(FusedArgs& a, int max_tiles, cudaStream_t stream) {
+  const int64_t cap = (int64_t)sm_count() * fused_blocks_per_sm<P>();
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(max_tiles, cap));
+  void* params[] = {&a};
+  cudaError_t e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(relay_fused_kernel<P>),
+                                              dim3(grid), dim3(kThreads), params, 0, stream);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 }  // namespace
+
+bool launch_fused(int dtype, const std::vector<Pass>& passes, float scale, cudaStream_t stream,
+                  cudaError_t* err) {
+  *err = cudaSuccess;
+  if (passes.size() < 2 || passes.size() > (size_t)kMaxFusedPasses || !cooperative_supported())
+    return false;
+  static thread_local FusedArgs a;
+  static thread_local std::vector<Seg> segs;
+  const int E = esize_of(dtype);
+  const int64_t tile = kTileBytes / E;
+  int n = 0, max_tiles = 0;
+  a.npass = (int32_t)passes.size();
+  a.scale = scale;
+  for (size_t p = 0; p < passes.size(); ++p) {
+    split_for_alignment(passes[p].segs, E, &segs);
+    a.seg0[p] = n;
+    int64_t tiles = 0;
+    for (const Seg& sg : segs) {
+      if ((sg.flags & kFlagRealign) || n >= kFusedCap) return false;
+      a.seg[n] = sg;
+      a.seg[n].tile0 = (int32_t)tiles;
+      tiles += (sg.n + tile - 1) / tile;
+      ++n;
+    }
+    if (tiles > INT32_MAX) return false;
+    a.ntiles[p] = (int32_t)tiles;
+    max_tiles = std::max<int>(max_tiles, (int)tiles);
+  }
+  a.seg0[passes.size()] = n;
+  switch (dtype) {
+    case RELAY_F32: *err = launch_fused_typed<TF32>(a, max_tiles, stream); break;
+    case RELAY_BF16: *err = launch_fused_typed<TBF16>(a, max_tiles, stream); break;
+    default: *err = launch_fused_typed<TI32>(a, max_tiles, stream); break;
+  }
+  return true;
+}
 
 // Segments with realigned sources go to their own launch after the others; the two
 // launches of such a pass touch disjoint memory, so their order does not matter.

@@ -77,6 +77,13 @@ void build_multi_program(const std::vector<relay_plan_t>& plans, const std::vect
 // segment table exceeds one launch's parameter capacity.
 cudaError_t launch_pass(int dtype, const Pass& pass, float scale, cudaStream_t stream);
 
+// Launch every pass of a small call as one cooperative kernel with grid barriers between
+// the passes -- passes.cu. Returns false (and launches nothing) when the call does not
+// qualify: more than 4 passes, more than 128 segments, a segment needing realigned
+// sources, or no cooperative launch on this device.
+bool launch_fused(int dtype, const std::vector<Pass>& passes, float scale, cudaStream_t stream,
+                  cudaError_t* err);
+
 // Record `msg` as this thread's last error and return `st` -- abi.cpp.
 relay_status_t report_error(relay_status_t st, const std::string& msg);
 

@@ -56,9 +56,9 @@ class Call:
 
 def run(coll, A, R, count, dtype, scale=1.0, config=0, schedule=rv.SCHEDULE_AUTO,
         in_place=False, permille=-1, device="cuda", gpu_generator=False, check_hazards=True,
-        inputs=None):
+        inputs=None, flags=0):
     opts = rv.make_opts(offload_permille=permille, schedule=schedule,
-                        flags=rv.FLAG_CHECK_HAZARDS if check_hazards else 0)
+                        flags=flags | (rv.FLAG_CHECK_HAZARDS if check_hazards else 0))
     plan = rv.relay_plan(coll, count, dtype, A, R, opts)
     c = Call()
     c.plan, c.coll, c.A, c.R, c.count, c.dtype, c.scale = plan, coll, A, R, count, dtype, scale

@@ -33,9 +33,11 @@ def _scale(coll, A, dtype):
 @pytest.mark.parametrize("dtype", [rv.F32, rv.BF16, rv.I32])
 @pytest.mark.parametrize("A", [2, 4])
 @pytest.mark.parametrize("coll", [rv.ALLREDUCE, rv.REDUCE_SCATTER, rv.ALL_GATHER, rv.ALL_TO_ALL])
-def test_small_sizes_every_schedule(coll, A, dtype):
+@pytest.mark.parametrize("launch", [0, rv.FLAG_SEPARATE_PASSES])
+def test_small_sizes_every_schedule(coll, A, dtype, launch):
     """Every count around the 128-element alignment and chunk boundaries, every
-    schedule, R = A+1 (one helper) and R = 8, in-place and out-of-place."""
+    schedule, R = A+1 (one helper) and R = 8, in-place and out-of-place; small calls run
+    as one cooperative launch by default and pass by pass when asked."""
     n = 0
     for R in (A + 1, 8):
         for count in SMALL_COUNTS:
@@ -51,7 +53,7 @@ def test_small_sizes_every_schedule(coll, A, dtype):
                         assert sched == rv.SCHEDULE_LEGACY   # chunk aligns down to 0
                         continue
                     c = hz.run(coll, A, R, count, dtype, _scale(coll, A, dtype), config=7,
-                               schedule=sched, in_place=in_place)
+                               schedule=sched, in_place=in_place, flags=launch)
                     hz.check_all(c)
                     n += 1
     assert n > 50
@@ -252,3 +254,15 @@ def test_pass_events_inside_a_cuda_graph():
     torch.cuda.synchronize()
     assert all(ev[i].elapsed_time(ev[i + 1]) > 0 for i in range(npass))
     hz.check_all(c)
+
+
+@pytest.mark.parametrize("coll", [rv.ALLREDUCE, rv.REDUCE_SCATTER, rv.ALL_GATHER, rv.ALL_TO_ALL])
+def test_fused_launch_at_sizes_past_its_default(coll):
+    """The one-launch path forced on calls of many tiles per pass (grid barriers between
+    passes; loads through L2) matches the oracle like the per-pass path."""
+    for A in (2, 4):
+        for count in (3 << 20, (1 << 21) + 129):
+            scale = _scale(coll, A, rv.BF16)
+            c = hz.run(coll, A, 8, count, rv.BF16, scale, config=17,
+                       schedule=rv.SCHEDULE_RELAY, flags=rv.FLAG_FUSED_PASSES)
+            hz.check_all(c)
