@@ -183,6 +183,20 @@ typedef struct relay_pass_info {
 int relay_plan_passes(const relay_plan_t* plan, int in_place, relay_pass_info_t* out, int cap);
 const char* relay_pass_name(int kind);
 
+/* Scratch sizes of a plan, in elements (the plan's helper_elems / active_scratch_elems):
+ * what each helper and each active must be given for this schedule. */
+int64_t relay_helper_size(const relay_plan_t* plan);
+int64_t relay_active_scratch_size(const relay_plan_t* plan);
+
+/* The page's helper-buffer contract for one group (what its distributed layer
+ * allocates per helper), in elements: the passthrough size with num_chunks = (R-A)+1 at
+ * A=2 (D115998370); 2*count for the 4-active allreduce (D115998382) and reduce-scatter
+ * (item 6); A*count for the 4-active all-gather (D115998397); 1 for the 4-active
+ * all-to-all, which the page runs pure-direct (D115998358). -1 on bad arguments. This
+ * library's schedules never need more than the contract, except the coalesced 4-active
+ * all-to-all, which the page does not have. */
+int64_t relay_helper_contract_size(relay_coll_t coll, int64_t count, int A, int R);
+
 /* Helper-buffer size contract of the page's distributed layer (D115998394, D115998388,
  * D115998370): min(count_g, A * align_down(count_g / num_chunks, 128)); count_g when the
  * aligned chunk is 0 (the page only says the fallback can over-allocate). */

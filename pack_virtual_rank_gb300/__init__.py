@@ -15,4 +15,5 @@ from ._binding import (  # noqa: F401
     relay_passthrough_helper_size, relay_plan, relay_plan_cost_bytes, relay_plan_link_bytes,
     relay_plan_passes, relay_reduce_scatter, group_ranks, relay_multi_group,
     relay_multi_group_link_bytes, alloc_multi_scratch, relay_pack_flat, relay_unpack_flat,
-    relay_allreduce_noalloc)
+    relay_allreduce_noalloc, relay_helper_size, relay_active_scratch_size,
+    relay_helper_contract_size)

@@ -105,6 +105,12 @@ def lib():
     L.relay_multi_group_link_bytes.argtypes = [i32, i32, P(sz), i32, i32, P(RelayOpts),
                                                P(ctypes.c_uint64), sz, P(ctypes.c_int)]
     L.relay_multi_group_link_bytes.restype = i32
+    L.relay_helper_size.argtypes = [P(RelayPlan)]
+    L.relay_helper_size.restype = i64
+    L.relay_active_scratch_size.argtypes = [P(RelayPlan)]
+    L.relay_active_scratch_size.restype = i64
+    L.relay_helper_contract_size.argtypes = [i32, i64, i32, i32]
+    L.relay_helper_contract_size.restype = i64
     L.relay_allreduce_noalloc.argtypes = [arr, arr, sz, i32, i32, i32, f32, P(RelayOpts), vp]
     L.relay_allreduce_noalloc.restype = i32
     L.relay_pack_flat.argtypes = [arr, P(sz), i32, vp, i32, vp]
@@ -189,6 +195,18 @@ def relay_plan_passes(plan: RelayPlan, in_place: bool = False) -> list:
 
 def relay_passthrough_helper_size(count_g: int, A: int, num_chunks: int) -> int:
     return int(lib().relay_passthrough_helper_size(count_g, A, num_chunks))
+
+
+def relay_helper_size(plan: RelayPlan) -> int:
+    return int(lib().relay_helper_size(ctypes.byref(plan)))
+
+
+def relay_active_scratch_size(plan: RelayPlan) -> int:
+    return int(lib().relay_active_scratch_size(ctypes.byref(plan)))
+
+
+def relay_helper_contract_size(coll: int, count: int, A: int, R: int) -> int:
+    return int(lib().relay_helper_contract_size(coll, count, A, R))
 
 
 def relay_pass_name(kind: int) -> str:

@@ -398,6 +398,24 @@ const char* relay_pass_name(int kind) {
   }
 }
 
+int64_t relay_helper_size(const relay_plan_t* plan) { return plan ? plan->helper_elems : -1; }
+
+int64_t relay_active_scratch_size(const relay_plan_t* plan) {
+  return plan ? plan->active_scratch_elems : -1;
+}
+
+int64_t relay_helper_contract_size(relay_coll_t coll, int64_t count, int A, int R) {
+  if (count < 0 || (A != 2 && A != 4) || R <= A || coll < RELAY_ALLREDUCE || coll > RELAY_ALL_TO_ALL)
+    return -1;
+  if (A == 2) return relay_passthrough_helper_size(count, A, (R - A) + 1);
+  switch (coll) {
+    case RELAY_ALLREDUCE:
+    case RELAY_REDUCE_SCATTER: return 2 * count;
+    case RELAY_ALL_GATHER: return (int64_t)A * count;
+    default: return 1;
+  }
+}
+
 // D115998394, D115998388, D115998370: A slots, each a whole number of 128-element
 // chunks, never more than the group count itself
 int64_t relay_passthrough_helper_size(int64_t count_g, int A, int num_chunks) {

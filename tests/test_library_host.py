@@ -416,3 +416,17 @@ def test_flat_pack_validation():
         == rv.ERR_INVALID_ARGUMENT
     # empty list: nothing to do
     assert rv.lib().relay_pack_flat(arr([None]), c, 0, None, 0, None) == rv.OK
+
+
+def test_size_queries_and_page_contract(orc):
+    for coll in range(4):
+        for A in (2, 4):
+            for R in (A + 1, 8, 12):
+                for count in (0, 100, 1024, 896_000, 12_002_982_488 // 1024, 12_002_982_488):
+                    assert rv.relay_helper_contract_size(coll, count, A, R) == \
+                        orc.relay_helper_contract(coll, A, R, count)
+                    if count < (1 << 31):
+                        p = rv.relay_plan(coll, count, rv.BF16, A, R)
+                        assert rv.relay_helper_size(p) == p.helper_elems
+                        assert rv.relay_active_scratch_size(p) == p.active_scratch_elems
+    assert rv.relay_helper_contract_size(0, 10, 3, 8) == -1
