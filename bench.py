@@ -400,6 +400,23 @@ def run_sweep(args):
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(2 * l2 // 4, dtype=torch.float32, device=dev)
     flush_read = torch.ones(2 * l2 // 4, dtype=torch.float32, device=dev)
+    # the achievable copy rate on this device in this run, for reference: a 1 GiB bf16
+    # device-to-device copy, best of 5, read + written bytes
+    src = torch.ones(1 << 29, dtype=torch.bfloat16, device=dev)
+    dst = torch.empty_like(src)
+    best = None
+    for _ in range(6):
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record()
+        dst.copy_(src)
+        a1.record()
+        torch.cuda.synchronize()
+        t = a0.elapsed_time(a1)
+        best = t if best is None else min(best, t)
+    copy_gbs = 2 * src.numel() * 2 / best / 1e6
+    del src, dst
+    print(json.dumps({"device_copy_gbs_this_run": round(copy_gbs, 1), "measured_peak_gbs": peak}),
+          flush=True)
     rows = []
     for name, A, dt, nbytes, sched in _sweep_points():
         coll, d = colls[name], dts[dt]
@@ -510,7 +527,50 @@ def run_sweep(args):
         torch.cuda.empty_cache()
     if args.sweep_out:
         with open(args.sweep_out, "w") as f:
-            json.dump({"peak_gbs": peak, "rows": rows}, f, indent=1)
+            json.dump({"peak_gbs": peak, "device_copy_gbs_this_run": round(copy_gbs, 1),
+                       "rows": rows}, f, indent=1)
+    return 0
+
+
+def run_profile_case(args):
+    """A named collective run W + K times under the library's default launch policy, for
+    profiler captures of kernels the bench workload does not exercise (not a bench line).
+    Case: COLLECTIVE:A:DTYPE:COUNT[:relay], COUNT in the collective's own count."""
+    import torch
+    import pack_virtual_rank_gb300.build as b
+    b.build()
+    import pack_virtual_rank_gb300 as rv
+    import synth
+    name, a, dt, cnt, *rest = args.profile_case.split(":")
+    Ap, count = int(a), int(cnt)
+    coll = {"allreduce": rv.ALLREDUCE, "reduce_scatter": rv.REDUCE_SCATTER,
+            "all_gather": rv.ALL_GATHER, "all_to_all": rv.ALL_TO_ALL}[name]
+    d = {"f32": rv.F32, "bf16": rv.BF16, "i32": rv.I32}[dt]
+    opts = rv.make_opts(schedule=rv.SCHEDULE_RELAY if rest and rest[0] == "relay"
+                        else rv.SCHEDULE_AUTO)
+    dev = torch.device("cuda", 0)
+    plan = rv.relay_plan(coll, count, d, Ap, R, opts)
+    xs = [synth.rank_input(9, r, plan.input_elems, dt, device=dev) for r in range(Ap)]
+    ys = [torch.empty(plan.output_elems, dtype=xs[0].dtype, device=dev) for _ in range(Ap)]
+    scratch = rv.alloc_scratch(plan, dev)
+    scale = 1.0 if (d == rv.I32 or coll in (rv.ALL_GATHER, rv.ALL_TO_ALL)) else 1.0 / Ap
+    fn = rv.COLLECTIVES[coll]
+    a0 = (xs + [None] * (R - Ap), ys + [None] * (R - Ap), scratch, count, d, Ap, R)
+    call = (lambda: fn(*a0, scale, opts)) if coll in (rv.ALLREDUCE, rv.REDUCE_SCATTER) \
+        else (lambda: fn(*a0, opts))
+    for _ in range(args.warmup):
+        call()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(args.steps):
+        call()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    nbytes = sum(p["bytes_read"] + p["bytes_written"] for p in rv.relay_plan_passes(plan))
+    print(json.dumps({"profile_case": args.profile_case, "passes": len(rv.relay_plan_passes(plan)),
+                      "ms_per_call": round(ms, 4), "gbs": round(nbytes / ms / 1e6, 1)}))
     return 0
 
 
@@ -523,6 +583,9 @@ def main():
     ap.add_argument("--count", type=int, default=COUNT,
                     help="elements per rank (default 2^29 = 1 GiB of bf16); smaller counts are "
                          "for profiling captures, not bench lines")
+    ap.add_argument("--profile-case", default=None,
+                    help="COLLECTIVE:A:DTYPE:COUNT[:relay] run under the default launch policy "
+                         "for profiler captures (not a bench line)")
     ap.add_argument("--sweep", action="store_true",
                     help="per-collective, per-count pass table of the five reference workloads "
                          "(not a bench line)")
@@ -537,6 +600,8 @@ def main():
         return run_reference(args)
     if args.sweep:
         return run_sweep(args)
+    if args.profile_case:
+        return run_profile_case(args)
     return run_ours(args)
 
 

@@ -430,3 +430,14 @@ def test_size_queries_and_page_contract(orc):
                         assert rv.relay_helper_size(p) == p.helper_elems
                         assert rv.relay_active_scratch_size(p) == p.active_scratch_elems
     assert rv.relay_helper_contract_size(0, 10, 3, 8) == -1
+
+
+def test_oversized_counts_are_rejected():
+    p = rv.RelayPlan()
+    for coll in range(4):
+        assert rv.lib().relay_plan(coll, 1 << 62, 0, 2, 8, None, ctypes.byref(p)) == \
+            rv.ERR_INVALID_ARGUMENT
+    arr = lambda xs: (ctypes.c_void_p * 8)(*(xs + [None] * (8 - len(xs))))
+    st = rv.lib().relay_allreduce(arr([1 << 40, 2 << 40]), arr([3 << 40, 4 << 40]), arr([]),
+                                  (1 << 64) - 1, 0, 2, 8, 1.0, None, None)
+    assert st == rv.ERR_INVALID_ARGUMENT
