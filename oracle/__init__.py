@@ -58,6 +58,8 @@ def lib():
         L.orc_allreduce.argtypes = [i32, i32, vp, i64, i64, f32, vp, vp, vp]
         L.orc_reduce_scatter.argtypes = [i32, i32, vp, i64, i32, i64, i64, f32, i64,
                                          vp, vp, vp]
+        L.orc_reduce_scatter_wide.argtypes = [i32, i32, vp, i64, i32, i64, i64, f32, i64,
+                                              vp, vp, vp]
         L.orc_all_gather.argtypes = [i32, i32, vp, i64, vp]
         L.orc_all_to_all.argtypes = [i32, i32, vp, i64, i32, vp]
         L.orc_align_down.restype = i64
@@ -126,6 +128,19 @@ def reduce_scatter(dtype, xs, m, owner, scale=1.0, helper_span=0, i0=0, i1=None)
     lib().orc_reduce_scatter(dtype, len(xs), _ptrs(xs), m, owner, i0, i1, scale,
                              helper_span, r64.ctypes.data, r32.ctypes.data,
                              rq.ctypes.data)
+    return r64, r32, rq
+
+
+def reduce_scatter_wide(dtype, xs, m, owner, scale=1.0, helper_span=0, i0=0, i1=None):
+    """Flat reduce-at-helper with the helper partial carried in fp32 (not rounded)."""
+    _check(xs, dtype)
+    i1 = m if i1 is None else i1
+    n = i1 - i0
+    r64 = np.empty(n, np.float64)
+    r32 = np.empty(n, np.float32)
+    rq = np.empty(n, NP_DTYPE[dtype])
+    lib().orc_reduce_scatter_wide(dtype, len(xs), _ptrs(xs), m, owner, i0, i1, scale,
+                                  helper_span, r64.ctypes.data, r32.ctypes.data, rq.ctypes.data)
     return r64, r32, rq
 
 

@@ -123,9 +123,9 @@ void orc_allreduce(int dtype, int A, const void* const* x, int64_t i0, int64_t i
  * ("A-1 chunks in, one out"), so it is rounded to the payload type before the owner
  * adds its own contribution and applies the scale.  Positions past helper_span are
  * reduced at the owner from all A sources, ascending. */
-void orc_reduce_scatter(int dtype, int A, const void* const* x, int64_t m, int owner,
-                        int64_t i0, int64_t i1, float scale, int64_t helper_span,
-                        double* ref64, float* ref32, void* refq) {
+static void reduce_scatter_impl(int dtype, int A, const void* const* x, int64_t m, int owner,
+                                int64_t i0, int64_t i1, float scale, int64_t helper_span,
+                                int round_partial, double* ref64, float* ref32, void* refq) {
   for (int64_t i = i0; i < i1; ++i) {
     int64_t o = i - i0;
     int64_t p = (int64_t)owner * m + i;
@@ -152,7 +152,7 @@ void orc_reduce_scatter(int dtype, int A, const void* const* x, int64_t m, int o
         if (s == owner) continue;
         partial = partial + load_f(dtype, x[s], p);
       }
-      partial = quantize(dtype, partial);
+      if (round_partial) partial = quantize(dtype, partial);
       acc32 = load_f(dtype, x[owner], p) + partial;
     } else {
       acc32 = load_f(dtype, x[0], p);
@@ -163,6 +163,21 @@ void orc_reduce_scatter(int dtype, int A, const void* const* x, int64_t m, int o
     if (ref32) ref32[o] = r32;
     if (refq) store_q(dtype, refq, o, r32);
   }
+}
+
+void orc_reduce_scatter(int dtype, int A, const void* const* x, int64_t m, int owner,
+                        int64_t i0, int64_t i1, float scale, int64_t helper_span,
+                        double* ref64, float* ref32, void* refq) {
+  reduce_scatter_impl(dtype, A, x, m, owner, i0, i1, scale, helper_span, 1, ref64, ref32, refq);
+}
+
+/* The same flat reduce-at-helper with the helper's partial carried back in fp32 instead
+ * of the payload type (a reading the page leaves open: it does not state the precision
+ * of the returned chunk).  The owner still adds its own value first, then the partial. */
+void orc_reduce_scatter_wide(int dtype, int A, const void* const* x, int64_t m, int owner,
+                             int64_t i0, int64_t i1, float scale, int64_t helper_span,
+                             double* ref64, float* ref32, void* refq) {
+  reduce_scatter_impl(dtype, A, x, m, owner, i0, i1, scale, helper_span, 0, ref64, ref32, refq);
 }
 
 /* All-gather (D115998385): every active's output is the A inputs of S elements laid

@@ -48,6 +48,9 @@ void orc_allreduce(int dtype, int A, const void* const* x, int64_t i0, int64_t i
 void orc_reduce_scatter(int dtype, int A, const void* const* x, int64_t m, int owner,
                         int64_t i0, int64_t i1, float scale, int64_t helper_span,
                         double* ref64, float* ref32, void* refq);
+void orc_reduce_scatter_wide(int dtype, int A, const void* const* x, int64_t m, int owner,
+                             int64_t i0, int64_t i1, float scale, int64_t helper_span,
+                             double* ref64, float* ref32, void* refq);
 void orc_all_gather(int esize, int A, const void* const* x, int64_t S, void* out);
 void orc_all_to_all(int esize, int A, const void* const* x, int64_t seg, int dst, void* out);
 

@@ -135,6 +135,35 @@ def test_rs4_partial_rounding_hand_case(orc):
         assert int(rq_direct[0]) == int(direct, 16)
 
 
+def test_rs4_wide_partial_hand_case(orc):
+    # the fp32 partial 1 + 2^-8 is exact, so the owner's result is the single-rounding
+    # one: the golden file's "direct" column
+    for *xb, scale, relayed, direct in _rows("rs4_partial_rounding.txt"):
+        xs = [np.array([int(b, 16)], np.uint16) for b in xb]
+        _, _, rq = orc.reduce_scatter_wide(1, xs, 1, 0, float(scale), helper_span=1)
+        assert int(rq[0]) == int(direct, 16)
+
+
+def test_rs4_wide_partial_is_one_reassociation(orc):
+    # fp32: carrying the partial unrounded changes only the association (own + others)
+    rng = np.random.default_rng(9)
+    m = 500
+    xs = [rng.standard_normal(4 * m).astype(np.float32) for _ in range(4)]
+    for o in range(4):
+        _, r32, _ = orc.reduce_scatter_wide(0, xs, m, o, 0.5, helper_span=m)
+        others = [x[o * m:(o + 1) * m] for s, x in enumerate(xs) if s != o]
+        part = others[0] + others[1]
+        part = part + others[2]
+        exp = (xs[o][o * m:(o + 1) * m] + part) * np.float32(0.5)
+        assert np.array_equal(r32, exp)
+    # bf16, integer-valued inputs: every partial is exact, all three forms agree
+    xs = [orc.bf16_rne(rng.integers(-8, 9, 4 * m).astype(np.float32)) for _ in range(4)]
+    for o in range(4):
+        a = orc.reduce_scatter_wide(1, xs, m, o, 0.25, helper_span=m)[2]
+        b = orc.reduce_scatter(1, xs, m, o, 0.25, helper_span=0)[2]
+        assert np.array_equal(a, b)
+
+
 def test_rs4_partial_rounding_is_noop_on_exact_sums(orc):
     # small integers: every partial sum is exact in bf16, so the relayed and the
     # direct reading must agree bit for bit
