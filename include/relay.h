@@ -86,6 +86,15 @@ typedef enum {
  * as ONE cooperative launch whose passes are separated by grid-wide barriers; any other
  * call launches each pass separately. */
 #define RELAY_FUSED_MAX_BYTES (64ll << 20)
+#define RELAY_FLAG_PAYLOAD_PARTIAL 16 /* 4-active reduce-scatter, bf16 payload: carry each
+                                      helper's partial to its owner in the payload type,
+                                      one payload-sized chunk per return hop as in the link
+                                      model (item 6). The partial is then rounded to bf16
+                                      before the owner adds its own value: a second rounding
+                                      that can move results several ulps off the exact sum.
+                                      Without this flag the partial crosses in fp32 (twice
+                                      the bytes of that hop, H*chunk more owner scratch) and
+                                      results stay within half an ulp of the exact sum. */
 
 typedef struct relay_opts {
   int32_t offload_permille;      /* A=4 allreduce / reduce-scatter / all-gather offload share;
@@ -133,7 +142,8 @@ typedef struct relay_plan {
   int32_t kind;            /* relay_kind_t */
   int32_t num_groups;      /* serialized groups of the schedule (cost model) */
   int32_t offload_permille;
-  int32_t reserved0;
+  int32_t wide_partial;    /* 1: 4-active reduce-scatter partials cross in fp32 (bf16
+                              payload without RELAY_FLAG_PAYLOAD_PARTIAL) */
   int64_t count;
   int64_t chunk;           /* A=2: relay chunk; A=4: offload slice per helper */
   int64_t relay_total;     /* H * chunk */

@@ -25,6 +25,7 @@ FLAG_CHECK_HAZARDS = 1
 FLAG_DRY_RUN = 2
 FLAG_SEPARATE_PASSES = 4
 FLAG_FUSED_PASSES = 8
+FLAG_PAYLOAD_PARTIAL = 16
 ESIZE = {F32: 4, BF16: 2, I32: 4}
 PASS_NAMES = ("group1", "group2", "group3", "active_reduce", "pack", "helper_forward", "unpack")
 
@@ -43,7 +44,7 @@ class RelayOpts(ctypes.Structure):
 
 class RelayPlan(ctypes.Structure):
     _fields_ = ([(f, ctypes.c_int32) for f in ("coll", "dtype", "A", "R", "H", "esize", "kind",
-                                               "num_groups", "offload_permille", "reserved0")]
+                                               "num_groups", "offload_permille", "wide_partial")]
                 + [(f, ctypes.c_int64) for f in ("count", "chunk", "relay_total", "dirA_offset",
                                                  "dirA_size", "dirB_size", "direct_total",
                                                  "direct_g1", "direct_g2", "owner_slice",
@@ -52,7 +53,7 @@ class RelayPlan(ctypes.Structure):
                                                  "output_elems")])
 
     def as_dict(self) -> dict:
-        return {name: getattr(self, name) for name, _ in self._fields_ if name != "reserved0"}
+        return {name: getattr(self, name) for name, _ in self._fields_}
 
 
 class RelayPassInfo(ctypes.Structure):

@@ -63,23 +63,23 @@ bool overlaps(const Range& a, const Range& b) { return a.lo < b.hi && b.lo < a.h
 // orders CTAs within a launch.
 bool find_hazard(const Pass& pass, int E, std::string* why) {
   const auto& s = pass.segs;
-  auto rng = [&](const void* p, int64_t n) {
+  auto rng = [&](const void* p, int64_t bytes) {
     const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
-    return Range{lo, lo + (uintptr_t)(n * E), ""};
+    return Range{lo, lo + (uintptr_t)bytes, ""};
   };
   for (size_t i = 0; i < s.size(); ++i)
     for (int d = 0; d < s[i].ndst; ++d) {
-      const Range w = rng(s[i].dst[d], s[i].n);
+      const Range w = rng(s[i].dst[d], seg_dst_bytes(s[i], E));
       for (size_t j = 0; j < s.size(); ++j) {
         if (j == i) continue;
         for (int k = 0; k < s[j].nsrc; ++k)
-          if (overlaps(w, rng(s[j].src[k], s[j].n))) {
+          if (overlaps(w, rng(s[j].src[k], seg_src_bytes(s[j], k, E)))) {
             *why = "segment " + std::to_string(i) + " writes what segment " + std::to_string(j) +
                    " reads in pass " + relay_pass_name(pass.kind);
             return true;
           }
         for (int k = 0; k < s[j].ndst; ++k)
-          if (overlaps(w, rng(s[j].dst[k], s[j].n))) {
+          if (overlaps(w, rng(s[j].dst[k], seg_dst_bytes(s[j], E)))) {
             *why = "segments " + std::to_string(i) + " and " + std::to_string(j) +
                    " write the same bytes in pass " + relay_pass_name(pass.kind);
             return true;
@@ -92,8 +92,8 @@ bool find_hazard(const Pass& pass, int E, std::string* why) {
 // Every range a segment reads or writes must lie inside one declared buffer.
 bool find_out_of_bounds(const Pass& pass, int E, const std::vector<Range>& bufs,
                         std::string* why) {
-  auto inside = [&](const void* p, int64_t n) {
-    const uintptr_t lo = reinterpret_cast<uintptr_t>(p), hi = lo + (uintptr_t)(n * E);
+  auto inside = [&](const void* p, int64_t bytes) {
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(p), hi = lo + (uintptr_t)bytes;
     for (const Range& b : bufs)
       if (lo >= b.lo && hi <= b.hi) return true;
     return false;
@@ -101,8 +101,8 @@ bool find_out_of_bounds(const Pass& pass, int E, const std::vector<Range>& bufs,
   for (size_t i = 0; i < pass.segs.size(); ++i) {
     const Seg& s = pass.segs[i];
     bool ok = true;
-    for (int k = 0; k < s.nsrc; ++k) ok &= inside(s.src[k], s.n);
-    for (int d = 0; d < s.ndst; ++d) ok &= inside(s.dst[d], s.n);
+    for (int k = 0; k < s.nsrc; ++k) ok &= inside(s.src[k], seg_src_bytes(s, k, E));
+    for (int d = 0; d < s.ndst; ++d) ok &= inside(s.dst[d], seg_dst_bytes(s, E));
     if (!ok) {
       *why = "segment " + std::to_string(i) + " of pass " + relay_pass_name(pass.kind) +
              " leaves the declared buffers";
@@ -185,7 +185,10 @@ relay_status_t execute(const std::vector<Pass>& passes, const std::vector<Range>
   if (!events_wanted && !(flags & RELAY_FLAG_SEPARATE_PASSES)) {
     int64_t bytes = 0;
     for (const Pass& ps : passes)
-      for (const Seg& sg : ps.segs) bytes += sg.n * E * (sg.nsrc + sg.ndst);
+      for (const Seg& sg : ps.segs) {
+        for (int k = 0; k < sg.nsrc; ++k) bytes += seg_src_bytes(sg, k, E);
+        bytes += seg_dst_bytes(sg, E) * sg.ndst;
+      }
     if ((flags & RELAY_FLAG_FUSED_PASSES) || bytes <= RELAY_FUSED_MAX_BYTES) {
       cudaError_t e = cudaSuccess;
       if (launch_fused(dtype, passes, scale, stream, &e)) {
@@ -351,7 +354,7 @@ relay_status_t relay_plan_link_bytes(const relay_plan_t* plan, uint64_t* out, si
       for (int d = 0; d < ps.segs[i].ndst; ++d)
         if (m.dst_rank[d] != m.exec_rank)
           out[((size_t)m.group * R + m.exec_rank) * R + m.dst_rank[d]] +=
-              (uint64_t)ps.segs[i].n * plan->esize;
+              (uint64_t)seg_dst_bytes(ps.segs[i], plan->esize);
     }
   return RELAY_OK;
 }
@@ -378,8 +381,8 @@ int relay_plan_passes(const relay_plan_t* plan, int in_place, relay_pass_info_t*
     q.num_segments = (int32_t)passes[i].segs.size();
     q.bytes_read = q.bytes_written = 0;
     for (const Seg& s : passes[i].segs) {
-      q.bytes_read += s.n * plan->esize * s.nsrc;
-      q.bytes_written += s.n * plan->esize * s.ndst;
+      for (int k = 0; k < s.nsrc; ++k) q.bytes_read += seg_src_bytes(s, k, plan->esize);
+      q.bytes_written += seg_dst_bytes(s, plan->esize) * s.ndst;
     }
   }
   return (int)passes.size();

@@ -405,11 +405,87 @@ __device__ __noinline__ void run_partial_tile(const Seg& s, int64_t base, int64_
   }
 }
 
-// REALIGN selects the variant that runs segments with realigned sources; it is its own
-// kernel so that its register need does not cost the others occupancy. Both run 5 CTAs
-// per SM (48 registers): measured on GB300, the realigned all-to-all passes gain more
-// from occupancy than from holding more vectors per thread.
-template <class P, int CAP, bool REALIGN>
+// Mixed-width segments of the wide-partial reduce-scatter (bf16 payload): a helper
+// summing bf16 slots into an fp32 partial (kFlagOutF32), and an owner adding its bf16 value
+// and the fp32 partial (kFlagSrc1F32). 8 elements per step: one 16-byte bf16 vector or
+// two 16-byte fp32 vectors per operand. Rare and optional, so one vector at a time.
+__device__ __forceinline__ void unpack_f32x8(uint4 a, uint4 b, float* v) {
+  v[0] = __uint_as_float(a.x); v[1] = __uint_as_float(a.y);
+  v[2] = __uint_as_float(a.z); v[3] = __uint_as_float(a.w);
+  v[4] = __uint_as_float(b.x); v[5] = __uint_as_float(b.y);
+  v[6] = __uint_as_float(b.z); v[7] = __uint_as_float(b.w);
+}
+
+template <class P>
+__device__ __noinline__ void run_mixed_tile(const Seg& s, int64_t base, int64_t len, float scale) {
+  const bool do_scale = (s.flags & kFlagScale) != 0;
+  const bool out_f32 = (s.flags & kFlagOutF32) != 0;
+  const bool src1_f32 = (s.flags & kFlagSrc1F32) != 0;
+  int64_t done = 0;
+  if (P::kE == 2 && (s.flags & kFlagVector)) {
+    const int64_t vb = base / 8, nvec = len / 8;
+#pragma unroll 1
+    for (int64_t vi = threadIdx.x; vi < nvec; vi += kThreads) {
+      float acc[8], t[8];
+      TBF16::unpack(Mem<false>::v4(static_cast<const uint4*>(s.src[0]) + vb + vi), acc);
+#pragma unroll 1
+      for (int k = 1; k < s.nsrc; ++k) {
+        if (k == 1 && src1_f32) {
+          const uint4* q = static_cast<const uint4*>(s.src[1]) + 2 * (vb + vi);
+          unpack_f32x8(Mem<false>::v4(q), Mem<false>::v4(q + 1), t);
+        } else {
+          TBF16::unpack(Mem<false>::v4(static_cast<const uint4*>(s.src[k]) + vb + vi), t);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], t[i]);
+      }
+      if (do_scale) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = __fmul_rn(acc[i], scale);
+      }
+#pragma unroll 1
+      for (int d = 0; d < s.ndst; ++d) {
+        if (out_f32) {
+          uint4* q = static_cast<uint4*>(s.dst[d]) + 2 * (vb + vi);
+          st_v4(q, make_uint4(__float_as_uint(acc[0]), __float_as_uint(acc[1]),
+                              __float_as_uint(acc[2]), __float_as_uint(acc[3])));
+          st_v4(q + 1, make_uint4(__float_as_uint(acc[4]), __float_as_uint(acc[5]),
+                                  __float_as_uint(acc[6]), __float_as_uint(acc[7])));
+        } else {
+          st_v4(static_cast<uint4*>(s.dst[d]) + vb + vi, TBF16::pack(acc));
+        }
+      }
+    }
+    done = nvec * 8;
+  }
+#pragma unroll 1
+  for (int64_t e = done + threadIdx.x; e < len; e += kThreads) {
+    const int64_t i = base + e;
+    float acc = TBF16::template load1<false>(static_cast<const char*>(s.src[0]) + i * 2);
+#pragma unroll 1
+    for (int k = 1; k < s.nsrc; ++k) {
+      const float v = (k == 1 && src1_f32)
+                          ? TF32::template load1<false>(static_cast<const char*>(s.src[1]) + i * 4)
+                          : TBF16::template load1<false>(static_cast<const char*>(s.src[k]) + i * 2);
+      acc = __fadd_rn(acc, v);
+    }
+    if (do_scale) acc = __fmul_rn(acc, scale);
+#pragma unroll 1
+    for (int d = 0; d < s.ndst; ++d) {
+      if (out_f32) TF32::store1(static_cast<char*>(s.dst[d]) + i * 4, acc);
+      else TBF16::store1(static_cast<char*>(s.dst[d]) + i * 2, acc);
+    }
+  }
+}
+
+// MODE selects the segments a launch runs: kModeMain (aligned and per-element paths),
+// kModeRealign (realigned sources), kModeMixed (fp32 partials next to bf16). Each is its
+// own kernel so that the rarer variants' register needs do not cost the main path
+// occupancy. All run 5 CTAs per SM (48 registers): measured on GB300, the realigned
+// all-to-all passes gain more from occupancy than from more vectors per thread.
+constexpr int kModeMain = 0, kModeRealign = 1, kModeMixed = 2;
+
+template <class P, int CAP, int MODE>
 __global__ void __launch_bounds__(kThreads, 5)
     relay_pass_kernel(const __grid_constant__ PassArgs<CAP> args) {
   constexpr int64_t kTile = kTileBytes / P::kE;
@@ -423,8 +499,10 @@ __global__ void __launch_bounds__(kThreads, 5)
     const Seg& s = args.seg[lo];
     const int64_t base = (int64_t)(t - s.tile0) * kTile;
     const int64_t len = min(kTile, s.n - base);
-    if (!REALIGN && (s.flags & kFlagVector) && len == kTile) run_full_tile<P, false>(s, base, args.scale);
-    else if (REALIGN && len == kTile) run_realign_tile<P>(s, base, args.scale);
+    if (MODE == kModeMixed) run_mixed_tile<P>(s, base, len, args.scale);
+    else if (MODE == kModeMain && (s.flags & kFlagVector) && len == kTile)
+      run_full_tile<P, false>(s, base, args.scale);
+    else if (MODE == kModeRealign && len == kTile) run_realign_tile<P>(s, base, args.scale);
     else run_partial_tile<P, false>(s, base, len, args.scale);
   }
 }
@@ -517,12 +595,12 @@ int sm_count() {
   return n;
 }
 
-template <class P, int CAP, bool REALIGN>
+template <class P, int CAP, int MODE>
 int blocks_per_sm() {
   static int cached = 0;
   if (cached == 0) {
     int nb = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, relay_pass_kernel<P, CAP, REALIGN>, kThreads, 0) !=
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, relay_pass_kernel<P, CAP, MODE>, kThreads, 0) !=
             cudaSuccess ||
         nb <= 0)
       nb = 1;
@@ -531,7 +609,7 @@ int blocks_per_sm() {
   return cached;
 }
 
-template <class P, int CAP, bool REALIGN>
+template <class P, int CAP, int MODE>
 cudaError_t launch_cap(const Seg* segs, int nseg, float scale, cudaStream_t stream) {
   static thread_local PassArgs<CAP> a;  // up to ~30 KiB: keep it off the stack
   constexpr int64_t kTile = kTileBytes / P::kE;
@@ -546,36 +624,27 @@ cudaError_t launch_cap(const Seg* segs, int nseg, float scale, cudaStream_t stre
   a.ntiles = (int32_t)tiles;
   a.scale = scale;
   a.pad = 0;
-  const int64_t cap = (int64_t)sm_count() * blocks_per_sm<P, CAP, REALIGN>();
+  const int64_t cap = (int64_t)sm_count() * blocks_per_sm<P, CAP, MODE>();
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, cap));
-  relay_pass_kernel<P, CAP, REALIGN><<<grid, kThreads, 0, stream>>>(a);
+  relay_pass_kernel<P, CAP, MODE><<<grid, kThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
-template <class P, bool REALIGN>
+template <class P, int MODE>
 cudaError_t launch_typed(const std::vector<Seg>& segs, float scale, cudaStream_t stream) {
   constexpr int kMaxCap = 384;  // 16 + 384 * 80 bytes of parameters, under the 32 KiB limit
   size_t i = 0;
   while (i < segs.size()) {
     const int n = (int)std::min<size_t>(segs.size() - i, kMaxCap);
     cudaError_t e;
-    if (n <= 8) e = launch_cap<P, 8, REALIGN>(segs.data() + i, n, scale, stream);
-    else if (n <= 32) e = launch_cap<P, 32, REALIGN>(segs.data() + i, n, scale, stream);
-    else if (n <= 128) e = launch_cap<P, 128, REALIGN>(segs.data() + i, n, scale, stream);
-    else e = launch_cap<P, kMaxCap, REALIGN>(segs.data() + i, n, scale, stream);
+    if (n <= 8) e = launch_cap<P, 8, MODE>(segs.data() + i, n, scale, stream);
+    else if (n <= 32) e = launch_cap<P, 32, MODE>(segs.data() + i, n, scale, stream);
+    else if (n <= 128) e = launch_cap<P, 128, MODE>(segs.data() + i, n, scale, stream);
+    else e = launch_cap<P, kMaxCap, MODE>(segs.data() + i, n, scale, stream);
     if (e != cudaSuccess) return e;
     i += n;
   }
   return cudaSuccess;
-}
-
-template <class P>
-cudaError_t launch_split(const std::vector<Seg>& direct, const std::vector<Seg>& realigned,
-                         float scale, cudaStream_t stream) {
-  cudaError_t e = cudaSuccess;
-  if (!direct.empty()) e = launch_typed<P, false>(direct, scale, stream);
-  if (e == cudaSuccess && !realigned.empty()) e = launch_typed<P, true>(realigned, scale, stream);
-  return e;
 }
 
 template <class P>
@@ -633,7 +702,7 @@ bool launch_fused(int dtype, const std::vector<Pass>& passes, float scale, cudaS
     a.seg0[p] = n;
     int64_t tiles = 0;
     for (const Seg& sg : segs) {
-      if ((sg.flags & kFlagRealign) || n >= kFusedCap) return false;
+      if ((sg.flags & kFlagRealign) || seg_mixed(sg) || n >= kFusedCap) return false;
       a.seg[n] = sg;
       a.seg[n].tile0 = (int32_t)tiles;
       tiles += (sg.n + tile - 1) / tile;
@@ -652,18 +721,48 @@ bool launch_fused(int dtype, const std::vector<Pass>& passes, float scale, cudaS
   return true;
 }
 
-// Segments with realigned sources go to their own launch after the others; the two
-// launches of such a pass touch disjoint memory, so their order does not matter.
+namespace {
+
+template <class P>
+cudaError_t launch_split(const std::vector<Seg>& direct, const std::vector<Seg>& realigned,
+                         const std::vector<Seg>& mixed, float scale, cudaStream_t stream) {
+  cudaError_t e = cudaSuccess;
+  if (!direct.empty()) e = launch_typed<P, kModeMain>(direct, scale, stream);
+  if (e == cudaSuccess && !realigned.empty()) e = launch_typed<P, kModeRealign>(realigned, scale, stream);
+  if (e == cudaSuccess && !mixed.empty()) e = launch_typed<P, kModeMixed>(mixed, scale, stream);
+  return e;
+}
+
+}  // namespace
+
+// Segments with realigned sources, and mixed-width segments, go to their own launches
+// after the others; the launches of one pass touch disjoint memory, so their order does
+// not matter.
 cudaError_t launch_pass(int dtype, const Pass& pass, float scale, cudaStream_t stream) {
-  static thread_local std::vector<Seg> segs, direct, realigned;
-  split_for_alignment(pass.segs, esize_of(dtype), &segs);
+  static thread_local std::vector<Seg> plain, segs, direct, realigned, mixed;
+  plain.clear();
+  mixed.clear();
+  for (const Seg& sg : pass.segs) {
+    if (!seg_mixed(sg)) {
+      plain.push_back(sg);
+      continue;
+    }
+    if (dtype != RELAY_BF16) return cudaErrorInvalidValue;  // only bf16 payloads widen
+    Seg m = sg;
+    bool aligned = true;
+    for (int k = 0; k < m.nsrc; ++k) aligned &= (reinterpret_cast<uintptr_t>(m.src[k]) & 15u) == 0;
+    for (int d = 0; d < m.ndst; ++d) aligned &= (reinterpret_cast<uintptr_t>(m.dst[d]) & 15u) == 0;
+    m.flags = (uint8_t)((m.flags & ~(kFlagVector | kFlagRealign)) | (aligned ? kFlagVector : 0));
+    mixed.push_back(m);
+  }
+  split_for_alignment(plain, esize_of(dtype), &segs);
   direct.clear();
   realigned.clear();
   for (const Seg& sg : segs) (sg.flags & kFlagRealign ? realigned : direct).push_back(sg);
   switch (dtype) {
-    case RELAY_F32: return launch_split<TF32>(direct, realigned, scale, stream);
-    case RELAY_BF16: return launch_split<TBF16>(direct, realigned, scale, stream);
-    default: return launch_split<TI32>(direct, realigned, scale, stream);
+    case RELAY_F32: return launch_split<TF32>(direct, realigned, mixed, scale, stream);
+    case RELAY_BF16: return launch_split<TBF16>(direct, realigned, mixed, scale, stream);
+    default: return launch_split<TI32>(direct, realigned, mixed, scale, stream);
   }
 }
 

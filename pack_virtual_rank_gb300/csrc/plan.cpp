@@ -185,6 +185,12 @@ relay_status_t make_plan(relay_coll_t coll, int64_t count, relay_dtype_t dtype, 
       }
       p.helper_elems = (int64_t)A * (A - 1) * oc;
       p.active_scratch_elems = H * oc + (A - 1) * pD;
+      // a bf16 partial crosses in fp32 unless the caller asks for the payload type; an
+      // fp32 partial takes two bf16 elements of the owner's scratch
+      if (!(o.flags & RELAY_FLAG_PAYLOAD_PARTIAL) && dtype == RELAY_BF16 && oc > 0) {
+        p.wide_partial = 1;
+        p.active_scratch_elems += H * oc;
+      }
       break;
     }
     case RELAY_ALL_GATHER: {

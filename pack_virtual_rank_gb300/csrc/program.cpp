@@ -43,8 +43,9 @@ class Builder {
     emit(group, exec, kOpCopy, &src, 1, dsts, n, false);
   }
   void reduce(int group, int exec, const std::vector<const void*>& srcs,
-              const std::vector<Dst>& dsts, int64_t n, bool scale) {
+              const std::vector<Dst>& dsts, int64_t n, bool scale, uint8_t extra_flags = 0) {
     emit(group, exec, kOpReduce, srcs.data(), (int)srcs.size(), dsts, n, scale);
+    if (n > 0) cur_->segs.back().flags |= extra_flags;
   }
 
   // element-offset pointers into the rank buffers
@@ -269,14 +270,15 @@ void build_a4_allreduce(Builder& B, const relay_plan_t& p) {
 void build_a4_reduce_scatter(Builder& B, const relay_plan_t& p) {
   // item 6: flat reduce-at-helper. Helper h owns position slice h of every block; the
   // A-1 non-owner sources send it their slice (group 1), the helper sums them into one
-  // payload-typed partial and returns that single chunk to the owner (group 2). The
-  // direct positions go source -> owner in two parts (group 1, group 2). The owner
-  // scratch: [partials: H*oc, position-aligned | A-1 direct slots of pD].
+  // partial and returns that single chunk to the owner (group 2). The direct positions
+  // go source -> owner in two parts (group 1, group 2). The owner scratch:
+  //   [partials: H*oc positions, payload-typed (or fp32 when wide) | A-1 direct slots of pD].
   const int A = p.A, H = p.H;
   const int64_t m = p.count, oc = p.chunk, pD = p.direct_total;
-  const int64_t P = H * oc;  // offload positions per block
+  const int64_t P = H * oc;                      // offload positions per block
+  const int64_t pw = p.wide_partial ? 2 : 1;     // payload elements per partial element
   auto slot = [&](int o, int s) { return (o * (A - 1) + other_index(s, o)) * oc; };
-  auto dslot = [&](int o, int s) { return P + other_index(s, o) * pD; };
+  auto dslot = [&](int o, int s) { return pw * P + other_index(s, o) * pD; };
   B.begin(RELAY_PASS_G1);
   for (int s = 0; s < A; ++s)
     for (int h = 0; h < H; ++h)
@@ -292,7 +294,8 @@ void build_a4_reduce_scatter(Builder& B, const relay_plan_t& p) {
         std::vector<const void*> srcs;
         for (int s = 0; s < A; ++s)
           if (s != o) srcs.push_back(B.Hh(h, slot(o, s)));
-        B.reduce(1, A + h, srcs, {Dst{o, B.W(o, h * oc)}}, oc, false);
+        B.reduce(1, A + h, srcs, {Dst{o, B.W(o, pw * h * oc)}}, oc, false,
+                 p.wide_partial ? kFlagOutF32 : 0);
       }
     for (int s = 0; s < A; ++s)
       for (int o = 0; o < A; ++o)
@@ -303,7 +306,8 @@ void build_a4_reduce_scatter(Builder& B, const relay_plan_t& p) {
   B.begin(RELAY_PASS_ACTIVE_REDUCE);
   for (int o = 0; o < A; ++o) {
     // offload positions: the owner's own value first, then the returned partial
-    B.reduce(-1, o, {B.X(o, o * m), B.W(o, 0)}, {Dst{o, B.Y(o, 0)}}, P, true);
+    B.reduce(-1, o, {B.X(o, o * m), B.W(o, 0)}, {Dst{o, B.Y(o, 0)}}, P, true,
+             p.wide_partial ? kFlagSrc1F32 : 0);
     std::vector<const void*> srcs;
     for (int s = 0; s < A; ++s)
       srcs.push_back(s == o ? (const void*)B.X(o, o * m + P) : (const void*)B.W(o, dslot(o, s)));

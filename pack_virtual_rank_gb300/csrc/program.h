@@ -22,7 +22,13 @@ constexpr int kMaxSrc = 4;
 constexpr int kMaxDst = 4;
 
 enum SegOp : uint8_t { kOpCopy = 0, kOpReduce = 1 };
-enum SegFlag : uint8_t { kFlagScale = 1, kFlagVector = 2, kFlagRealign = 4 };
+enum SegFlag : uint8_t {
+  kFlagScale = 1,
+  kFlagVector = 2,    // every pointer 16-byte aligned (set at launch)
+  kFlagRealign = 4,   // destinations aligned, sources realigned in registers (set at launch)
+  kFlagOutF32 = 8,    // bf16 sources, result stored as fp32 (a wide helper partial)
+  kFlagSrc1F32 = 16   // source 1 is fp32, the rest bf16 (an owner adding a wide partial)
+};
 
 // Device-visible segment descriptor (kernel parameter space).
 struct Seg {
@@ -40,6 +46,16 @@ struct SegMeta {
   int8_t exec_rank;       // rank whose kernel work this is (owner of the sources)
   int8_t dst_rank[kMaxDst];
 };
+
+// Bytes one source / one destination of a segment spans (mixed-width segments carry
+// fp32 next to the payload type).
+inline int64_t seg_src_bytes(const Seg& s, int k, int E) {
+  return s.n * ((k == 1 && (s.flags & kFlagSrc1F32)) ? 4 : E);
+}
+inline int64_t seg_dst_bytes(const Seg& s, int E) {
+  return s.n * ((s.flags & kFlagOutF32) ? 4 : E);
+}
+inline bool seg_mixed(const Seg& s) { return (s.flags & (kFlagOutF32 | kFlagSrc1F32)) != 0; }
 
 struct Pass {
   relay_pass_kind_t kind;

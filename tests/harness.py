@@ -128,7 +128,8 @@ def expected(c, xs_host, rank, i0, i1):
         r64, r32, rq = orc.allreduce(d, xs_host, c.scale, i0, i1)
         return rq, r32, r64
     if c.coll == rv.REDUCE_SCATTER:
-        r64, r32, rq = orc.reduce_scatter(d, xs_host, n, rank, c.scale, helper_span(c), i0, i1)
+        rs = orc.reduce_scatter_wide if c.plan.wide_partial else orc.reduce_scatter
+        r64, r32, rq = rs(d, xs_host, n, rank, c.scale, helper_span(c), i0, i1)
         return rq, r32, r64
     if c.coll == rv.ALL_GATHER:
         return orc.all_gather(xs_host, n)[i0:i1], None, None
@@ -266,7 +267,8 @@ def _check_block_window(c, rank, k, lo, hi):
             t[rank * w:(rank + 1) * w] = host(x[rank * n + lo: rank * n + hi])
             tiny.append(t)
         span = max(0, min(helper_span(c) - lo, w))
-        exp = orc.reduce_scatter(d, tiny, w, rank, c.scale, span)[2]
+        rs = orc.reduce_scatter_wide if c.plan.wide_partial else orc.reduce_scatter
+        exp = rs(d, tiny, w, rank, c.scale, span)[2]
     elif c.coll == rv.ALL_GATHER:
         tiny = [np.zeros(w, dtype=NP[d]) for _ in range(A)]
         tiny[k] = host(c.inputs[k][lo:hi])

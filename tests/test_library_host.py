@@ -60,7 +60,10 @@ def test_planner_and_accountant_match_oracle(orc, coll):
             continue
         E = rv.ESIZE[dt]
         for pm in (500, 780):
-            opts = rv.make_opts(offload_permille=pm, schedule=sched)
+            # the oracle's cost model carries the 4-active reduce-scatter partial as one
+            # payload-typed chunk (item 6); the library's default fp32 partial doubles
+            # that hop and is checked separately
+            opts = rv.make_opts(offload_permille=pm, schedule=sched, flags=rv.FLAG_PAYLOAD_PARTIAL)
             try:
                 g, gv = orc.plan(coll, A, R, count, E, permille=pm, force=sched)
             except ValueError:
@@ -441,3 +444,41 @@ def test_oversized_counts_are_rejected():
     st = rv.lib().relay_allreduce(arr([1 << 40, 2 << 40]), arr([3 << 40, 4 << 40]), arr([]),
                                   (1 << 64) - 1, 0, 2, 8, 1.0, None, None)
     assert st == rv.ERR_INVALID_ARGUMENT
+
+
+def test_wide_partial_plan_links_and_bounds(orc):
+    """By default a bf16 4-active reduce-scatter carries each helper partial in fp32: that
+    doubles the bytes of each helper -> owner hop and nothing else, and the owner scratch
+    grows by H*chunk. RELAY_FLAG_PAYLOAD_PARTIAL restores the one payload-sized chunk.
+    Every program stays in bounds and race-free either way."""
+    for m in (1 << 20, 250_001, 4096 + 77):
+        p = rv.relay_plan(rv.REDUCE_SCATTER, m, rv.BF16, 4, 8, rv.make_opts(schedule=rv.SCHEDULE_RELAY))
+        narrow = rv.relay_plan(rv.REDUCE_SCATTER, m, rv.BF16, 4, 8,
+                               rv.make_opts(schedule=rv.SCHEDULE_RELAY, flags=rv.FLAG_PAYLOAD_PARTIAL))
+        assert p.wide_partial == 1 and narrow.wide_partial == 0
+        assert p.active_scratch_elems == narrow.active_scratch_elems + 4 * p.chunk
+        _, gv = orc.plan(rv.REDUCE_SCATTER, 4, 8, m, 2, force=rv.SCHEDULE_RELAY)
+        exp = orc.link_elems(gv).astype(np.uint64) * np.uint64(2)
+        assert np.array_equal(rv.relay_plan_link_bytes(narrow), exp)
+        exp[1, 4:, :4] *= np.uint64(2)            # helpers -> owners in group 2
+        assert np.array_equal(rv.relay_plan_link_bytes(p), exp)
+        for in_place in (False, True):
+            for extra in (0, rv.FLAG_PAYLOAD_PARTIAL):
+                st = _dry_wide(m, in_place, extra)
+                assert st == rv.OK, rv.lib().relay_last_error()
+    # fp32 payloads have nothing to widen
+    p = rv.relay_plan(rv.REDUCE_SCATTER, 1 << 20, rv.F32, 4, 8, rv.make_opts(schedule=rv.SCHEDULE_RELAY))
+    assert p.wide_partial == 0
+
+
+def _dry_wide(m, in_place, extra=0):
+    A, R, E = 4, 8, 2
+    opts = rv.make_opts(schedule=rv.SCHEDULE_RELAY,
+                        flags=extra | rv.FLAG_CHECK_HAZARDS | rv.FLAG_DRY_RUN)
+    send = [(r + 1) << 40 for r in range(A)]
+    recv = [s + r * m * E for r, s in enumerate(send)] if in_place else \
+        [((r + 10) << 40) for r in range(A)]
+    scratch = [((r + 20) << 40) for r in range(R)]
+    arr = lambda xs: (ctypes.c_void_p * R)(*(xs + [None] * (R - len(xs))))
+    return rv.lib().relay_reduce_scatter(arr(send), arr(recv), arr(scratch), m, rv.BF16, A, R,
+                                         0.25, ctypes.byref(opts), None)

@@ -266,3 +266,22 @@ def test_fused_launch_at_sizes_past_its_default(coll):
             c = hz.run(coll, A, 8, count, rv.BF16, scale, config=17,
                        schedule=rv.SCHEDULE_RELAY, flags=rv.FLAG_FUSED_PASSES)
             hz.check_all(c)
+
+
+def test_reduce_scatter_partial_precision():
+    """4-active bf16 reduce-scatter. By default the helper partial crosses in fp32: results
+    match the oracle's wide reading bit for bit and sit within half a bf16 ulp of the
+    fp64 sum. With RELAY_FLAG_PAYLOAD_PARTIAL the partial crosses as bf16: results match
+    the oracle's payload-typed reading bit for bit."""
+    for m, in_place in ((300_000, False), (250_001, True), (1 << 20, False)):
+        for flags in (0, rv.FLAG_SEPARATE_PASSES, rv.FLAG_PAYLOAD_PARTIAL):
+            c = hz.run(rv.REDUCE_SCATTER, 4, 8, m, rv.BF16, 0.25, config=19,
+                       schedule=rv.SCHEDULE_RELAY, in_place=in_place, flags=flags)
+            assert c.plan.wide_partial == (0 if flags & rv.FLAG_PAYLOAD_PARTIAL else 1)
+            hz.check_all(c)
+            if c.plan.wide_partial:
+                xs = [hz.host(x) for x in c.inputs]
+                for o in range(4):
+                    r64 = orc.reduce_scatter(rv.BF16, xs, m, o, 0.25, 0)[0]
+                    got = orc.bf16_to_f32(hz.host(c.recv[o])).astype(np.float64)
+                    assert np.all(np.abs(got - r64) <= hz.bf16_ulp(r64.astype(np.float32)) / 2)
