@@ -108,6 +108,11 @@ bool find_out_of_bounds(const Pass& pass, int E, const std::vector<Range>& bufs,
              " leaves the declared buffers";
       return true;
     }
+    if (!seg_operands_aligned(s, E)) {
+      *why = "segment " + std::to_string(i) + " of pass " + relay_pass_name(pass.kind) +
+             " has an operand not aligned to its element width";
+      return true;
+    }
   }
   return false;
 }

@@ -747,7 +747,9 @@ cudaError_t launch_pass(int dtype, const Pass& pass, float scale, cudaStream_t s
       plain.push_back(sg);
       continue;
     }
-    if (dtype != RELAY_BF16) return cudaErrorInvalidValue;  // only bf16 payloads widen
+    // only bf16 payloads widen, and every fp32 operand must be 4-byte aligned: never
+    // launch anything else
+    if (dtype != RELAY_BF16 || !seg_operands_aligned(sg, 2)) return cudaErrorInvalidValue;
     Seg m = sg;
     bool aligned = true;
     for (int k = 0; k < m.nsrc; ++k) aligned &= (reinterpret_cast<uintptr_t>(m.src[k]) & 15u) == 0;

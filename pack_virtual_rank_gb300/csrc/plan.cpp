@@ -189,7 +189,7 @@ relay_status_t make_plan(relay_coll_t coll, int64_t count, relay_dtype_t dtype, 
       // fp32 partial takes two bf16 elements of the owner's scratch
       if (!(o.flags & RELAY_FLAG_PAYLOAD_PARTIAL) && dtype == RELAY_BF16 && oc > 0) {
         p.wide_partial = 1;
-        p.active_scratch_elems += H * oc;
+        p.active_scratch_elems += H * oc + kWideSlackElems;
       }
       break;
     }

@@ -272,13 +272,22 @@ void build_a4_reduce_scatter(Builder& B, const relay_plan_t& p) {
   // A-1 non-owner sources send it their slice (group 1), the helper sums them into one
   // partial and returns that single chunk to the owner (group 2). The direct positions
   // go source -> owner in two parts (group 1, group 2). The owner scratch:
-  //   [partials: H*oc positions, payload-typed (or fp32 when wide) | A-1 direct slots of pD].
+  //   [partials: H*oc positions, payload-typed | A-1 direct slots of pD], or, with fp32
+  //   partials, [partials: H*oc fp32 starting on the first 16-byte boundary within the
+  //   8-element slack | A-1 direct slots of pD].
   const int A = p.A, H = p.H;
   const int64_t m = p.count, oc = p.chunk, pD = p.direct_total;
   const int64_t P = H * oc;                      // offload positions per block
   const int64_t pw = p.wide_partial ? 2 : 1;     // payload elements per partial element
+  const int64_t slack = p.wide_partial ? kWideSlackElems : 0;
+  // element offset of owner o's partial region: 16-byte aligned for fp32 partials
+  auto pofs = [&](int o) -> int64_t {
+    if (!p.wide_partial) return 0;
+    const unsigned mis = (unsigned)(reinterpret_cast<uintptr_t>(B.W(o, 0)) & 15u);
+    return (int64_t)((16u - mis) & 15u) / p.esize;
+  };
   auto slot = [&](int o, int s) { return (o * (A - 1) + other_index(s, o)) * oc; };
-  auto dslot = [&](int o, int s) { return pw * P + other_index(s, o) * pD; };
+  auto dslot = [&](int o, int s) { return pw * P + slack + other_index(s, o) * pD; };
   B.begin(RELAY_PASS_G1);
   for (int s = 0; s < A; ++s)
     for (int h = 0; h < H; ++h)
@@ -294,7 +303,7 @@ void build_a4_reduce_scatter(Builder& B, const relay_plan_t& p) {
         std::vector<const void*> srcs;
         for (int s = 0; s < A; ++s)
           if (s != o) srcs.push_back(B.Hh(h, slot(o, s)));
-        B.reduce(1, A + h, srcs, {Dst{o, B.W(o, pw * h * oc)}}, oc, false,
+        B.reduce(1, A + h, srcs, {Dst{o, B.W(o, pofs(o) + pw * h * oc)}}, oc, false,
                  p.wide_partial ? kFlagOutF32 : 0);
       }
     for (int s = 0; s < A; ++s)
@@ -306,7 +315,7 @@ void build_a4_reduce_scatter(Builder& B, const relay_plan_t& p) {
   B.begin(RELAY_PASS_ACTIVE_REDUCE);
   for (int o = 0; o < A; ++o) {
     // offload positions: the owner's own value first, then the returned partial
-    B.reduce(-1, o, {B.X(o, o * m), B.W(o, 0)}, {Dst{o, B.Y(o, 0)}}, P, true,
+    B.reduce(-1, o, {B.X(o, o * m), B.W(o, pofs(o))}, {Dst{o, B.Y(o, 0)}}, P, true,
              p.wide_partial ? kFlagSrc1F32 : 0);
     std::vector<const void*> srcs;
     for (int s = 0; s < A; ++s)

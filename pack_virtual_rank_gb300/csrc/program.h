@@ -57,6 +57,24 @@ inline int64_t seg_dst_bytes(const Seg& s, int E) {
 }
 inline bool seg_mixed(const Seg& s) { return (s.flags & (kFlagOutF32 | kFlagSrc1F32)) != 0; }
 
+// bf16 elements of slack in an owner's scratch that let its fp32 partials start on a
+// 16-byte boundary whatever the scratch pointer's alignment (bf16 pointers are only
+// 2-byte aligned; fp32 accesses need 4, the vector path 16).
+constexpr int64_t kWideSlackElems = 8;
+
+// Every operand of a segment sits at an address its element width divides: payload
+// operands at multiples of E, fp32 partials at multiples of 4.
+inline bool seg_operands_aligned(const Seg& s, int E) {
+  for (int k = 0; k < s.nsrc; ++k) {
+    const uintptr_t w = (k == 1 && (s.flags & kFlagSrc1F32)) ? 4 : (uintptr_t)E;
+    if (reinterpret_cast<uintptr_t>(s.src[k]) % w) return false;
+  }
+  const uintptr_t w = (s.flags & kFlagOutF32) ? 4 : (uintptr_t)E;
+  for (int d = 0; d < s.ndst; ++d)
+    if (reinterpret_cast<uintptr_t>(s.dst[d]) % w) return false;
+  return true;
+}
+
 struct Pass {
   relay_pass_kind_t kind;
   std::vector<Seg> segs;

@@ -266,14 +266,14 @@ def test_pass_names():
 
 # ------------------------------------------- bounds and races of every program (dry) --
 
-def _dry(coll, count, dt, A, R, sched, in_place):
+def _dry(coll, count, dt, A, R, sched, in_place, skew=0):
     """Run a collective in dry-run mode over fake, disjoint buffers of exactly the
     declared sizes: the library builds every pass and checks that each segment stays
     inside a declared buffer and that no launch races with itself; nothing launches."""
     opts = rv.make_opts(schedule=sched, flags=rv.FLAG_CHECK_HAZARDS | rv.FLAG_DRY_RUN)
     p = rv.relay_plan(coll, count, dt, A, R, opts)
     E = rv.ESIZE[dt]
-    base = lambda r, k: ((4 * r + k + 1) << 40) + 256 * (r % 3)
+    base = lambda r, k: ((4 * r + k + 1) << 40) + 256 * (r % 3) + skew * ((r + k) % 2)
     send, recv, scratch = [], [], []
     for a in range(A):
         s, r = base(a, 0), base(a, 1)
@@ -316,8 +316,9 @@ def test_every_program_stays_in_bounds_and_race_free(coll):
                                 rv.relay_plan(coll, count, dt, A, R, rv.make_opts(schedule=sched))
                             except rv.RelayError:
                                 continue
-                            st = _dry(coll, count, dt, A, R, sched, in_place)
-                            assert st == rv.OK, rv.lib().relay_last_error()
+                            for skew in (0, rv.ESIZE[dt]):
+                                st = _dry(coll, count, dt, A, R, sched, in_place, skew)
+                                assert st == rv.OK, rv.lib().relay_last_error()
                             n += 1
     assert n > 200
 
@@ -456,7 +457,9 @@ def test_wide_partial_plan_links_and_bounds(orc):
         narrow = rv.relay_plan(rv.REDUCE_SCATTER, m, rv.BF16, 4, 8,
                                rv.make_opts(schedule=rv.SCHEDULE_RELAY, flags=rv.FLAG_PAYLOAD_PARTIAL))
         assert p.wide_partial == 1 and narrow.wide_partial == 0
-        assert p.active_scratch_elems == narrow.active_scratch_elems + 4 * p.chunk
+        # fp32 partials take H*chunk more elements plus 8 of slack that lets them start on
+        # a 16-byte boundary
+        assert p.active_scratch_elems == narrow.active_scratch_elems + 4 * p.chunk + 8
         _, gv = orc.plan(rv.REDUCE_SCATTER, 4, 8, m, 2, force=rv.SCHEDULE_RELAY)
         exp = orc.link_elems(gv).astype(np.uint64) * np.uint64(2)
         assert np.array_equal(rv.relay_plan_link_bytes(narrow), exp)
@@ -464,21 +467,24 @@ def test_wide_partial_plan_links_and_bounds(orc):
         assert np.array_equal(rv.relay_plan_link_bytes(p), exp)
         for in_place in (False, True):
             for extra in (0, rv.FLAG_PAYLOAD_PARTIAL):
-                st = _dry_wide(m, in_place, extra)
-                assert st == rv.OK, rv.lib().relay_last_error()
+                for skew in (0, 2, 6, 14):      # bf16 scratch is only 2-byte aligned
+                    st = _dry_wide(m, in_place, extra, skew)
+                    assert st == rv.OK, rv.lib().relay_last_error()
     # fp32 payloads have nothing to widen
     p = rv.relay_plan(rv.REDUCE_SCATTER, 1 << 20, rv.F32, 4, 8, rv.make_opts(schedule=rv.SCHEDULE_RELAY))
     assert p.wide_partial == 0
 
 
-def _dry_wide(m, in_place, extra=0):
+def _dry_wide(m, in_place, extra=0, skew=0):
+    """Dry run with every buffer `skew` bytes past a 16-byte boundary: the host checks
+    (bounds, races, operand alignment: fp32 partials need 4 bytes) must all pass."""
     A, R, E = 4, 8, 2
     opts = rv.make_opts(schedule=rv.SCHEDULE_RELAY,
                         flags=extra | rv.FLAG_CHECK_HAZARDS | rv.FLAG_DRY_RUN)
-    send = [(r + 1) << 40 for r in range(A)]
+    send = [((r + 1) << 40) + skew for r in range(A)]
     recv = [s + r * m * E for r, s in enumerate(send)] if in_place else \
-        [((r + 10) << 40) for r in range(A)]
-    scratch = [((r + 20) << 40) for r in range(R)]
+        [((r + 10) << 40) + skew for r in range(A)]
+    scratch = [((r + 20) << 40) + skew for r in range(R)]
     arr = lambda xs: (ctypes.c_void_p * R)(*(xs + [None] * (R - len(xs))))
     return rv.lib().relay_reduce_scatter(arr(send), arr(recv), arr(scratch), m, rv.BF16, A, R,
                                          0.25, ctypes.byref(opts), None)
