@@ -270,9 +270,10 @@ def test_fused_launch_at_sizes_past_its_default(coll):
 
 def test_reduce_scatter_partial_precision():
     """4-active bf16 reduce-scatter. By default the helper partial crosses in fp32: results
-    match the oracle's wide reading bit for bit and sit within half a bf16 ulp of the
-    fp64 sum. With RELAY_FLAG_PAYLOAD_PARTIAL the partial crosses as bf16: results match
-    the oracle's payload-typed reading bit for bit."""
+    match the oracle's wide reading bit for bit and sit within one bf16 ulp of the fp64
+    sum (the fp32 partial is exact unless a tiny term needs more than 24 bits next to
+    large ones). With RELAY_FLAG_PAYLOAD_PARTIAL the partial crosses as bf16: results
+    match the oracle's payload-typed reading bit for bit."""
     for m, in_place in ((300_000, False), (250_001, True), (1 << 20, False)):
         for flags in (0, rv.FLAG_SEPARATE_PASSES, rv.FLAG_PAYLOAD_PARTIAL):
             c = hz.run(rv.REDUCE_SCATTER, 4, 8, m, rv.BF16, 0.25, config=19,
@@ -284,4 +285,4 @@ def test_reduce_scatter_partial_precision():
                 for o in range(4):
                     r64 = orc.reduce_scatter(rv.BF16, xs, m, o, 0.25, 0)[0]
                     got = orc.bf16_to_f32(hz.host(c.recv[o])).astype(np.float64)
-                    assert np.all(np.abs(got - r64) <= hz.bf16_ulp(r64.astype(np.float32)) / 2)
+                    assert np.all(np.abs(got - r64) <= hz.bf16_ulp(r64.astype(np.float32)))
