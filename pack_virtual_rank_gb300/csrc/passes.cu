@@ -416,6 +416,80 @@ __device__ __forceinline__ void unpack_f32x8(uint4 a, uint4 b, float* v) {
   v[6] = __uint_as_float(b.z); v[7] = __uint_as_float(b.w);
 }
 
+// Whole tiles of the two mixed-width segment kinds, with the same batching as the main
+// path (loads of a batch issued together). bf16 payload only: 8 elements per step.
+template <int NSRC>
+__device__ __forceinline__ void mixed_partial_full(const Seg& s, int64_t base) {
+  // NSRC bf16 slots summed in order into an fp32 partial (no scale)
+  constexpr int UB = NSRC <= 2 ? 4 : 2;
+  const int64_t v0 = base / 8 + threadIdx.x;
+#pragma unroll
+  for (int u0 = 0; u0 < kUnroll; u0 += UB) {
+    uint4 v[NSRC][UB];
+#pragma unroll
+    for (int u = 0; u < UB; ++u)
+#pragma unroll
+      for (int k = 0; k < NSRC; ++k)
+        v[k][u] = Mem<false>::v4(static_cast<const uint4*>(s.src[k]) + v0 + (u0 + u) * kThreads);
+#pragma unroll
+    for (int u = 0; u < UB; ++u) {
+      float acc[8], t[8];
+      TBF16::unpack(v[0][u], acc);
+#pragma unroll
+      for (int k = 1; k < NSRC; ++k) {
+        TBF16::unpack(v[k][u], t);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], t[i]);
+      }
+      const uint4 lo = make_uint4(__float_as_uint(acc[0]), __float_as_uint(acc[1]),
+                                  __float_as_uint(acc[2]), __float_as_uint(acc[3]));
+      const uint4 hi = make_uint4(__float_as_uint(acc[4]), __float_as_uint(acc[5]),
+                                  __float_as_uint(acc[6]), __float_as_uint(acc[7]));
+      const int64_t q = 2 * (v0 + (u0 + u) * kThreads);
+#pragma unroll
+      for (int d = 0; d < kMaxDst; ++d)
+        if (d < s.ndst) {
+          st_v4(static_cast<uint4*>(s.dst[d]) + q, lo);
+          st_v4(static_cast<uint4*>(s.dst[d]) + q + 1, hi);
+        }
+    }
+  }
+}
+
+__device__ __forceinline__ void mixed_final_full(const Seg& s, int64_t base, float scale) {
+  // a bf16 value plus an fp32 partial, scaled once, rounded to bf16
+  const int64_t v0 = base / 8 + threadIdx.x;
+  const bool do_scale = (s.flags & kFlagScale) != 0;
+#pragma unroll
+  for (int u0 = 0; u0 < kUnroll; u0 += 2) {
+    uint4 x[2], p0[2], p1[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int64_t vi = v0 + (u0 + u) * kThreads;
+      x[u] = Mem<false>::v4(static_cast<const uint4*>(s.src[0]) + vi);
+      p0[u] = Mem<false>::v4(static_cast<const uint4*>(s.src[1]) + 2 * vi);
+      p1[u] = Mem<false>::v4(static_cast<const uint4*>(s.src[1]) + 2 * vi + 1);
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      float acc[8], t[8];
+      TBF16::unpack(x[u], acc);
+      unpack_f32x8(p0[u], p1[u], t);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], t[i]);
+      if (do_scale) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = __fmul_rn(acc[i], scale);
+      }
+      const uint4 r = TBF16::pack(acc);
+      const int64_t vi = v0 + (u0 + u) * kThreads;
+#pragma unroll
+      for (int d = 0; d < kMaxDst; ++d)
+        if (d < s.ndst) st_v4(static_cast<uint4*>(s.dst[d]) + vi, r);
+    }
+  }
+}
+
 template <class P>
 __device__ __noinline__ void run_mixed_tile(const Seg& s, int64_t base, int64_t len, float scale) {
   const bool do_scale = (s.flags & kFlagScale) != 0;
@@ -499,7 +573,13 @@ __global__ void __launch_bounds__(kThreads, 5)
     const Seg& s = args.seg[lo];
     const int64_t base = (int64_t)(t - s.tile0) * kTile;
     const int64_t len = min(kTile, s.n - base);
-    if (MODE == kModeMixed) run_mixed_tile<P>(s, base, len, args.scale);
+    if (MODE == kModeMixed) {
+      const bool full = P::kE == 2 && (s.flags & kFlagVector) && len == kTile;
+      if (full && (s.flags & kFlagOutF32) && s.nsrc == 3 && s.ndst == 1) mixed_partial_full<3>(s, base);
+      else if (full && (s.flags & kFlagOutF32) && s.nsrc == 2 && s.ndst == 1) mixed_partial_full<2>(s, base);
+      else if (full && (s.flags & kFlagSrc1F32) && s.nsrc == 2) mixed_final_full(s, base, args.scale);
+      else run_mixed_tile<P>(s, base, len, args.scale);
+    }
     else if (MODE == kModeMain && (s.flags & kFlagVector) && len == kTile)
       run_full_tile<P, false>(s, base, args.scale);
     else if (MODE == kModeRealign && len == kTile) run_realign_tile<P>(s, base, args.scale);
