@@ -535,7 +535,8 @@ def run_sweep(args):
 def run_profile_case(args):
     """A named collective run W + K times under the library's default launch policy, for
     profiler captures of kernels the bench workload does not exercise (not a bench line).
-    Case: COLLECTIVE:A:DTYPE:COUNT[:relay], COUNT in the collective's own count."""
+    Case: COLLECTIVE:A:DTYPE:COUNT[:relay][:payload], COUNT in the collective's own count;
+    "payload" carries 4-active reduce-scatter partials in the payload type."""
     import torch
     import pack_virtual_rank_gb300.build as b
     b.build()
@@ -546,8 +547,8 @@ def run_profile_case(args):
     coll = {"allreduce": rv.ALLREDUCE, "reduce_scatter": rv.REDUCE_SCATTER,
             "all_gather": rv.ALL_GATHER, "all_to_all": rv.ALL_TO_ALL}[name]
     d = {"f32": rv.F32, "bf16": rv.BF16, "i32": rv.I32}[dt]
-    opts = rv.make_opts(schedule=rv.SCHEDULE_RELAY if rest and rest[0] == "relay"
-                        else rv.SCHEDULE_AUTO)
+    opts = rv.make_opts(schedule=rv.SCHEDULE_RELAY if "relay" in rest else rv.SCHEDULE_AUTO,
+                        flags=rv.FLAG_PAYLOAD_PARTIAL if "payload" in rest else 0)
     dev = torch.device("cuda", 0)
     plan = rv.relay_plan(coll, count, d, Ap, R, opts)
     xs = [synth.rank_input(9, r, plan.input_elems, dt, device=dev) for r in range(Ap)]

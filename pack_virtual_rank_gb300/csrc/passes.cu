@@ -553,9 +553,9 @@ __device__ __noinline__ void run_mixed_tile(const Seg& s, int64_t base, int64_t 
 }
 
 // MODE selects the segments a launch runs: kModeMain (aligned and per-element paths),
-// kModeRealign (realigned sources), kModeMixed (fp32 partials next to bf16). Each is its
-// own kernel so that the rarer variants' register needs do not cost the main path
-// occupancy. All run 5 CTAs per SM (48 registers): measured on GB300, the realigned
+// kModeRealign (realigned sources), kModeMixed (the main paths plus fp32 partials next to
+// bf16, so that a pass with wide partials stays one launch). Each is its own kernel so
+// that the rarer variants' register needs do not cost the main path occupancy. All run 5 CTAs per SM (48 registers): measured on GB300, the realigned
 // all-to-all passes gain more from occupancy than from more vectors per thread.
 constexpr int kModeMain = 0, kModeRealign = 1, kModeMixed = 2;
 
@@ -573,14 +573,14 @@ __global__ void __launch_bounds__(kThreads, 5)
     const Seg& s = args.seg[lo];
     const int64_t base = (int64_t)(t - s.tile0) * kTile;
     const int64_t len = min(kTile, s.n - base);
-    if (MODE == kModeMixed) {
+    if (MODE == kModeMixed && seg_mixed(s)) {
       const bool full = P::kE == 2 && (s.flags & kFlagVector) && len == kTile;
       if (full && (s.flags & kFlagOutF32) && s.nsrc == 3 && s.ndst == 1) mixed_partial_full<3>(s, base);
       else if (full && (s.flags & kFlagOutF32) && s.nsrc == 2 && s.ndst == 1) mixed_partial_full<2>(s, base);
       else if (full && (s.flags & kFlagSrc1F32) && s.nsrc == 2) mixed_final_full(s, base, args.scale);
       else run_mixed_tile<P>(s, base, len, args.scale);
     }
-    else if (MODE == kModeMain && (s.flags & kFlagVector) && len == kTile)
+    else if (MODE != kModeRealign && (s.flags & kFlagVector) && len == kTile)
       run_full_tile<P, false>(s, base, args.scale);
     else if (MODE == kModeRealign && len == kTile) run_realign_tile<P>(s, base, args.scale);
     else run_partial_tile<P, false>(s, base, len, args.scale);
@@ -841,6 +841,11 @@ cudaError_t launch_pass(int dtype, const Pass& pass, float scale, cudaStream_t s
   direct.clear();
   realigned.clear();
   for (const Seg& sg : segs) (sg.flags & kFlagRealign ? realigned : direct).push_back(sg);
+  if (!mixed.empty()) {
+    // one launch for the pass: the mixed-mode kernel also runs the plain segments
+    mixed.insert(mixed.end(), direct.begin(), direct.end());
+    direct.clear();
+  }
   switch (dtype) {
     case RELAY_F32: return launch_split<TF32>(direct, realigned, mixed, scale, stream);
     case RELAY_BF16: return launch_split<TBF16>(direct, realigned, mixed, scale, stream);

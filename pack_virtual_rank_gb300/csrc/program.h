@@ -16,6 +16,12 @@
 
 #include "relay.h"
 
+#ifdef __CUDACC__
+#define RELAY_HD __host__ __device__
+#else
+#define RELAY_HD
+#endif
+
 namespace relay {
 
 constexpr int kMaxSrc = 4;
@@ -55,7 +61,7 @@ inline int64_t seg_src_bytes(const Seg& s, int k, int E) {
 inline int64_t seg_dst_bytes(const Seg& s, int E) {
   return s.n * ((s.flags & kFlagOutF32) ? 4 : E);
 }
-inline bool seg_mixed(const Seg& s) { return (s.flags & (kFlagOutF32 | kFlagSrc1F32)) != 0; }
+RELAY_HD inline bool seg_mixed(const Seg& s) { return (s.flags & (kFlagOutF32 | kFlagSrc1F32)) != 0; }
 
 // bf16 elements of slack in an owner's scratch that let its fp32 partials start on a
 // 16-byte boundary whatever the scratch pointer's alignment (bf16 pointers are only
