@@ -273,8 +273,8 @@ void build_a4_reduce_scatter(Builder& B, const relay_plan_t& p) {
   // partial and returns that single chunk to the owner (group 2). The direct positions
   // go source -> owner in two parts (group 1, group 2). The owner scratch:
   //   [partials: H*oc positions, payload-typed | A-1 direct slots of pD], or, with fp32
-  //   partials, [partials: H*oc fp32 starting on the first 16-byte boundary within the
-  //   8-element slack | A-1 direct slots of pD].
+  //   partials, [H*oc fp32 partials, starting at the first 16-byte boundary, with
+  //   kWideSlackElems elements of slack in all | A-1 direct slots of pD].
   const int A = p.A, H = p.H;
   const int64_t m = p.count, oc = p.chunk, pD = p.direct_total;
   const int64_t P = H * oc;                      // offload positions per block

@@ -63,10 +63,12 @@ inline int64_t seg_dst_bytes(const Seg& s, int E) {
 }
 RELAY_HD inline bool seg_mixed(const Seg& s) { return (s.flags & (kFlagOutF32 | kFlagSrc1F32)) != 0; }
 
-// bf16 elements of slack in an owner's scratch that let its fp32 partials start on a
-// 16-byte boundary whatever the scratch pointer's alignment (bf16 pointers are only
-// 2-byte aligned; fp32 accesses need 4, the vector path 16).
-constexpr int64_t kWideSlackElems = 8;
+// bf16 elements of slack in an owner's scratch with fp32 partials. The partials start on
+// the first 16-byte boundary within the slack whatever the scratch pointer's alignment
+// (bf16 pointers are only 2-byte aligned; fp32 accesses need 4, the vector path 16), and
+// the direct slots after the slack keep the 256-byte offset they would have had: a
+// misalignment of the direct slots to the 128-byte lines cost ~6% on GB300.
+constexpr int64_t kWideSlackElems = 128;
 
 // Every operand of a segment sits at an address its element width divides: payload
 // operands at multiples of E, fp32 partials at multiples of 4.
