@@ -1,9 +1,9 @@
 // passes.cu -- the one streaming kernel behind every relay pass (sm_103a).
 //
 // A pass is a table of segments (program.h) executed by one launch. Each segment is
-// cut into tiles of 16 KiB of payload; the grid is persistent (a multiple of the SM
-// count) and walks the tiles of the whole table, so one launch covers every transfer
-// and reduction of a schedule group regardless of how many there are (the page
+// cut into tiles of 16 KiB of payload and the grid has one CTA per tile of the whole
+// table, so one launch covers every transfer and reduction of a schedule group
+// regardless of how many there are (the page
 // "Link-balance the sharded relay schedules (up to 3.2x vs NCCL)", item 5, blames the
 // per-op launch overhead of many small groups; here a group costs one launch).
 //
@@ -81,8 +81,10 @@ struct Mem<true> {
   }
 };
 __device__ __forceinline__ uint4 ld_stream_v4(const void* p) { return Mem<false>::v4(p); }
+// 16-byte stores are streaming (.cs, evict first): no pass re-reads its own output, and
+// on GB300 this measured 0.4-2.7% faster than default stores with one CTA per tile.
 __device__ __forceinline__ void st_v4(void* p, uint4 v) {
-  asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+  asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
                "r"(v.w)
                : "memory");
 }
@@ -676,20 +678,6 @@ int sm_count() {
 }
 
 template <class P, int CAP, int MODE>
-int blocks_per_sm() {
-  static int cached = 0;
-  if (cached == 0) {
-    int nb = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, relay_pass_kernel<P, CAP, MODE>, kThreads, 0) !=
-            cudaSuccess ||
-        nb <= 0)
-      nb = 1;
-    cached = nb;
-  }
-  return cached;
-}
-
-template <class P, int CAP, int MODE>
 cudaError_t launch_cap(const Seg* segs, int nseg, float scale, cudaStream_t stream) {
   static thread_local PassArgs<CAP> a;  // up to ~30 KiB: keep it off the stack
   constexpr int64_t kTile = kTileBytes / P::kE;
@@ -704,8 +692,10 @@ cudaError_t launch_cap(const Seg* segs, int nseg, float scale, cudaStream_t stre
   a.ntiles = (int32_t)tiles;
   a.scale = scale;
   a.pad = 0;
-  const int64_t cap = (int64_t)sm_count() * blocks_per_sm<P, CAP, MODE>();
-  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, cap));
+  // one CTA per tile: the block scheduler starts a new tile on an SM the moment one of
+  // its 5 resident CTAs finishes, which on GB300 streams ~11% faster than a persistent
+  // grid walking the tiles (that grid's CTAs load, then store, tile after tile in step)
+  const int grid = (int)std::max<int64_t>(1, tiles);
   relay_pass_kernel<P, CAP, MODE><<<grid, kThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
