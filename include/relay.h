@@ -85,7 +85,7 @@ typedef enum {
  * 4 passes and 128 segments, needs no realigned sources and records no pass events runs
  * as ONE cooperative launch whose passes are separated by grid-wide barriers; any other
  * call launches each pass separately. */
-#define RELAY_FUSED_MAX_BYTES (64ll << 20)
+#define RELAY_FUSED_MAX_BYTES (256ll << 20)
 #define RELAY_FLAG_PAYLOAD_PARTIAL 16 /* 4-active reduce-scatter, bf16 payload: carry each
                                       helper's partial to its owner in the payload type,
                                       one payload-sized chunk per return hop as in the link
