@@ -525,11 +525,90 @@ def run_sweep(args):
         print(json.dumps(row), flush=True)
         del xs, ys, scratch, graph
         torch.cuda.empty_cache()
+    rows += _sweep_fused_groups(rv, synth, dev, peak, flush, flush_read, args.steps)
+    rows += _sweep_flat_pack(rv, dev, peak, flush, flush_read, args.steps)
     if args.sweep_out:
         with open(args.sweep_out, "w") as f:
             json.dump({"peak_gbs": peak, "device_copy_gbs_this_run": round(copy_gbs, 1),
                        "rows": rows}, f, indent=1)
     return 0
+
+
+def _timed(fn, reps, flush, flush_read):
+    import torch
+    ts = []
+    for _ in range(reps):
+        flush.fill_(1.0)
+        flush_read.sum()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    return statistics.median(ts)
+
+
+def _sweep_fused_groups(rv, synth, dev, peak, flush, flush_read, reps):
+    """The fused multi-group call: every rank active in its own group and a helper in
+    the others, all groups' passes merged phase by phase (commits D115998367, D115998376)."""
+    import torch
+    rows = []
+    for name, coll, A, dt, per_rank in (("allreduce", rv.ALLREDUCE, 2, "bf16", 256 << 20),
+                                        ("allreduce", rv.ALLREDUCE, 4, "bf16", 512 << 20),
+                                        ("reduce_scatter", rv.REDUCE_SCATTER, 2, "bf16", 256 << 20)):
+        G = R // A
+        d = rv.dtype_code(dt)
+        elems = per_rank // rv.ESIZE[d]
+        count = elems if coll == rv.ALLREDUCE else elems // A
+        counts = [count] * G
+        plans = [rv.relay_plan(coll, c, d, A, R) for c in counts]
+        xs = [synth.rank_input(9, r, plans[r // A].input_elems, dt, device=dev) for r in range(R)]
+        ys = [torch.empty(plans[r // A].output_elems, dtype=xs[0].dtype, device=dev) for r in range(R)]
+        scratch = rv.alloc_multi_scratch(coll, counts, d, A, dev)
+        scale = 1.0 / A
+        call = lambda: rv.relay_multi_group(coll, counts, xs, ys, scratch, d, A, scale)
+        for _ in range(3):
+            call()
+        ms = _timed(call, reps, flush, flush_read)
+        # bytes: every group's passes (the fused call runs them all)
+        nbytes = sum(p["bytes_read"] + p["bytes_written"] for pl in plans for p in rv.relay_plan_passes(pl))
+        link = rv.relay_multi_group_link_bytes(coll, counts, d, A)
+        row = {"collective": f"{name} fused {G} groups", "A": A, "dtype": dt,
+               "bytes_per_rank": per_rank, "count": count, "schedule": "relay",
+               "link_cost_bytes": int(sum(t.max() for t in link)), "ms_median": round(ms, 4),
+               "gbs": round(nbytes / ms / 1e6, 1), "frac": round(nbytes / ms / 1e6 / peak, 3),
+               "passes": []}
+        rows.append(row)
+        print(json.dumps(row), flush=True)
+        del xs, ys, scratch
+        torch.cuda.empty_cache()
+    return rows
+
+
+def _sweep_flat_pack(rv, dev, peak, flush, flush_read, reps):
+    """Packing 256 caller tensors of mixed sizes (1 GiB of bf16 in all) into one flat
+    buffer and back, one launch each (the analogue of commit D115998366's pack/unpack)."""
+    import torch
+    g = torch.Generator().manual_seed(3)
+    sizes = torch.randint(1, 4 << 20, (256,), generator=g)
+    sizes = (sizes * ((1 << 29) / sizes.sum())).long().clamp(min=1).tolist()
+    ts = [torch.empty(n, dtype=torch.bfloat16, device=dev) for n in sizes]
+    flat = torch.empty(sum(sizes), dtype=torch.bfloat16, device=dev)
+    rows = []
+    for name, fn in (("pack_flat", lambda: rv.relay_pack_flat(ts, flat)),
+                     ("unpack_flat", lambda: rv.relay_unpack_flat(flat, ts))):
+        for _ in range(3):
+            fn()
+        ms = _timed(fn, reps, flush, flush_read)
+        nbytes = 2 * flat.numel() * 2
+        row = {"collective": name, "A": 0, "dtype": "bf16", "bytes_per_rank": flat.numel() * 2,
+               "count": len(ts), "schedule": "-", "link_cost_bytes": 0, "ms_median": round(ms, 4),
+               "gbs": round(nbytes / ms / 1e6, 1), "frac": round(nbytes / ms / 1e6 / peak, 3),
+               "passes": []}
+        rows.append(row)
+        print(json.dumps(row), flush=True)
+    return rows
 
 
 def run_profile_case(args):
