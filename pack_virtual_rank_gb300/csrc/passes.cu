@@ -274,7 +274,9 @@ template <class P, int NSRC>
 __device__ __forceinline__ void realign_full_tile(const Seg& s, int64_t base, float scale) {
   constexpr int L = P::kLanes;
   // vectors per source held at once (plus lane 31's neighbours)
-  constexpr int NB = NSRC == 1 ? 2 : 1;
+  // (copies of 4-byte payloads hold 4: +5% on the int32 all-to-all on GB300; bf16 copies
+  // hold 2, since 4 spilled there)
+  constexpr int NB = NSRC == 1 ? (P::kE == 4 ? 4 : 2) : 1;
   using Acc = typename P::Acc;
   const int64_t v0 = base / L + threadIdx.x;
   const bool last_lane = (threadIdx.x & 31u) == 31u;
