@@ -273,13 +273,15 @@ __device__ __forceinline__ uint4 shift_pair(uint4 lo, uint4 hi, unsigned sigma) 
 template <class P, int NSRC>
 __device__ __forceinline__ void realign_full_tile(const Seg& s, int64_t base, float scale) {
   constexpr int L = P::kLanes;
-  // vectors per source held at once (plus lane 31's neighbours)
-  // (copies of 4-byte payloads hold 4: +5% on the int32 all-to-all on GB300; bf16 copies
-  // hold 2, since 4 spilled there)
-  constexpr int NB = NSRC == 1 ? (P::kE == 4 ? 4 : 2) : 1;
+  // vectors per source in flight: all kUnroll for one source, 2 at a time for two
+  constexpr int NB = NSRC == 1 ? kUnroll : 2;
   using Acc = typename P::Acc;
-  const int64_t v0 = base / L + threadIdx.x;
-  const bool last_lane = (threadIdx.x & 31u) == 31u;
+  // Warp w covers the tile's vectors [w, w + 1) x 32 * kUnroll, lane l takes l + 32 * j:
+  // the block after lane 31's j-th is lane 0's (j+1)-th, so a warp loads only one extra
+  // block (lane 31's last neighbour) per batch instead of one per vector.
+  const unsigned lane = threadIdx.x & 31u;
+  const bool last_lane = lane == 31u;
+  const int64_t v0 = base / L + (int64_t)(threadIdx.x >> 5) * (32 * kUnroll) + lane;
   const bool do_scale = (s.flags & kFlagScale) != 0;
   unsigned sig[NSRC];
   const uint4* a[NSRC];
@@ -288,18 +290,16 @@ __device__ __forceinline__ void realign_full_tile(const Seg& s, int64_t base, fl
     sig[k] = (unsigned)(reinterpret_cast<uintptr_t>(s.src[k]) & 15u);
     a[k] = reinterpret_cast<const uint4*>(static_cast<const char*>(s.src[k]) - sig[k]);
   }
-#pragma unroll 1
+#pragma unroll
   for (int u = 0; u < kUnroll; u += NB) {
-    // one round trip: every lane's aligned block, and lane 31's right neighbour
-    uint4 cur[NSRC][NB], ext[NSRC][NB];
+    uint4 cur[NSRC][NB], ext[NSRC];
 #pragma unroll
     for (int j = 0; j < NB; ++j)
 #pragma unroll
-      for (int k = 0; k < NSRC; ++k) {
-        const int64_t vi = v0 + (u + j) * kThreads;
-        cur[k][j] = ld_stream_v4(a[k] + vi);
-        if (sig[k] != 0 && last_lane) ext[k][j] = ld_stream_v4(a[k] + vi + 1);
-      }
+      for (int k = 0; k < NSRC; ++k) cur[k][j] = ld_stream_v4(a[k] + v0 + (u + j) * 32);
+#pragma unroll
+    for (int k = 0; k < NSRC; ++k)
+      if (sig[k] != 0 && last_lane) ext[k] = ld_stream_v4(a[k] + v0 + (u + NB - 1) * 32 + 1);
 #pragma unroll
     for (int j = 0; j < NB; ++j) {
       uint4 v[NSRC];
@@ -307,12 +307,17 @@ __device__ __forceinline__ void realign_full_tile(const Seg& s, int64_t base, fl
       for (int k = 0; k < NSRC; ++k) {
         v[k] = cur[k][j];
         if (sig[k] != 0) {
+          // every lane reads its right neighbour's block; lane 0 offers its next one,
+          // which is what lane 31 needs
+          uint4 send = cur[k][j];
+          if (j + 1 < NB && lane == 0) send = cur[k][j + 1];
+          const int from = (int)((lane + 1) & 31u);
           uint4 nxt;
-          nxt.x = __shfl_down_sync(0xffffffffu, cur[k][j].x, 1);
-          nxt.y = __shfl_down_sync(0xffffffffu, cur[k][j].y, 1);
-          nxt.z = __shfl_down_sync(0xffffffffu, cur[k][j].z, 1);
-          nxt.w = __shfl_down_sync(0xffffffffu, cur[k][j].w, 1);
-          if (last_lane) nxt = ext[k][j];
+          nxt.x = __shfl_sync(0xffffffffu, send.x, from);
+          nxt.y = __shfl_sync(0xffffffffu, send.y, from);
+          nxt.z = __shfl_sync(0xffffffffu, send.z, from);
+          nxt.w = __shfl_sync(0xffffffffu, send.w, from);
+          if (j + 1 == NB && last_lane) nxt = ext[k];
           v[k] = shift_pair(cur[k][j], nxt, sig[k]);
         }
       }
@@ -332,7 +337,7 @@ __device__ __forceinline__ void realign_full_tile(const Seg& s, int64_t base, fl
         }
         r = P::pack(acc);
       }
-      const int64_t vi = v0 + (u + j) * kThreads;
+      const int64_t vi = v0 + (u + j) * 32;
 #pragma unroll
       for (int d = 0; d < kMaxDst; ++d)
         if (d < s.ndst) st_v4(static_cast<uint4*>(s.dst[d]) + vi, r);
