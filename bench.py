@@ -150,6 +150,51 @@ def _cpu_oracle(sample: int, seed_config: int = 2, inputs=None):
     return time.perf_counter() - t0
 
 
+def _host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def _cpu_model():
+    """The host CPU as /proc/cpuinfo names it (x86: model name; Arm: implementer/part)."""
+    import platform
+    try:
+        info = open("/proc/cpuinfo").read().split("\n")
+    except OSError:
+        return platform.machine()
+    for key in ("model name", "Model"):
+        for ln in info:
+            if ln.split(":")[0].strip() == key:
+                return ln.split(":", 1)[1].strip()
+    parts = {ln.split(":")[0].strip(): ln.split(":", 1)[1].strip() for ln in info if ":" in ln}
+    return f"{platform.machine()} implementer {parts.get('CPU implementer', '?')} " \
+           f"part {parts.get('CPU part', '?')}"
+
+
+def _cpu_oracle_all_cores(sample: int, seed_config: int = 2, inputs=None):
+    """The same oracle call on every host core at once: each thread runs the unchanged
+    oracle allreduce on its own contiguous range of the sample's elements (elementwise
+    collectives split by element without changing any result; the C call releases the
+    GIL). Returns (seconds, threads)."""
+    import concurrent.futures as cf
+    import oracle as orc
+    import synth
+    if inputs is None:
+        xs = [synth.to_numpy(synth.rank_input(seed_config, r, sample, "bf16")) for r in range(A)]
+    else:
+        xs = [synth.to_numpy(x[:sample]) for x in inputs]
+    nt = _host_cores()
+    cuts = [sample * t // nt for t in range(nt + 1)]
+    orc.lib()
+    with cf.ThreadPoolExecutor(nt) as ex:
+        t0 = time.perf_counter()
+        list(ex.map(lambda t: orc.allreduce(orc.BF16, xs, SCALE, cuts[t], cuts[t + 1]), range(nt)))
+        dt = time.perf_counter() - t0
+    return dt, nt
+
+
 def _bytes_per_step(plan, rv, count=None):
     if count is not None and count != plan.count:
         plan = rv.relay_plan(rv.ALLREDUCE, count, rv.BF16, A, R)
@@ -189,6 +234,7 @@ def run_reference(args):
     ts = [_cpu_oracle(CPU_SAMPLE) for _ in range(args.steps)]
     total = sum(ts)
     value = nbytes * args.steps / total / 1e9
+    t_all, cores = _cpu_oracle_all_cores(CPU_SAMPLE)
     sample = (f"oracle allreduce (bf16, A=2, fp32 sum, scale 1/2) on {CPU_SAMPLE} elements per "
               f"rank per step; GB/s counts the relay schedule's algorithmic bytes for that count")
     line = {"impl": "reference", "metric": "relay-pass HBM GB/s (allreduce A=2 of R=8, bf16)",
@@ -198,7 +244,12 @@ def run_reference(args):
             "data": "synthetic (seeded N(0,1) bf16)",
             "config": {"workload": WORKLOAD, "sample_count": CPU_SAMPLE, "A": A, "R": R},
             "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": 1,
-                             "kind": "oracle", "sample": sample},
+                             "kind": "oracle", "sample": sample, "cpu_model": _cpu_model(),
+                             "all_cores": {"value": round(nbytes / t_all / 1e9, 3),
+                                           "cores": cores,
+                                           "how": "one step's sample split into one contiguous "
+                                                  "element range per host thread, each running "
+                                                  "the unchanged oracle"}},
             "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
@@ -316,6 +367,7 @@ def run_ours(args):
         tr = traffic.get(passes[top]["name"]) if traffic else None
         sample = min(CPU_BASELINE_SAMPLE, count)
         cpu_t = None if args.kernel_only else _cpu_oracle(sample, inputs=hx)
+        cpu_all = None if args.kernel_only else _cpu_oracle_all_cores(sample, inputs=hx)
         cpu_bytes, _ = _bytes_per_step(plan, rv, sample)
         cpu_val = cpu_bytes / cpu_t / 1e9 if cpu_t else None
         line = {
@@ -345,7 +397,12 @@ def run_ours(args):
                 "value": round(cpu_val, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
                 "sample": f"oracle allreduce on the first {sample} elements of each rank's "
                           f"bench input ({cpu_t:.2f} s); GB/s counts the relay schedule's "
-                          "algorithmic bytes for that count"},
+                          "algorithmic bytes for that count",
+                "cpu_model": _cpu_model(),
+                "all_cores": {"value": round(cpu_bytes / cpu_all[0] / 1e9, 3), "cores": cpu_all[1],
+                              "seconds": round(cpu_all[0], 3),
+                              "how": "the same sample split into one contiguous element range "
+                                     "per host thread, each running the unchanged oracle"}},
             "e2e": None if e2e is None else {
                 "value": round(e2e, 2), "unit": "GB/s", "h2d_bytes_per_step": A * count * 2,
                 "d2h_bytes_per_step": A * count * 2, "steps": e2e_steps,
