@@ -195,6 +195,31 @@ def _cpu_oracle_all_cores(sample: int, seed_config: int = 2, inputs=None):
     return dt, nt
 
 
+def _calibrate_link(rv, host_in, dev_buf, host_out, ctas, nbytes=256 << 20):
+    """Host-link rates on this GPU, both directions, for the copy engines (torch copies)
+    and for relay_copy with `ctas` CTAs: the median of 3 timed copies of `nbytes`."""
+    import torch
+    n = min(nbytes // host_in.element_size(), host_in.numel())
+    hi, d, ho = host_in[:n], dev_buf[:n], host_out[:n]
+    ways = {"h2d_engine_gbs": lambda: d.copy_(hi, non_blocking=True),
+            "h2d_kernel_gbs": lambda: rv.relay_copy(d, hi, max_ctas=ctas),
+            "d2h_engine_gbs": lambda: ho.copy_(d, non_blocking=True),
+            "d2h_kernel_gbs": lambda: rv.relay_copy(ho, d, max_ctas=ctas)}
+    out = {}
+    for k, fn in ways.items():
+        fn()
+        ts = []
+        for _ in range(3):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        out[k] = round(n * host_in.element_size() / statistics.median(ts) / 1e6, 1)
+    return out
+
+
 def _bytes_per_step(plan, rv, count=None):
     if count is not None and count != plan.count:
         plan = rv.relay_plan(rv.ALLREDUCE, count, rv.BF16, A, R)
@@ -320,6 +345,16 @@ def run_ours(args):
         hy = [torch.empty(count, dtype=torch.bfloat16).pin_memory() for _ in range(A)]
         sets = [(xs, ys), ([torch.empty_like(x) for x in xs], [torch.empty_like(y) for y in ys])]
         s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+        # host-link copies: the library's kernel with half a CTA per SM (it reaches the
+        # link's rate and leaves the other CTA slots to the passes), or the copy engines
+        link_ctas = args.e2e_ctas or max(1, torch.cuda.get_device_properties(dev).multi_processor_count // 2)
+        e2e_mode, calib = args.e2e_copy, None
+        if e2e_mode == "auto":
+            calib = _calibrate_link(rv, hx[0], xs[0], hy[0], link_ctas)
+            e2e_mode = {(True, True): "library", (True, False): "library-in",
+                        (False, True): "library-out", (False, False): "torch"}[
+                (calib["h2d_kernel_gbs"] > 1.1 * calib["h2d_engine_gbs"],
+                 calib["d2h_kernel_gbs"] > 1.1 * calib["d2h_engine_gbs"])]
         ev = lambda: torch.cuda.Event()
         done_in = [ev() for _ in range(e2e_steps)]
         done_comp = [ev() for _ in range(e2e_steps)]
@@ -335,7 +370,10 @@ def run_ours(args):
                 if k >= 2:
                     s_in.wait_event(done_comp[k - 2])   # set k%2's inputs are free again
                 for a in range(A):
-                    bx[a].copy_(hx[a], non_blocking=True)
+                    if e2e_mode in ("torch", "library-out"):
+                        bx[a].copy_(hx[a], non_blocking=True)
+                    else:
+                        rv.relay_copy(bx[a], hx[a], max_ctas=link_ctas, stream=s_in)
                 done_in[k].record(s_in)
             stream.wait_event(done_in[k])
             if k >= 2:
@@ -346,7 +384,10 @@ def run_ours(args):
             with torch.cuda.stream(s_out):
                 s_out.wait_event(done_comp[k])
                 for a in range(A):
-                    hy[a].copy_(by[a], non_blocking=True)
+                    if e2e_mode in ("library", "library-out"):
+                        rv.relay_copy(hy[a], by[a], max_ctas=link_ctas, stream=s_out)
+                    else:
+                        hy[a].copy_(by[a], non_blocking=True)
                 done_out[k].record(s_out)
         stream.wait_event(done_out[e2e_steps - 1])
         e1.record(stream)
@@ -407,7 +448,16 @@ def run_ours(args):
                 "value": round(e2e, 2), "unit": "GB/s", "h2d_bytes_per_step": A * count * 2,
                 "d2h_bytes_per_step": A * count * 2, "steps": e2e_steps,
                 "note": "pinned host inputs copied in and results copied out every step; "
-                        "two device buffer sets overlap the copies with the passes"},
+                        "two device buffer sets overlap the copies with the passes",
+                "copies": {"library": "relay_copy both ways",
+                           "library-in": "relay_copy in, copy engine out",
+                           "library-out": "copy engine in, relay_copy out",
+                           "torch": "copy engines both ways"}[e2e_mode]
+                          + ("" if e2e_mode == "torch" else f" ({link_ctas} CTAs)")
+                          + ("" if calib is None else
+                             ", the faster way per direction on this GPU (calibration "
+                             "outside the timed region, GB/s: "
+                             + ", ".join(f"{k} {v}" for k, v in calib.items()) + ")")},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks,
         }
@@ -737,6 +787,11 @@ def main():
     ap.add_argument("--sweep-out", default=None, help="write the sweep table as JSON here")
     ap.add_argument("--graph", action="store_true",
                     help="sweep: replay each call from a CUDA graph (device time without host gaps)")
+    ap.add_argument("--e2e-copy", choices=["auto", "library", "library-in", "library-out", "torch"],
+                    default="auto",
+                    help="how the end-to-end leg moves inputs in and results out")
+    ap.add_argument("--e2e-ctas", type=int, default=0,
+                    help="CTA cap of the end-to-end leg's relay_copy launches (0: half the SMs)")
     ap.add_argument("--kernel-only", action="store_true",
                     help="time the device passes only (no end-to-end leg, no CPU baseline)")
     args = ap.parse_args()

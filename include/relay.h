@@ -289,6 +289,28 @@ relay_status_t relay_unpack_flat(const void* flat, void* const* dsts, const size
                                  relay_dtype_t dtype, cudaStream_t stream);
 
 /*
+ * relay_copy -- copies `count` elements of `dtype` from `src` to `dst` with the library's
+ * streaming kernel, asynchronously on `stream`. It is how callers stage a collective's
+ * inputs into HBM and its results back out when those live in host memory. The page has
+ * no counterpart: its buffers always sit in device memory.
+ *   - Either pointer may be device memory, pinned or registered host memory, or (only
+ *     where the device reports cudaDevAttrPageableMemoryAccess) ordinary pageable host
+ *     memory. The SMs load and store across the host link themselves. On GB300 this
+ *     reaches the link's rate whether or not the copy engines do.
+ *   - max_ctas caps the CTAs of the launch. Each CTA then walks 16 KiB tiles. 0 means
+ *     one CTA per tile, the fastest form for device-to-device copies. A copy over the host
+ *     link reaches the link's rate with about one CTA per SM, which leaves the other CTA
+ *     slots to kernels running at the same time on other streams.
+ *   - Pointers must be element-aligned, and the two ranges must not overlap.
+ *   - count == 0 returns RELAY_OK without a launch.
+ *   - Errors: RELAY_ERR_INVALID_ARGUMENT (NULL, misaligned, overlapping, max_ctas < 0);
+ *     RELAY_ERR_UNSUPPORTED (pageable host memory on a device that cannot address it);
+ *     RELAY_ERR_CUDA (pointer query or launch failure).
+ */
+relay_status_t relay_copy(void* dst, const void* src, size_t count, relay_dtype_t dtype,
+                          int max_ctas, cudaStream_t stream);
+
+/*
  * relay_allreduce_noalloc -- an allreduce for callers that cannot allocate device
  * memory when they call it (an allocator or memory-pool hook that would recurse into
  * itself, a process that reserved all of HBM at start-up, a path that cannot take the

@@ -17,4 +17,4 @@ from ._binding import (  # noqa: F401
     relay_plan_passes, relay_reduce_scatter, group_ranks, relay_multi_group,
     relay_multi_group_link_bytes, alloc_multi_scratch, relay_pack_flat, relay_unpack_flat,
     relay_allreduce_noalloc, relay_helper_size, relay_active_scratch_size,
-    relay_helper_contract_size)
+    relay_helper_contract_size, relay_copy)

@@ -118,6 +118,8 @@ def lib():
     L.relay_pack_flat.restype = i32
     L.relay_unpack_flat.argtypes = [vp, arr, P(sz), i32, i32, vp]
     L.relay_unpack_flat.restype = i32
+    L.relay_copy.argtypes = [vp, vp, sz, i32, i32, vp]
+    L.relay_copy.restype = i32
     if L.relay_abi_version() != 1:
         raise RuntimeError("librelay.so ABI version mismatch")
     _lib = L
@@ -381,3 +383,24 @@ def relay_unpack_flat(flat, tensors: Sequence, dtype=None, stream=None) -> None:
     counts = (ctypes.c_size_t * max(n, 1))(*[t.numel() for t in tensors])
     _check(lib().relay_unpack_flat(_ptr(flat), (ctypes.c_void_p * max(n, 1))(*[_ptr(t) for t in tensors]),
                                    counts, n, dt, _stream(stream)))
+
+
+# ---------------------------------------------------------------------- host link --
+
+def _any_ptr(x) -> int:
+    """Address of a contiguous tensor in device memory or host memory (pinned or not)."""
+    if isinstance(x, int):
+        return x
+    if not x.is_contiguous():
+        raise ValueError("relay_copy tensors must be contiguous")
+    return x.data_ptr()
+
+
+def relay_copy(dst, src, max_ctas: int = 0, stream=None) -> None:
+    """Copy `src` into `dst` (same dtype and numel) with the library's streaming kernel.
+    Either may be a CUDA tensor or a host tensor (pinned, or pageable where the device
+    reads host page tables); max_ctas caps the launch's CTAs (0: one per 16 KiB tile)."""
+    if dst.dtype != src.dtype or dst.numel() != src.numel():
+        raise ValueError("relay_copy: dst and src must have the same dtype and size")
+    _check(lib().relay_copy(_any_ptr(dst), _any_ptr(src), src.numel(), dtype_code(src.dtype),
+                            max_ctas, _stream(stream)))

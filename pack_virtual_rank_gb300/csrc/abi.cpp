@@ -525,6 +525,70 @@ relay_status_t relay_unpack_flat(const void* flat, void* const* dsts, const size
                    false, stream);
 }
 
+// Where the device can reach `p`: device or managed memory and pinned/registered host
+// memory through their device address, pageable host memory only on devices that read
+// the host's page tables. *dev receives the address the kernel uses.
+static relay_status_t device_view(const void* p, const char* what, const void** dev) {
+  cudaPointerAttributes at{};
+  cudaError_t e = cudaPointerGetAttributes(&at, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(RELAY_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+  }
+  if (at.type == cudaMemoryTypeUnregistered) {
+    int d = 0, pageable = 0;
+    if (cudaGetDevice(&d) != cudaSuccess ||
+        cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccess, d) != cudaSuccess) {
+      cudaGetLastError();
+      return fail(RELAY_ERR_CUDA, std::string(what) + ": device query failed");
+    }
+    if (!pageable)
+      return fail(RELAY_ERR_UNSUPPORTED,
+                  std::string(what) + " is pageable host memory this device cannot address");
+    *dev = p;
+    return RELAY_OK;
+  }
+  if (at.type == cudaMemoryTypeHost && at.devicePointer != nullptr) {
+    // the device address of this byte: the allocation's device base + the same offset
+    *dev = static_cast<const char*>(at.devicePointer) +
+           (static_cast<const char*>(p) - static_cast<const char*>(at.hostPointer));
+    return RELAY_OK;
+  }
+  *dev = p;
+  return RELAY_OK;
+}
+
+relay_status_t relay_copy(void* dst, const void* src, size_t count, relay_dtype_t dtype,
+                          int max_ctas, cudaStream_t stream) {
+  if (dtype < RELAY_F32 || dtype > RELAY_I32) return fail(RELAY_ERR_INVALID_ARGUMENT, "unknown dtype");
+  if (max_ctas < 0) return fail(RELAY_ERR_INVALID_ARGUMENT, "max_ctas < 0");
+  if (count == 0) return RELAY_OK;
+  if (count > (size_t)INT64_MAX / 16) return fail(RELAY_ERR_INVALID_ARGUMENT, "count too large");
+  if (dst == nullptr || src == nullptr) return fail(RELAY_ERR_INVALID_ARGUMENT, "NULL pointer");
+  const int E = esize_of(dtype);
+  if ((reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src)) % E)
+    return fail(RELAY_ERR_INVALID_ARGUMENT, "pointer not element-aligned");
+  const uintptr_t s0 = reinterpret_cast<uintptr_t>(src), d0 = reinterpret_cast<uintptr_t>(dst);
+  const uintptr_t bytes = (uintptr_t)count * E;
+  relay_status_t st = check_disjoint({Range{s0, s0 + bytes, "src"}, Range{d0, d0 + bytes, "dst"}});
+  if (st != RELAY_OK) return st;
+  const void *sv = nullptr, *dv = nullptr;
+  if ((st = device_view(src, "src", &sv)) != RELAY_OK) return st;
+  if ((st = device_view(dst, "dst", &dv)) != RELAY_OK) return st;
+  Pass ps{RELAY_PASS_PACK, {}, {}};
+  Seg sg{};
+  sg.src[0] = sv;
+  sg.dst[0] = const_cast<void*>(dv);
+  sg.n = (int64_t)count;
+  sg.op = kOpCopy;
+  sg.nsrc = sg.ndst = 1;
+  ps.segs.push_back(sg);
+  ps.meta.push_back(SegMeta{-1, 0, {0, -1, -1, -1}});
+  const cudaError_t e = launch_pass(dtype, ps, 1.0f, stream, max_ctas);
+  if (e != cudaSuccess) return fail(RELAY_ERR_CUDA, cudaGetErrorString(e));
+  return RELAY_OK;
+}
+
 relay_status_t relay_multi_group_link_bytes(relay_coll_t coll, int num_groups,
                                             const size_t* counts, relay_dtype_t dtype, int A,
                                             const relay_opts_t* opts, uint64_t* out, size_t cap,

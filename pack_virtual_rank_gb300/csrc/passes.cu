@@ -685,7 +685,8 @@ int sm_count() {
 }
 
 template <class P, int CAP, int MODE>
-cudaError_t launch_cap(const Seg* segs, int nseg, float scale, cudaStream_t stream) {
+cudaError_t launch_cap(const Seg* segs, int nseg, float scale, cudaStream_t stream,
+                       int max_ctas) {
   static thread_local PassArgs<CAP> a;  // up to ~30 KiB: keep it off the stack
   constexpr int64_t kTile = kTileBytes / P::kE;
   int64_t tiles = 0;
@@ -701,23 +702,26 @@ cudaError_t launch_cap(const Seg* segs, int nseg, float scale, cudaStream_t stre
   a.pad = 0;
   // one CTA per tile: the block scheduler starts a new tile on an SM the moment one of
   // its 5 resident CTAs finishes, which on GB300 streams ~11% faster than a persistent
-  // grid walking the tiles (that grid's CTAs load, then store, tile after tile in step)
-  const int grid = (int)std::max<int64_t>(1, tiles);
+  // grid walking the tiles (that grid's CTAs load, then store, tile after tile in step).
+  // A capped grid (copies over the host link) walks the tiles instead.
+  const int64_t want = max_ctas > 0 ? std::min<int64_t>(tiles, max_ctas) : tiles;
+  const int grid = (int)std::max<int64_t>(1, want);
   relay_pass_kernel<P, CAP, MODE><<<grid, kThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
 template <class P, int MODE>
-cudaError_t launch_typed(const std::vector<Seg>& segs, float scale, cudaStream_t stream) {
+cudaError_t launch_typed(const std::vector<Seg>& segs, float scale, cudaStream_t stream,
+                         int max_ctas) {
   constexpr int kMaxCap = 384;  // 16 + 384 * 80 bytes of parameters, under the 32 KiB limit
   size_t i = 0;
   while (i < segs.size()) {
     const int n = (int)std::min<size_t>(segs.size() - i, kMaxCap);
     cudaError_t e;
-    if (n <= 8) e = launch_cap<P, 8, MODE>(segs.data() + i, n, scale, stream);
-    else if (n <= 32) e = launch_cap<P, 32, MODE>(segs.data() + i, n, scale, stream);
-    else if (n <= 128) e = launch_cap<P, 128, MODE>(segs.data() + i, n, scale, stream);
-    else e = launch_cap<P, kMaxCap, MODE>(segs.data() + i, n, scale, stream);
+    if (n <= 8) e = launch_cap<P, 8, MODE>(segs.data() + i, n, scale, stream, max_ctas);
+    else if (n <= 32) e = launch_cap<P, 32, MODE>(segs.data() + i, n, scale, stream, max_ctas);
+    else if (n <= 128) e = launch_cap<P, 128, MODE>(segs.data() + i, n, scale, stream, max_ctas);
+    else e = launch_cap<P, kMaxCap, MODE>(segs.data() + i, n, scale, stream, max_ctas);
     if (e != cudaSuccess) return e;
     i += n;
   }
@@ -802,11 +806,13 @@ namespace {
 
 template <class P>
 cudaError_t launch_split(const std::vector<Seg>& direct, const std::vector<Seg>& realigned,
-                         const std::vector<Seg>& mixed, float scale, cudaStream_t stream) {
+                         const std::vector<Seg>& mixed, float scale, cudaStream_t stream,
+                         int max_ctas) {
   cudaError_t e = cudaSuccess;
-  if (!direct.empty()) e = launch_typed<P, kModeMain>(direct, scale, stream);
-  if (e == cudaSuccess && !realigned.empty()) e = launch_typed<P, kModeRealign>(realigned, scale, stream);
-  if (e == cudaSuccess && !mixed.empty()) e = launch_typed<P, kModeMixed>(mixed, scale, stream);
+  if (!direct.empty()) e = launch_typed<P, kModeMain>(direct, scale, stream, max_ctas);
+  if (e == cudaSuccess && !realigned.empty())
+    e = launch_typed<P, kModeRealign>(realigned, scale, stream, max_ctas);
+  if (e == cudaSuccess && !mixed.empty()) e = launch_typed<P, kModeMixed>(mixed, scale, stream, max_ctas);
   return e;
 }
 
@@ -815,7 +821,8 @@ cudaError_t launch_split(const std::vector<Seg>& direct, const std::vector<Seg>&
 // Segments with realigned sources, and mixed-width segments, go to their own launches
 // after the others; the launches of one pass touch disjoint memory, so their order does
 // not matter.
-cudaError_t launch_pass(int dtype, const Pass& pass, float scale, cudaStream_t stream) {
+cudaError_t launch_pass(int dtype, const Pass& pass, float scale, cudaStream_t stream,
+                        int max_ctas) {
   static thread_local std::vector<Seg> plain, segs, direct, realigned, mixed;
   plain.clear();
   mixed.clear();
@@ -844,9 +851,9 @@ cudaError_t launch_pass(int dtype, const Pass& pass, float scale, cudaStream_t s
     direct.clear();
   }
   switch (dtype) {
-    case RELAY_F32: return launch_split<TF32>(direct, realigned, mixed, scale, stream);
-    case RELAY_BF16: return launch_split<TBF16>(direct, realigned, mixed, scale, stream);
-    default: return launch_split<TI32>(direct, realigned, mixed, scale, stream);
+    case RELAY_F32: return launch_split<TF32>(direct, realigned, mixed, scale, stream, max_ctas);
+    case RELAY_BF16: return launch_split<TBF16>(direct, realigned, mixed, scale, stream, max_ctas);
+    default: return launch_split<TI32>(direct, realigned, mixed, scale, stream, max_ctas);
   }
 }
 

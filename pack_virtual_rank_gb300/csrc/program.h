@@ -117,7 +117,9 @@ void build_multi_program(const std::vector<relay_plan_t>& plans, const std::vect
 
 // Launch one pass on `stream` -- passes.cu. Splits into several launches when the
 // segment table exceeds one launch's parameter capacity.
-cudaError_t launch_pass(int dtype, const Pass& pass, float scale, cudaStream_t stream);
+// max_ctas > 0 caps each launch's grid (its CTAs then walk the tiles); 0 is one CTA per tile.
+cudaError_t launch_pass(int dtype, const Pass& pass, float scale, cudaStream_t stream,
+                        int max_ctas = 0);
 
 // Launch every pass of a small call as one cooperative kernel with grid barriers between
 // the passes -- passes.cu. Returns false (and launches nothing) when the call does not

@@ -422,6 +422,21 @@ def test_flat_pack_validation():
     assert rv.lib().relay_pack_flat(arr([None]), c, 0, None, 0, None) == rv.OK
 
 
+def test_copy_validation():
+    L = rv.lib()
+    # nothing to copy: no launch, no pointer check
+    assert L.relay_copy(None, None, 0, rv.BF16, 0, None) == rv.OK
+    assert L.relay_copy(None, 1 << 40, 16, rv.BF16, 0, None) == rv.ERR_INVALID_ARGUMENT
+    # a negative CTA cap, an unknown dtype, a misaligned pointer
+    assert L.relay_copy(2 << 40, 1 << 40, 16, rv.BF16, -1, None) == rv.ERR_INVALID_ARGUMENT
+    assert L.relay_copy(2 << 40, 1 << 40, 16, 7, 0, None) == rv.ERR_INVALID_ARGUMENT
+    assert L.relay_copy((2 << 40) + 2, 1 << 40, 16, rv.F32, 0, None) == rv.ERR_INVALID_ARGUMENT
+    # overlapping ranges (either way round)
+    assert L.relay_copy((1 << 40) + 30, 1 << 40, 16, rv.BF16, 0, None) == rv.ERR_INVALID_ARGUMENT
+    assert L.relay_copy(1 << 40, (1 << 40) + 30, 16, rv.BF16, 0, None) == rv.ERR_INVALID_ARGUMENT
+    assert "overlap" in L.relay_last_error().decode()
+
+
 def test_size_queries_and_page_contract(orc):
     for coll in range(4):
         for A in (2, 4):
