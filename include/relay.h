@@ -82,9 +82,9 @@ typedef enum {
 #define RELAY_FLAG_FUSED_PASSES 8  /* one cooperative launch for the whole call whenever it
                                       qualifies, whatever its size */
 /* Launch policy: a call of at most RELAY_FUSED_MAX_BYTES of pass traffic that has at most
- * 4 passes and 128 segments, needs no realigned sources and records no pass events runs
- * as ONE cooperative launch whose passes are separated by grid-wide barriers; any other
- * call launches each pass separately. */
+ * 4 passes and 384 segments (after alignment splitting), has no mixed-width (fp32 partial)
+ * segments and records no pass events runs as ONE cooperative launch whose passes are
+ * separated by grid-wide barriers; any other call launches each pass separately. */
 #define RELAY_FUSED_MAX_BYTES (256ll << 20)
 #define RELAY_FLAG_PAYLOAD_PARTIAL 16 /* 4-active reduce-scatter, bf16 payload: carry each
                                       helper's partial to its owner in the payload type,

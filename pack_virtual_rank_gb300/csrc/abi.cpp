@@ -196,7 +196,7 @@ relay_status_t execute(const std::vector<Pass>& passes, const std::vector<Range>
       }
     if ((flags & RELAY_FLAG_FUSED_PASSES) || bytes <= RELAY_FUSED_MAX_BYTES) {
       cudaError_t e = cudaSuccess;
-      if (launch_fused(dtype, passes, scale, stream, &e)) {
+      if (launch_fused(dtype, passes, scale, stream, &e, (flags & RELAY_FLAG_FUSED_PASSES) != 0)) {
         if (e != cudaSuccess) return fail(RELAY_ERR_CUDA, cudaGetErrorString(e));
         return RELAY_OK;
       }

@@ -414,6 +414,73 @@ __device__ __noinline__ void run_partial_tile(const Seg& s, int64_t base, int64_
   }
 }
 
+// Every tile of a realigned segment in the one-launch kernel: each thread takes whole
+// vectors, loads the two aligned blocks a vector's source bytes straddle and funnel-shifts
+// them (no shuffles, since any subset of lanes may hold a vector), then finishes the tail
+// per element.
+template <class P, bool COH>
+__device__ __noinline__ void run_partial_realign_tile(const Seg& s, int64_t base, int64_t len,
+                                                      float scale) {
+  using Acc = typename P::Acc;
+  constexpr int L = P::kLanes;
+  const bool do_scale = (s.flags & kFlagScale) != 0;
+  const bool copy = s.op == kOpCopy;
+  {
+    const int64_t vb = base / L, nvec = len / L;
+#pragma unroll 1
+    for (int64_t vi = threadIdx.x; vi < nvec; vi += kThreads) {
+      uint4 v[2];
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        if (k >= s.nsrc) break;
+        const unsigned sig = (unsigned)(reinterpret_cast<uintptr_t>(s.src[k]) & 15u);
+        const uint4* a = reinterpret_cast<const uint4*>(static_cast<const char*>(s.src[k]) - sig);
+        v[k] = Mem<COH>::v4(a + vb + vi);
+        if (sig != 0) v[k] = shift_pair(v[k], Mem<COH>::v4(a + vb + vi + 1), sig);
+      }
+      uint4 r = v[0];
+      if (!copy) {
+        Acc acc[L], t[L];
+        P::unpack(v[0], acc);
+        if (s.nsrc == 2) {
+          P::unpack(v[1], t);
+#pragma unroll
+          for (int i = 0; i < L; ++i) acc[i] = P::add(acc[i], t[i]);
+        }
+        if (do_scale) {
+#pragma unroll
+          for (int i = 0; i < L; ++i) acc[i] = P::scale(acc[i], scale);
+        }
+        r = P::pack(acc);
+      }
+#pragma unroll 1
+      for (int d = 0; d < s.ndst; ++d) st_v4(static_cast<uint4*>(s.dst[d]) + vb + vi, r);
+    }
+    // the last < L elements one at a time (copies move raw bits)
+#pragma unroll 1
+    for (int64_t e = nvec * L + threadIdx.x; e < len; e += kThreads) {
+      const int64_t off = (base + e) * P::kE;
+      if (copy) {
+        if (P::kE == 4) {
+          const uint32_t x = Mem<COH>::u32(static_cast<const char*>(s.src[0]) + off);
+#pragma unroll 1
+          for (int d = 0; d < s.ndst; ++d) st_u32(static_cast<char*>(s.dst[d]) + off, x);
+        } else {
+          const uint16_t x = Mem<COH>::u16(static_cast<const char*>(s.src[0]) + off);
+#pragma unroll 1
+          for (int d = 0; d < s.ndst; ++d) st_u16(static_cast<char*>(s.dst[d]) + off, x);
+        }
+        continue;
+      }
+      Acc acc = P::template load1<COH>(static_cast<const char*>(s.src[0]) + off);
+      if (s.nsrc == 2) acc = P::add(acc, P::template load1<COH>(static_cast<const char*>(s.src[1]) + off));
+      if (do_scale) acc = P::scale(acc, scale);
+#pragma unroll 1
+      for (int d = 0; d < s.ndst; ++d) P::store1(static_cast<char*>(s.dst[d]) + off, acc);
+    }
+  }
+}
+
 // Mixed-width segments of the wide-partial reduce-scatter (bf16 payload): a helper
 // summing bf16 slots into an fp32 partial (kFlagOutF32), and an owner adding its bf16 value
 // and the fp32 partial (kFlagSrc1F32). 8 elements per step: one 16-byte bf16 vector or
@@ -602,7 +669,14 @@ __global__ void __launch_bounds__(kThreads, 5)
 // uniform). For calls small enough that the fixed cost of a launch per pass dominates.
 
 constexpr int kMaxFusedPasses = 4;
-constexpr int kFusedCap = 128;
+constexpr int kFusedCap = 384;  // 48 + 384 * 80 bytes of parameters, under the 32 KiB limit
+// Calls with more segments than this fuse only when some of them need realigning (whose
+// per-pass form costs a second launch per pass) and their traffic is at most
+// kFusedManyBytes: on GB300 a 54 MiB-per-rank aligned all-to-all (172 segments, 241 MB of
+// traffic) ran 42 us pass by pass and 49 us fused, a misaligned one 67 us and 70 us, while
+// a misaligned 13 MiB one ran 45 us pass by pass and 23 us fused.
+constexpr int kFusedPlainCap = 128;
+constexpr int64_t kFusedManyBytes = 128ll << 20;
 
 struct FusedArgs {
   int32_t npass;
@@ -612,8 +686,11 @@ struct FusedArgs {
   Seg seg[kFusedCap];                  // tile0 counts from the start of its pass
 };
 
+// 4 CTAs per SM (64 registers): with its realigning path the kernel spills at 48, and on
+// GB300 the 4-CTA build was as fast or faster on every small call measured (a 16 MiB
+// 2-active allreduce 22.7 -> 20.6 us).
 template <class P>
-__global__ void __launch_bounds__(kThreads, 5) relay_fused_kernel(const __grid_constant__ FusedArgs args) {
+__global__ void __launch_bounds__(kThreads, 4) relay_fused_kernel(const __grid_constant__ FusedArgs args) {
   namespace cg = cooperative_groups;
   constexpr int64_t kTile = kTileBytes / P::kE;
   for (int p = 0; p < args.npass; ++p) {
@@ -627,6 +704,7 @@ __global__ void __launch_bounds__(kThreads, 5) relay_fused_kernel(const __grid_c
       const int64_t base = (int64_t)(t - s.tile0) * kTile;
       const int64_t len = min(kTile, s.n - base);
       if ((s.flags & kFlagVector) && len == kTile) run_full_tile<P, true>(s, base, args.scale);
+      else if (s.flags & kFlagRealign) run_partial_realign_tile<P, true>(s, base, len, args.scale);
       else run_partial_tile<P, true>(s, base, len, args.scale);
     }
     if (p + 1 < args.npass) cg::this_grid().sync();
@@ -767,7 +845,7 @@ cudaError_t launch_fused_typed(FusedArgs& a, int max_tiles, cudaStream_t stream)
 }  // namespace
 
 bool launch_fused(int dtype, const std::vector<Pass>& passes, float scale, cudaStream_t stream,
-                  cudaError_t* err) {
+                  cudaError_t* err, bool forced) {
   *err = cudaSuccess;
   if (passes.size() < 2 || passes.size() > (size_t)kMaxFusedPasses || !cooperative_supported())
     return false;
@@ -776,6 +854,8 @@ bool launch_fused(int dtype, const std::vector<Pass>& passes, float scale, cudaS
   const int E = esize_of(dtype);
   const int64_t tile = kTileBytes / E;
   int n = 0, max_tiles = 0;
+  bool realign = false;
+  int64_t traffic = 0;
   a.npass = (int32_t)passes.size();
   a.scale = scale;
   for (size_t p = 0; p < passes.size(); ++p) {
@@ -783,7 +863,9 @@ bool launch_fused(int dtype, const std::vector<Pass>& passes, float scale, cudaS
     a.seg0[p] = n;
     int64_t tiles = 0;
     for (const Seg& sg : segs) {
-      if ((sg.flags & kFlagRealign) || seg_mixed(sg) || n >= kFusedCap) return false;
+      if (seg_mixed(sg) || n >= kFusedCap) return false;
+      realign |= (sg.flags & kFlagRealign) != 0;
+      traffic += sg.n * E * (sg.nsrc + sg.ndst);
       a.seg[n] = sg;
       a.seg[n].tile0 = (int32_t)tiles;
       tiles += (sg.n + tile - 1) / tile;
@@ -793,6 +875,7 @@ bool launch_fused(int dtype, const std::vector<Pass>& passes, float scale, cudaS
     a.ntiles[p] = (int32_t)tiles;
     max_tiles = std::max<int>(max_tiles, (int)tiles);
   }
+  if (!forced && n > kFusedPlainCap && (!realign || traffic > kFusedManyBytes)) return false;
   a.seg0[passes.size()] = n;
   switch (dtype) {
     case RELAY_F32: *err = launch_fused_typed<TF32>(a, max_tiles, stream); break;

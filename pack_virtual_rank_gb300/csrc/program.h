@@ -123,10 +123,11 @@ cudaError_t launch_pass(int dtype, const Pass& pass, float scale, cudaStream_t s
 
 // Launch every pass of a small call as one cooperative kernel with grid barriers between
 // the passes -- passes.cu. Returns false (and launches nothing) when the call does not
-// qualify: more than 4 passes, more than 128 segments, a segment needing realigned
-// sources, or no cooperative launch on this device.
+// qualify: more than 4 passes, more than 384 segments after alignment splitting, a
+// mixed-width segment, or no cooperative launch on this device. Unless `forced`, it also
+// declines calls of more than 128 segments that the per-pass launches run faster.
 bool launch_fused(int dtype, const std::vector<Pass>& passes, float scale, cudaStream_t stream,
-                  cudaError_t* err);
+                  cudaError_t* err, bool forced = false);
 
 // Record `msg` as this thread's last error and return `st` -- abi.cpp.
 relay_status_t report_error(relay_status_t st, const std::string& msg);

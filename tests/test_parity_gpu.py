@@ -221,10 +221,13 @@ def test_cuda_graph_capture_and_replay():
             assert np.array_equal(hz.host(y), r)
 
 
+@pytest.mark.parametrize("policy", [0, rv.FLAG_SEPARATE_PASSES, rv.FLAG_FUSED_PASSES])
 @pytest.mark.parametrize("dtype", [rv.F32, rv.BF16, rv.I32])
-def test_realigned_sources_span_whole_tiles(dtype):
+def test_realigned_sources_span_whole_tiles(dtype, policy):
     """Odd counts put sources at different offsets modulo 16 bytes from their
-    destinations over many whole tiles: the register-realigned vector path."""
+    destinations over many whole tiles: the register-realigned vector path of the per-pass
+    kernel, and the two-block path of the one-launch kernel (forced, and as the default
+    policy picks it)."""
     cases = [(rv.ALL_TO_ALL, 4, 200_003), (rv.ALL_TO_ALL, 2, 300_001),
              (rv.REDUCE_SCATTER, 2, 300_001), (rv.REDUCE_SCATTER, 4, 250_001),
              (rv.ALL_GATHER, 4, 500_001), (rv.ALLREDUCE, 4, 1_000_001)]
@@ -234,7 +237,7 @@ def test_realigned_sources_span_whole_tiles(dtype):
             if in_place and coll == rv.ALL_TO_ALL:
                 continue
             c = hz.run(coll, A, 8, count, dtype, scale, config=13, schedule=rv.SCHEDULE_RELAY,
-                       in_place=in_place)
+                       in_place=in_place, flags=policy)
             hz.check_all(c)
 
 
