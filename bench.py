@@ -58,6 +58,32 @@ def _peaks():
         return 6800.0, "fallback"
 
 
+def _theoretical_hbm_gbs(dev):
+    """The device's own figure: 2 transfers per memory clock x bus width (None where this
+    PyTorch does not expose the clock or the width)."""
+    import ctypes
+    import torch
+    pr = torch.cuda.get_device_properties(dev)
+    khz, bits = getattr(pr, "memory_clock_rate", 0), getattr(pr, "memory_bus_width", 0)
+    if not khz or not bits:
+        # older PyTorch: ask the CUDA runtime (memory clock in kHz = attribute 36, global
+        # memory bus width in bits = attribute 37)
+        for name in ("libcudart.so", "/usr/local/cuda/lib64/libcudart.so"):
+            try:
+                rt = ctypes.CDLL(name)
+            except OSError:
+                continue
+            v36, v37 = ctypes.c_int(0), ctypes.c_int(0)
+            idx = dev.index if hasattr(dev, "index") and dev.index is not None else 0
+            if rt.cudaDeviceGetAttribute(ctypes.byref(v36), 36, idx) == 0 and \
+                    rt.cudaDeviceGetAttribute(ctypes.byref(v37), 37, idx) == 0:
+                khz, bits = v36.value, v37.value
+            break
+    if not khz or not bits:
+        return None
+    return round(2 * khz * 1e3 * bits / 8 / 1e9, 1)
+
+
 def _profiled_traffic():
     """Per-launch DRAM bytes of the dominant pass from the committed ncu summary, or
     None when the kernel source changed since the counters were taken."""
@@ -339,7 +365,7 @@ def run_ours(args):
     # public call, and copies its results back to pinned host memory. Two device buffer
     # sets let step k+1's input copy and step k-1's result copy overlap step k's passes
     # (copy-in, compute and copy-out each on their own stream, ordered by events).
-    e2e_ms, e2e_steps = None, max(2, min(args.steps, 8))
+    e2e_ms, e2e_steps, calib = None, max(2, min(args.steps, 8)), None
     if not args.kernel_only:
         hx = [x.cpu().pin_memory() for x in xs]
         hy = [torch.empty(count, dtype=torch.bfloat16).pin_memory() for _ in range(A)]
@@ -399,6 +425,14 @@ def run_ours(args):
 
     if rank == 0:
         peak, peak_kind = _peaks()
+        theo = _theoretical_hbm_gbs(dev)
+        # end-to-end ceiling: each direction's bytes at the faster calibrated single-direction
+        # rate, both directions at once (full duplex, no interference: an upper bound)
+        link_ceiling = None
+        if calib:
+            t_in = A * count * 2 / (max(calib["h2d_engine_gbs"], calib["h2d_kernel_gbs"]) * 1e9)
+            t_out = A * count * 2 / (max(calib["d2h_engine_gbs"], calib["d2h_kernel_gbs"]) * 1e9)
+            link_ceiling = round(nbytes / max(t_in, t_out) / 1e9, 1)
         value = whole_job_gbs(nbytes, args.steps, world, ms)
         e2e = whole_job_gbs(nbytes, e2e_steps, world, e2e_ms) if e2e_ms else None
         top = max(range(npass), key=lambda i: per_pass[i])
@@ -433,6 +467,8 @@ def run_ours(args):
                          "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": tr,
                          "peak_source": f"{peak_kind} hbm_gbs (copy, burst)",
+                         "hbm_theoretical_gbs": theo,
+                         "frac_of_theoretical": None if not theo else round(achieved / theo, 4),
                          "algorithmic_bytes_per_launch": top_bytes},
             "cpu_baseline": None if cpu_t is None else {
                 "value": round(cpu_val, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
@@ -449,6 +485,8 @@ def run_ours(args):
                 "d2h_bytes_per_step": A * count * 2, "steps": e2e_steps,
                 "note": "pinned host inputs copied in and results copied out every step; "
                         "two device buffer sets overlap the copies with the passes",
+                "link_ceiling_gbs": link_ceiling,
+                "frac_of_link_ceiling": None if not link_ceiling else round(e2e / link_ceiling, 3),
                 "copies": {"library": "relay_copy both ways",
                            "library-in": "relay_copy in, copy engine out",
                            "library-out": "copy engine in, relay_copy out",
@@ -637,6 +675,7 @@ def run_sweep(args):
     if args.sweep_out:
         with open(args.sweep_out, "w") as f:
             json.dump({"peak_gbs": peak, "device_copy_gbs_this_run": round(copy_gbs, 1),
+                       "hbm_theoretical_gbs": _theoretical_hbm_gbs(dev),
                        "rows": rows}, f, indent=1)
     return 0
 
