@@ -84,6 +84,17 @@ def _theoretical_hbm_gbs(dev):
     return round(2 * khz * 1e3 * bits / 8 / 1e9, 1)
 
 
+def kernel_code_sha() -> str:
+    """First 16 hex digits of the SHA-256 of the kernel source's code: comments removed and
+    every run of whitespace folded to one space, so that an edit to a comment does not void
+    the recorded counters while any change to the code does."""
+    text = open(KERNEL_SRC).read()
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    text = " ".join(text.split())
+    return hashlib.sha256(text.encode()).hexdigest()[:16]
+
+
 def _profiled_traffic():
     """Per-launch DRAM bytes of the dominant pass from the committed ncu summary, or
     None when the kernel source changed since the counters were taken."""
@@ -91,8 +102,8 @@ def _profiled_traffic():
         text = open(PROFILE).read()
     except OSError:
         return None, None
-    sha = hashlib.sha256(open(KERNEL_SRC, "rb").read()).hexdigest()[:16]
-    m_sha = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    sha = kernel_code_sha()
+    m_sha = re.search(r"kernel_code_sha256_16:\s*([0-9a-f]+)", text)
     out = {}
     for m in re.finditer(r"traffic_bytes_per_launch\[(\w+)\]:\s*([0-9]+)", text):
         out[m.group(1)] = int(m.group(2))

@@ -241,9 +241,9 @@ __device__ __forceinline__ void run_full_tile(const Seg& s, int64_t base, float 
 // Destinations 16-byte aligned, sources at any element offset (an all-to-all whose
 // segmentCount is not a multiple of the vector width, an odd recvCount): each lane loads
 // the aligned 16-byte vector that holds the start of its source range, takes the next
-// one from its right neighbour by a warp shuffle (lane 31 loads it itself), and funnel-
-// shifts the pair by the source's byte offset. Reads stay inside the 16-byte blocks
-// that hold the segment's own bytes.
+// one from its right neighbour by a warp shuffle, and funnel-shifts the pair by the
+// source's byte offset (the full-tile path below; the one-launch kernel loads both blocks
+// itself). Reads stay inside the 16-byte blocks that hold the segment's own bytes.
 
 __device__ __forceinline__ uint4 shift_pair(uint4 lo, uint4 hi, unsigned sigma) {
   const unsigned r = (sigma & 3u) * 8u;
