@@ -539,6 +539,44 @@ def _sweep_points():
     return pts
 
 
+ORACLE_SWEEP_SAMPLE = 1 << 23  # input elements per active rank in the sweep's oracle timing
+
+
+def _sweep_oracle(rv, coll, A, dt, opts0):
+    """The oracle timed beside a sweep row: the collective's results for a bounded sample
+    (ORACLE_SWEEP_SAMPLE input elements per active rank) computed by the unchanged oracle
+    on one host core -- one call for allreduce and all-gather (every active gets the same
+    result), one per owner or destination for reduce-scatter and all-to-all. GB/s counts the
+    relay schedule's algorithmic bytes for the sample's count, as the bench's CPU leg does."""
+    import oracle as orc
+    import synth
+    d = rv.dtype_code(dt)
+    S = ORACLE_SWEEP_SAMPLE
+    count = {rv.ALLREDUCE: S, rv.REDUCE_SCATTER: S // A, rv.ALL_GATHER: S,
+             rv.ALL_TO_ALL: S // (A * (A - 1))}[coll]
+    plan = rv.relay_plan(coll, count, d, A, R, opts0)
+    xs = [synth.to_numpy(synth.rank_input(9, r, plan.input_elems, dt)) for r in range(A)]
+    od = {rv.F32: orc.F32, rv.BF16: orc.BF16, rv.I32: orc.I32}[d]
+    scale = 1.0 if (d == rv.I32 or coll in (rv.ALL_GATHER, rv.ALL_TO_ALL)) else 1.0 / A
+    orc.lib()
+    t0 = time.perf_counter()
+    if coll == rv.ALLREDUCE:
+        orc.allreduce(od, xs, scale)
+    elif coll == rv.REDUCE_SCATTER:
+        rs = orc.reduce_scatter_wide if plan.wide_partial else orc.reduce_scatter
+        for o in range(A):
+            rs(od, xs, count, o, scale, plan.relay_total)
+    elif coll == rv.ALL_GATHER:
+        orc.all_gather(xs, count)
+    else:
+        for dst in range(A):
+            orc.all_to_all(xs, count, dst)
+    sec = time.perf_counter() - t0
+    nbytes = sum(p["bytes_read"] + p["bytes_written"] for p in rv.relay_plan_passes(plan))
+    return {"gbs": round(nbytes / sec / 1e9, 3), "seconds": round(sec, 3), "cores": 1,
+            "sample_count": count, "kind": "oracle"}
+
+
 def run_sweep(args):
     """Per collective and count: each pass's time (CUDA events; before every repetition
     a buffer twice the L2 is written and another read, so L2 holds no dirty lines),
@@ -677,6 +715,10 @@ def run_sweep(args):
             row.update({"ms_call_default_policy": round(wm, 4),
                         "gbs_call_default_policy": round(tot_b / wm / 1e6, 1),
                         "frac_call_default_policy": round(tot_b / wm / 1e6 / peak, 3)})
+        key = (name, A, dt, sched)
+        if sched in ("auto", "relay") and nbytes == max(b for n2, a2, d2, b, s2 in _sweep_points()
+                                                        if (n2, a2, d2, s2) == key):
+            row["oracle"] = _sweep_oracle(rv, coll, A, dt, opts0)
         rows.append(row)
         print(json.dumps(row), flush=True)
         del xs, ys, scratch, graph
