@@ -232,29 +232,50 @@ def _cpu_oracle_all_cores(sample: int, seed_config: int = 2, inputs=None):
     return dt, nt
 
 
-def _calibrate_link(rv, host_in, dev_buf, host_out, ctas, nbytes=256 << 20):
-    """Host-link rates on this GPU, both directions, for the copy engines (torch copies)
-    and for relay_copy with `ctas` CTAs: the median of 3 timed copies of `nbytes`."""
+def _calibrate_link(rv, host_in, dev_in, dev_out, host_out, ctas, nbytes=256 << 20):
+    """Host-link rates on this GPU for the copy engines (torch copies) and for relay_copy
+    with `ctas` CTAs: each direction alone, then every pairing of the two directions
+    running at once on two streams, as the end-to-end leg runs them (median of 3, `nbytes`
+    each way). Returns (rates in GB/s, the fastest pairing)."""
     import torch
     n = min(nbytes // host_in.element_size(), host_in.numel())
-    hi, d, ho = host_in[:n], dev_buf[:n], host_out[:n]
-    ways = {"h2d_engine_gbs": lambda: d.copy_(hi, non_blocking=True),
-            "h2d_kernel_gbs": lambda: rv.relay_copy(d, hi, max_ctas=ctas),
-            "d2h_engine_gbs": lambda: ho.copy_(d, non_blocking=True),
-            "d2h_kernel_gbs": lambda: rv.relay_copy(ho, d, max_ctas=ctas)}
-    out = {}
-    for k, fn in ways.items():
-        fn()
+    hi, di, do, ho = host_in[:n], dev_in[:n], dev_out[:n], host_out[:n]
+    eng_in = lambda: di.copy_(hi, non_blocking=True)
+    ker_in = lambda: rv.relay_copy(di, hi, max_ctas=ctas)
+    eng_out = lambda: ho.copy_(do, non_blocking=True)
+    ker_out = lambda: rv.relay_copy(ho, do, max_ctas=ctas)
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def timed(fin, fout):
         ts = []
-        for _ in range(3):
+        for rep in range(4):
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            fn()
-            e1.record()
+            cur = torch.cuda.current_stream()
+            e0.record(cur)
+            for st, fn in ((s_in, fin), (s_out, fout)):
+                if fn is None:
+                    continue
+                st.wait_event(e0)
+                with torch.cuda.stream(st):
+                    fn()
+                cur.wait_stream(st)
+            e1.record(cur)
             torch.cuda.synchronize()
-            ts.append(e0.elapsed_time(e1))
-        out[k] = round(n * host_in.element_size() / statistics.median(ts) / 1e6, 1)
-    return out
+            if rep:
+                ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts)
+
+    gb = n * host_in.element_size() / 1e6
+    out = {"h2d_engine_gbs": round(gb / timed(eng_in, None), 1),
+           "h2d_kernel_gbs": round(gb / timed(ker_in, None), 1),
+           "d2h_engine_gbs": round(gb / timed(None, eng_out), 1),
+           "d2h_kernel_gbs": round(gb / timed(None, ker_out), 1)}
+    pairs = {"torch": (eng_in, eng_out), "library-in": (ker_in, eng_out),
+             "library-out": (eng_in, ker_out), "library": (ker_in, ker_out)}
+    both = {m: timed(*fns) for m, fns in pairs.items()}
+    for m, t in both.items():
+        out[f"both_{m}_gbs_each"] = round(gb / t, 1)
+    return out, min(both, key=both.get)
 
 
 def _bytes_per_step(plan, rv, count=None):
@@ -387,11 +408,7 @@ def run_ours(args):
         link_ctas = args.e2e_ctas or max(1, torch.cuda.get_device_properties(dev).multi_processor_count // 2)
         e2e_mode, calib = args.e2e_copy, None
         if e2e_mode == "auto":
-            calib = _calibrate_link(rv, hx[0], xs[0], hy[0], link_ctas)
-            e2e_mode = {(True, True): "library", (True, False): "library-in",
-                        (False, True): "library-out", (False, False): "torch"}[
-                (calib["h2d_kernel_gbs"] > 1.1 * calib["h2d_engine_gbs"],
-                 calib["d2h_kernel_gbs"] > 1.1 * calib["d2h_engine_gbs"])]
+            calib, e2e_mode = _calibrate_link(rv, hx[0], xs[0], ys[0], hy[0], link_ctas)
         ev = lambda: torch.cuda.Event()
         done_in = [ev() for _ in range(e2e_steps)]
         done_comp = [ev() for _ in range(e2e_steps)]
@@ -439,11 +456,14 @@ def run_ours(args):
         theo = _theoretical_hbm_gbs(dev)
         # end-to-end ceiling: each direction's bytes at the faster calibrated single-direction
         # rate, both directions at once (full duplex, no interference: an upper bound)
-        link_ceiling = None
+        link_ceiling = link_pair = None
         if calib:
             t_in = A * count * 2 / (max(calib["h2d_engine_gbs"], calib["h2d_kernel_gbs"]) * 1e9)
             t_out = A * count * 2 / (max(calib["d2h_engine_gbs"], calib["d2h_kernel_gbs"]) * 1e9)
             link_ceiling = round(nbytes / max(t_in, t_out) / 1e9, 1)
+            # the same with both directions at the rate the chosen pairing reached together
+            pair_rate = calib[f"both_{e2e_mode}_gbs_each"] * 1e9
+            link_pair = round(nbytes / (A * count * 2 / pair_rate) / 1e9, 1)
         value = whole_job_gbs(nbytes, args.steps, world, ms)
         e2e = whole_job_gbs(nbytes, e2e_steps, world, e2e_ms) if e2e_ms else None
         top = max(range(npass), key=lambda i: per_pass[i])
@@ -498,14 +518,16 @@ def run_ours(args):
                         "two device buffer sets overlap the copies with the passes",
                 "link_ceiling_gbs": link_ceiling,
                 "frac_of_link_ceiling": None if not link_ceiling else round(e2e / link_ceiling, 3),
+                "link_pair_bound_gbs": link_pair,
+                "frac_of_link_pair_bound": None if not link_pair else round(e2e / link_pair, 3),
                 "copies": {"library": "relay_copy both ways",
                            "library-in": "relay_copy in, copy engine out",
                            "library-out": "copy engine in, relay_copy out",
                            "torch": "copy engines both ways"}[e2e_mode]
                           + ("" if e2e_mode == "torch" else f" ({link_ctas} CTAs)")
                           + ("" if calib is None else
-                             ", the faster way per direction on this GPU (calibration "
-                             "outside the timed region, GB/s: "
+                             ", the fastest pairing of the two directions running at once on "
+                             "this GPU (calibration outside the timed region, GB/s: "
                              + ", ".join(f"{k} {v}" for k, v in calib.items()) + ")")},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks,
