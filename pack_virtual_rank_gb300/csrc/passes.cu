@@ -270,8 +270,13 @@ __device__ __forceinline__ uint4 shift_pair(uint4 lo, uint4 hi, unsigned sigma) 
   return o;
 }
 
-template <class P, int NSRC>
-__device__ __forceinline__ void realign_full_tile(const Seg& s, int64_t base, float scale) {
+// TAIL: a segment's last, partial tile. Only its first `nvec` whole vectors are stored; a
+// block is loaded only if it holds bytes of those vectors (the block after the last one
+// holds its final bytes when the source is misaligned), so every read stays inside the
+// segment's own 16-byte blocks. The shuffles still run on every lane.
+template <class P, int NSRC, bool TAIL = false>
+__device__ __forceinline__ void realign_full_tile(const Seg& s, int64_t base, float scale,
+                                                  int nvec = 0) {
   constexpr int L = P::kLanes;
   // vectors per source in flight: all kUnroll for one source, 2 at a time for two
   constexpr int NB = NSRC == 1 ? kUnroll : 2;
@@ -281,14 +286,17 @@ __device__ __forceinline__ void realign_full_tile(const Seg& s, int64_t base, fl
   // block (lane 31's last neighbour) per batch instead of one per vector.
   const unsigned lane = threadIdx.x & 31u;
   const bool last_lane = lane == 31u;
-  const int64_t v0 = base / L + (int64_t)(threadIdx.x >> 5) * (32 * kUnroll) + lane;
+  const int lv0 = (int)(threadIdx.x >> 5) * (32 * kUnroll) + (int)lane;  // within the tile
+  const int64_t v0 = base / L + lv0;
   const bool do_scale = (s.flags & kFlagScale) != 0;
   unsigned sig[NSRC];
   const uint4* a[NSRC];
+  int last_blk[NSRC];  // TAIL: last block index (within the tile) that may be read
 #pragma unroll
   for (int k = 0; k < NSRC; ++k) {
     sig[k] = (unsigned)(reinterpret_cast<uintptr_t>(s.src[k]) & 15u);
     a[k] = reinterpret_cast<const uint4*>(static_cast<const char*>(s.src[k]) - sig[k]);
+    last_blk[k] = sig[k] != 0 ? nvec : nvec - 1;
   }
 #pragma unroll
   for (int u = 0; u < kUnroll; u += NB) {
@@ -296,10 +304,16 @@ __device__ __forceinline__ void realign_full_tile(const Seg& s, int64_t base, fl
 #pragma unroll
     for (int j = 0; j < NB; ++j)
 #pragma unroll
-      for (int k = 0; k < NSRC; ++k) cur[k][j] = ld_stream_v4(a[k] + v0 + (u + j) * 32);
+      for (int k = 0; k < NSRC; ++k) {
+        if (!TAIL || lv0 + (u + j) * 32 <= last_blk[k])
+          cur[k][j] = ld_stream_v4(a[k] + v0 + (u + j) * 32);
+        else
+          cur[k][j] = make_uint4(0u, 0u, 0u, 0u);
+      }
 #pragma unroll
     for (int k = 0; k < NSRC; ++k)
-      if (sig[k] != 0 && last_lane) ext[k] = ld_stream_v4(a[k] + v0 + (u + NB - 1) * 32 + 1);
+      if (sig[k] != 0 && last_lane && (!TAIL || lv0 + (u + NB - 1) * 32 + 1 <= last_blk[k]))
+        ext[k] = ld_stream_v4(a[k] + v0 + (u + NB - 1) * 32 + 1);
 #pragma unroll
     for (int j = 0; j < NB; ++j) {
       uint4 v[NSRC];
@@ -338,6 +352,7 @@ __device__ __forceinline__ void realign_full_tile(const Seg& s, int64_t base, fl
         r = P::pack(acc);
       }
       const int64_t vi = v0 + (u + j) * 32;
+      if (TAIL && lv0 + (u + j) * 32 >= nvec) continue;
 #pragma unroll
       for (int d = 0; d < kMaxDst; ++d)
         if (d < s.ndst) st_v4(static_cast<uint4*>(s.dst[d]) + vi, r);
@@ -351,6 +366,39 @@ template <class P>
 __device__ __forceinline__ void run_realign_tile(const Seg& s, int64_t base, float scale) {
   if (s.nsrc == 1) realign_full_tile<P, 1>(s, base, scale);
   else realign_full_tile<P, 2>(s, base, scale);
+}
+
+// The last, partial tile of a realigned segment: its whole vectors on the shuffle path,
+// then the last < L elements one at a time (copies move raw bits).
+template <class P>
+__device__ __forceinline__ void run_realign_tail(const Seg& s, int64_t base, int64_t len,
+                                                 float scale) {
+  using Acc = typename P::Acc;
+  const int nvec = (int)(len / P::kLanes);
+  if (s.nsrc == 1) realign_full_tile<P, 1, true>(s, base, scale, nvec);
+  else realign_full_tile<P, 2, true>(s, base, scale, nvec);
+  const bool copy = s.op == kOpCopy;
+#pragma unroll 1
+  for (int64_t e = (int64_t)nvec * P::kLanes + threadIdx.x; e < len; e += kThreads) {
+    const int64_t off = (base + e) * P::kE;
+    if (copy) {
+      if (P::kE == 4) {
+        const uint32_t x = Mem<false>::u32(static_cast<const char*>(s.src[0]) + off);
+#pragma unroll 1
+        for (int d = 0; d < s.ndst; ++d) st_u32(static_cast<char*>(s.dst[d]) + off, x);
+      } else {
+        const uint16_t x = Mem<false>::u16(static_cast<const char*>(s.src[0]) + off);
+#pragma unroll 1
+        for (int d = 0; d < s.ndst; ++d) st_u16(static_cast<char*>(s.dst[d]) + off, x);
+      }
+      continue;
+    }
+    Acc acc = P::template load1<false>(static_cast<const char*>(s.src[0]) + off);
+    if (s.nsrc == 2) acc = P::add(acc, P::template load1<false>(static_cast<const char*>(s.src[1]) + off));
+    if (s.flags & kFlagScale) acc = P::scale(acc, scale);
+#pragma unroll 1
+    for (int d = 0; d < s.ndst; ++d) P::store1(static_cast<char*>(s.dst[d]) + off, acc);
+  }
 }
 
 // The last, partial tile of a segment and every tile of a segment whose pointers are
@@ -631,12 +679,15 @@ __device__ __noinline__ void run_mixed_tile(const Seg& s, int64_t base, int64_t 
 // MODE selects the segments a launch runs: kModeMain (aligned and per-element paths),
 // kModeRealign (realigned sources), kModeMixed (the main paths plus fp32 partials next to
 // bf16, so that a pass with wide partials stays one launch). Each is its own kernel so
-// that the rarer variants' register needs do not cost the main path occupancy. All run 5 CTAs per SM (48 registers): measured on GB300, the realigned
-// all-to-all passes gain more from occupancy than from more vectors per thread.
+// that the rarer variants' register needs do not cost the main path occupancy. Main and
+// mixed run 5 CTAs per SM (48 registers). The realign kernel runs 4 (64 registers): with
+// its vectorized partial tiles it spilled at 48, and on GB300 the 4-CTA build ran 1 GiB
+// all-to-alls as fast as the spill-free 5-CTA one without them, and misaligned 54-135 MiB
+// all-to-alls 10-22% faster.
 constexpr int kModeMain = 0, kModeRealign = 1, kModeMixed = 2;
 
 template <class P, int CAP, int MODE>
-__global__ void __launch_bounds__(kThreads, 5)
+__global__ void __launch_bounds__(kThreads, MODE == kModeRealign ? 4 : 5)
     relay_pass_kernel(const __grid_constant__ PassArgs<CAP> args) {
   constexpr int64_t kTile = kTileBytes / P::kE;
   for (int t = blockIdx.x; t < args.ntiles; t += gridDim.x) {
@@ -659,6 +710,7 @@ __global__ void __launch_bounds__(kThreads, 5)
     else if (MODE != kModeRealign && (s.flags & kFlagVector) && len == kTile)
       run_full_tile<P, false>(s, base, args.scale);
     else if (MODE == kModeRealign && len == kTile) run_realign_tile<P>(s, base, args.scale);
+    else if (MODE == kModeRealign) run_realign_tail<P>(s, base, len, args.scale);
     else run_partial_tile<P, false>(s, base, len, args.scale);
   }
 }
