@@ -178,11 +178,18 @@ relay_status_t execute(const std::vector<Pass>& passes, const std::vector<Range>
   const int E = esize_of(dtype);
   std::string why;
   const int flags = opts ? opts->flags : 0;
-  if (flags & RELAY_FLAG_CHECK_HAZARDS)
+  if (flags & RELAY_FLAG_CHECK_HAZARDS) {
     for (const Pass& ps : passes) {
       if (find_out_of_bounds(ps, E, ranges, &why) || find_hazard(ps, E, &why))
         return fail(RELAY_ERR_UNSUPPORTED, "internal: " + why);
     }
+    // the one-launch kernel's phases run segments of several passes side by side
+    std::vector<Pass> phases;
+    fused_phases(passes, &phases);
+    for (const Pass& ps : phases)
+      if (find_hazard(ps, E, &why))
+        return fail(RELAY_ERR_UNSUPPORTED, "internal (one-launch phase): " + why);
+  }
   if (flags & RELAY_FLAG_DRY_RUN) return RELAY_OK;
 
   // small calls: the whole call in one cooperative launch (no pass events there)

@@ -899,7 +899,9 @@ cudaError_t launch_fused_typed(FusedArgs& a, int max_tiles, cudaStream_t stream)
 bool launch_fused(int dtype, const std::vector<Pass>& passes, float scale, cudaStream_t stream,
                   cudaError_t* err, bool forced) {
   *err = cudaSuccess;
-  if (passes.size() < 2 || passes.size() > (size_t)kMaxFusedPasses || !cooperative_supported())
+  static thread_local std::vector<Pass> phases;
+  fused_phases(passes, &phases);
+  if (passes.size() < 2 || phases.size() > (size_t)kMaxFusedPasses || !cooperative_supported())
     return false;
   static thread_local FusedArgs a;
   static thread_local std::vector<Seg> segs;
@@ -908,10 +910,10 @@ bool launch_fused(int dtype, const std::vector<Pass>& passes, float scale, cudaS
   int n = 0, max_tiles = 0;
   bool realign = false;
   int64_t traffic = 0;
-  a.npass = (int32_t)passes.size();
+  a.npass = (int32_t)phases.size();
   a.scale = scale;
-  for (size_t p = 0; p < passes.size(); ++p) {
-    split_for_alignment(passes[p].segs, E, &segs);
+  for (size_t p = 0; p < phases.size(); ++p) {
+    split_for_alignment(phases[p].segs, E, &segs);
     a.seg0[p] = n;
     int64_t tiles = 0;
     for (const Seg& sg : segs) {
@@ -928,7 +930,7 @@ bool launch_fused(int dtype, const std::vector<Pass>& passes, float scale, cudaS
     max_tiles = std::max<int>(max_tiles, (int)tiles);
   }
   if (!forced && n > kFusedPlainCap && (!realign || traffic > kFusedManyBytes)) return false;
-  a.seg0[passes.size()] = n;
+  a.seg0[phases.size()] = n;
   switch (dtype) {
     case RELAY_F32: *err = launch_fused_typed<TF32>(a, max_tiles, stream); break;
     case RELAY_BF16: *err = launch_fused_typed<TBF16>(a, max_tiles, stream); break;

@@ -32,7 +32,10 @@ class Builder {
   void begin(relay_pass_kind_t kind) {
     out_->push_back(Pass{kind, {}, {}});
     cur_ = &out_->back();
+    phase_ = -1;
   }
+  // earliest one-launch phase of the segments emitted from here on (-1: their own pass)
+  void phase(int ph) { phase_ = ph; }
 
   // group: schedule group of the transfer (0-based), or -1 for work local to `exec`
   void copy(int group, int exec, const void* src, std::initializer_list<Dst> dsts, int64_t n) {
@@ -68,6 +71,7 @@ class Builder {
     for (int i = 0; i < nsrc; ++i) s.src[i] = srcs[i];
     m.group = (int8_t)group;
     m.exec_rank = (int8_t)exec;
+    m.phase = (int8_t)phase_;
     for (int i = 0; i < kMaxDst; ++i) m.dst_rank[i] = -1;
     for (size_t i = 0; i < dsts.size(); ++i) {
       s.dst[i] = dsts[i].ptr;
@@ -82,6 +86,7 @@ class Builder {
   std::vector<Pass>* out_;
   Pass* cur_ = nullptr;
   int E_;
+  int phase_ = -1;
 };
 
 // index of `s` among the A-1 ranks other than `o`, ascending
@@ -154,8 +159,9 @@ void a2_exchange(Builder& B, const relay_plan_t& p, SrcF src, DstF dst,
 // The actives' closing reduction: out = Q(scale * (own + received)), sources ascending
 // by rank (D115998376 phases 3 and 5 fused into one pass).
 void a2_active_reduce(Builder& B, int64_t n, const void* own0, const void* recv0, void* out0,
-                      const void* own1, const void* recv1, void* out1) {
+                      const void* own1, const void* recv1, void* out1, int phase = -1) {
   B.begin(RELAY_PASS_ACTIVE_REDUCE);
+  B.phase(phase);
   B.reduce(-1, 0, {own0, recv0}, {Dst{0, out0}}, n, true);
   B.reduce(-1, 1, {recv1, own1}, {Dst{1, out1}}, n, true);
 }
@@ -180,11 +186,15 @@ void build_a2(Builder& B, const relay_plan_t& p) {
         for (int h = 0; h < H; ++h)
           B.reduce(1, 2 + h, {B.Hh(h, 0), B.Hh(h, c)},
                    {Dst{0, B.Y(0, h * c)}, Dst{1, B.Y(1, h * c)}}, c, true);
+        // In the one-launch kernel the dirB copies read only inputs, so they run with
+        // group 1, and the closing reduction needs only dirA and dirB, so it runs with the
+        // helper reductions: two phases and one grid barrier instead of three and two.
+        B.phase(0);
         for (int a = 0; a < 2; ++a)
           B.copy(1, a, B.X(a, d0 + p.dirA_size), {Dst{1 - a, B.W(1 - a, p.dirA_size)}},
                  p.dirB_size);
         a2_active_reduce(B, n - d0, B.X(0, d0), B.W(0, 0), B.Y(0, d0), B.X(1, d0), B.W(1, 0),
-                         B.Y(1, d0));
+                         B.Y(1, d0), 1);
       } else {
         // item 3 full exchange, D115998367 halves, or the legacy three groups: the
         // received region is staged position-aligned in the scratch
@@ -464,6 +474,21 @@ void build_multi_program(const std::vector<relay_plan_t>& plans, const std::vect
   }
   for (int ph = 0; ph < 4; ++ph)
     if (used[ph] && !merged[ph].segs.empty()) out->push_back(std::move(merged[ph]));
+}
+
+void fused_phases(const std::vector<Pass>& passes, std::vector<Pass>* out) {
+  out->clear();
+  std::vector<Pass> ph(passes.size());
+  for (size_t p = 0; p < passes.size(); ++p) ph[p].kind = passes[p].kind;
+  for (size_t p = 0; p < passes.size(); ++p)
+    for (size_t i = 0; i < passes[p].segs.size(); ++i) {
+      const SegMeta& m = passes[p].meta[i];
+      const size_t q = (m.phase >= 0 && (size_t)m.phase < p) ? (size_t)m.phase : p;
+      ph[q].segs.push_back(passes[p].segs[i]);
+      ph[q].meta.push_back(m);
+    }
+  for (Pass& q : ph)
+    if (!q.segs.empty()) out->push_back(std::move(q));
 }
 
 }  // namespace relay

@@ -51,6 +51,11 @@ struct SegMeta {
   int8_t group;           // schedule group whose transfer this is; -1: local work only
   int8_t exec_rank;       // rank whose kernel work this is (owner of the sources)
   int8_t dst_rank[kMaxDst];
+  // Earliest phase of the one-launch kernel this segment may run in, where its data
+  // dependencies allow running it before its own pass; -1: its own pass. Phases stand in
+  // for group boundaries only inside that kernel: the per-pass launches keep one launch
+  // per schedule group.
+  int8_t phase = -1;
 };
 
 // Bytes one source / one destination of a segment spans (mixed-width segments carry
@@ -88,6 +93,11 @@ struct Pass {
   std::vector<Seg> segs;
   std::vector<SegMeta> meta;
 };
+
+// The one-launch kernel's phases: segment i of pass p runs in phase meta.phase if that is
+// set, else in phase p; empty phases are dropped. Each phase keeps the kind of the
+// earliest pass that lands in it -- program.cpp.
+void fused_phases(const std::vector<Pass>& passes, std::vector<Pass>* out);
 
 // Plan (relay_plan_t is the public POD) -- plan.cpp.
 relay_status_t make_plan(relay_coll_t coll, int64_t count, relay_dtype_t dtype, int A, int R,
