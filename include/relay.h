@@ -44,7 +44,7 @@ extern "C" {
 typedef enum {
   RELAY_OK = 0,
   RELAY_ERR_INVALID_ARGUMENT = 1, /* bad A/R/dtype/scale/pointer/alias/size */
-  RELAY_ERR_UNSUPPORTED = 2,      /* valid request this build does not execute */
+  RELAY_ERR_UNSUPPORTED = 2,      /* valid request this library does not execute */
   RELAY_ERR_CUDA = 3              /* a CUDA launch or event call failed */
 } relay_status_t;
 
