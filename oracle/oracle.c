@@ -120,8 +120,8 @@ void orc_allreduce(int dtype, int A, const void* const* x, int64_t i0, int64_t i
  * helper_span > 0 restates the 4-active flat reduce-at-helper (S6): positions
  * [0, helper_span) of every block are summed at a helper over the A-1 non-owner
  * sources, and that partial travels back to the owner as ONE payload-typed chunk
- * ("A-1 chunks in, one out"), so it is rounded to the payload type before the owner
- * adds its own contribution and applies the scale.  Positions past helper_span are
+ * (A-1 chunks come in, one goes out), so it is rounded to the payload type before
+ * the owner adds its own contribution and applies the scale.  Positions past helper_span are
  * reduced at the owner from all A sources, ascending. */
 static void reduce_scatter_impl(int dtype, int A, const void* const* x, int64_t m, int owner,
                                 int64_t i0, int64_t i1, float scale, int64_t helper_span,
@@ -302,7 +302,8 @@ int orc_plan(int coll, int A, int R, int64_t count, int esize, int permille, int
   if (relay) {
     if (coll == ORC_A2A) {
       /* offload geometry that balances both groups' cross links ((A-1)*oc per group)
-       * against the intra links (d1, d2); reproduces S7's "link model promised 1.67x" */
+       * against the intra links (d1, d2); reproduces the 1.67x that item 7's link
+       * model predicted */
       oc = orc_align_down(n / (2 * (A - 1) + H));
     } else {
       /* S4: offload fraction in permille of the region, split evenly over helpers */
@@ -465,7 +466,7 @@ uint64_t orc_cost_elems(const int64_t* g) {
 /* The passthrough helper size (D115998394, D115998388, D115998370):
  * min(count_g, A * align_down(count_g / num_chunks, 128)) -- A slots, each a whole
  * number of 128-element chunks.  Below one chunk the page only says the fallback
- * "can only over-allocate"; this returns count_g there (a reading). */
+ * errs only towards allocating too much; this returns count_g there (a reading). */
 int64_t orc_passthrough_helper_size(int64_t count_g, int A, int num_chunks) {
   int64_t c = orc_align_down(count_g / num_chunks);
   if (c == 0) return count_g;
