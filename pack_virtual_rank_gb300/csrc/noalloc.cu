@@ -28,19 +28,20 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
 // is only a host-side stand-in, so the address is looked up with cudaGetSymbolAddress,
 // once per device, while that device is current (the caller's current device).
 void* noalloc_base(int dev, cudaError_t* err) {
-  static void* cached[RELAY_MAX_RANKS] = {nullptr};
-  if (dev < 0 || dev >= RELAY_MAX_RANKS) {
+  static void* cached[kMaxDevices] = {nullptr};
+  if (dev < 0) {
     *err = cudaErrorInvalidDevice;
     return nullptr;
   }
-  if (cached[dev] == nullptr) {
-    void* p = nullptr;
-    *err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (*err != cudaSuccess) return nullptr;
-    cached[dev] = p;
+  if (dev < kMaxDevices && cached[dev] != nullptr) {
+    *err = cudaSuccess;
+    return cached[dev];
   }
-  *err = cudaSuccess;
-  return cached[dev];
+  void* p = nullptr;
+  *err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  if (*err != cudaSuccess) return nullptr;
+  if (dev < kMaxDevices) cached[dev] = p;
+  return p;
 }
 
 size_t round_up_256(size_t bytes) { return (bytes + 255) / 256 * 256; }

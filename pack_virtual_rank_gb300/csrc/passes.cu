@@ -804,13 +804,13 @@ void split_for_alignment(const std::vector<Seg>& in, int E, std::vector<Seg>* ou
 }
 
 int sm_count() {
-  static int cached[RELAY_MAX_RANKS] = {0};
+  static int cached[kMaxDevices] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 1;
-  if (dev >= 0 && dev < RELAY_MAX_RANKS && cached[dev] > 0) return cached[dev];
+  if (dev >= 0 && dev < kMaxDevices && cached[dev] > 0) return cached[dev];
   int n = 1;
   cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-  if (dev >= 0 && dev < RELAY_MAX_RANKS) cached[dev] = n;
+  if (dev >= 0 && dev < kMaxDevices) cached[dev] = n;
   return n;
 }
 
@@ -873,15 +873,14 @@ int fused_blocks_per_sm() {
 }
 
 bool cooperative_supported() {
-  static int cached[RELAY_MAX_RANKS] = {0};  // 0 unknown, 1 yes, 2 no
+  static int cached[kMaxDevices] = {0};  // 0 unknown, 1 yes, 2 no
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= RELAY_MAX_RANKS) return false;
-  if (cached[dev] == 0) {
-    int v = 0;
-    cudaDeviceGetAttribute(&v, cudaDevAttrCooperativeLaunch, dev);
-    cached[dev] = v ? 1 : 2;
-  }
-  return cached[dev] == 1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return false;
+  if (dev < kMaxDevices && cached[dev] != 0) return cached[dev] == 1;
+  int v = 0;
+  cudaDeviceGetAttribute(&v, cudaDevAttrCooperativeLaunch, dev);
+  if (dev < kMaxDevices) cached[dev] = v ? 1 : 2;
+  return v != 0;
 }
 
 template <class P>

@@ -24,6 +24,10 @@
 
 namespace relay {
 
+// Per-process caches of device properties hold this many device ordinals; a device past
+// them is queried on every call instead.
+constexpr int kMaxDevices = 64;
+
 constexpr int kMaxSrc = 4;
 constexpr int kMaxDst = 4;
 
