@@ -232,6 +232,51 @@ def _cpu_oracle_all_cores(sample: int, seed_config: int = 2, inputs=None):
     return dt, nt
 
 
+def _bind_near_gpu(dev):
+    """Pin this process to the host cores the GPU's PCI function reports as local (sysfs
+    local_cpulist), so that pinned host buffers allocated afterwards sit in the memory next
+    to the GPU's host link. Returns what was done, for the JSON line."""
+    import torch
+    pr = torch.cuda.get_device_properties(dev)
+    dom, bus, slot = (getattr(pr, k, None) for k in ("pci_domain_id", "pci_bus_id", "pci_device_id"))
+    if bus is not None and slot is not None:
+        addr = f"{dom or 0:04x}:{bus:02x}:{slot:02x}.0"
+    else:
+        # older PyTorch: find the GPU by UUID in nvidia-smi's PCI listing
+        try:
+            out = subprocess.run(["nvidia-smi", "--query-gpu=uuid,pci.bus_id", "--format=csv,noheader"],
+                                 capture_output=True, text=True, timeout=30).stdout
+        except (OSError, subprocess.SubprocessError):
+            return {"bound": False, "why": "no PCI location (nvidia-smi unavailable)"}
+        want = str(getattr(pr, "uuid", "")).lower().replace("gpu-", "")
+        addr = None
+        for ln in out.splitlines():
+            u, _, b = (x.strip() for x in ln.partition(","))
+            if want and u.lower().replace("gpu-", "") == want:
+                d, rest = b.split(":", 1)
+                addr = f"{int(d, 16):04x}:{rest}".lower()
+        if addr is None:
+            return {"bound": False, "why": "GPU not found in nvidia-smi's PCI listing"}
+    path = f"/sys/bus/pci/devices/{addr}/local_cpulist"
+    try:
+        spec = open(path).read().strip()
+    except OSError:
+        return {"bound": False, "why": f"no {path}"}
+    cpus = set()
+    for part in spec.split(","):
+        if "-" in part:
+            lo, hi = part.split("-")
+            cpus.update(range(int(lo), int(hi) + 1))
+        elif part:
+            cpus.add(int(part))
+    allowed = cpus & set(os.sched_getaffinity(0))
+    if not allowed:
+        return {"bound": False, "why": f"local cpus {spec} not in this process's set"}
+    if allowed != set(os.sched_getaffinity(0)):
+        os.sched_setaffinity(0, allowed)
+    return {"bound": True, "local_cpulist": spec, "cpus": len(allowed)}
+
+
 def _calibrate_link(rv, host_in, dev_in, dev_out, host_out, ctas, nbytes=256 << 20):
     """Host-link rates on this GPU for the copy engines (torch copies) and for relay_copy
     with `ctas` CTAs: each direction alone, then every pairing of the two directions
@@ -398,7 +443,9 @@ def run_ours(args):
     # sets let step k+1's input copy and step k-1's result copy overlap step k's passes
     # (copy-in, compute and copy-out each on their own stream, ordered by events).
     e2e_ms, e2e_steps, calib = None, max(2, min(args.steps, 8)), None
+    host_numa = None
     if not args.kernel_only:
+        host_numa = _bind_near_gpu(dev)
         hx = [x.cpu().pin_memory() for x in xs]
         hy = [torch.empty(count, dtype=torch.bfloat16).pin_memory() for _ in range(A)]
         sets = [(xs, ys), ([torch.empty_like(x) for x in xs], [torch.empty_like(y) for y in ys])]
@@ -519,6 +566,7 @@ def run_ours(args):
                 "link_ceiling_gbs": link_ceiling,
                 "frac_of_link_ceiling": None if not link_ceiling else round(e2e / link_ceiling, 3),
                 "link_pair_bound_gbs": link_pair,
+                "host_placement": host_numa,
                 "frac_of_link_pair_bound": None if not link_pair else round(e2e / link_pair, 3),
                 "copies": {"library": "relay_copy both ways",
                            "library-in": "relay_copy in, copy engine out",
