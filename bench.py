@@ -277,18 +277,32 @@ def _bind_near_gpu(dev):
     return {"bound": True, "local_cpulist": spec, "cpus": len(allowed)}
 
 
-def _calibrate_link(rv, host_in, dev_in, dev_out, host_out, ctas, nbytes=256 << 20):
+def _calibrate_link(rv, host_in, dev_in, dev_out, host_out, ctas):
     """Host-link rates on this GPU for the copy engines (torch copies) and for relay_copy
-    with `ctas` CTAs: each direction alone, then every pairing of the two directions
-    running at once on two streams, as the end-to-end leg runs them (median of 3, `nbytes`
-    each way). Returns (rates in GB/s, the fastest pairing)."""
+    with `ctas` CTAs, on the end-to-end leg's own transfers (every active's whole input in,
+    every active's whole output out): each direction alone, then every pairing of the two
+    directions running at once on two streams, as the leg runs them (median of 3). Returns
+    (rates in GB/s, the fastest pairing)."""
     import torch
-    n = min(nbytes // host_in.element_size(), host_in.numel())
-    hi, di, do, ho = host_in[:n], dev_in[:n], dev_out[:n], host_out[:n]
-    eng_in = lambda: di.copy_(hi, non_blocking=True)
-    ker_in = lambda: rv.relay_copy(di, hi, max_ctas=ctas)
-    eng_out = lambda: ho.copy_(do, non_blocking=True)
-    ker_out = lambda: rv.relay_copy(ho, do, max_ctas=ctas)
+    pairs_in = list(zip(host_in, dev_in))
+    pairs_out = list(zip(dev_out, host_out))
+
+    def eng_in():
+        for h, d in pairs_in:
+            d.copy_(h, non_blocking=True)
+
+    def ker_in():
+        for h, d in pairs_in:
+            rv.relay_copy(d, h, max_ctas=ctas)
+
+    def eng_out():
+        for d, h in pairs_out:
+            h.copy_(d, non_blocking=True)
+
+    def ker_out():
+        for d, h in pairs_out:
+            rv.relay_copy(h, d, max_ctas=ctas)
+
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
 
     def timed(fin, fout):
@@ -310,16 +324,17 @@ def _calibrate_link(rv, host_in, dev_in, dev_out, host_out, ctas, nbytes=256 << 
                 ts.append(e0.elapsed_time(e1))
         return statistics.median(ts)
 
-    gb = n * host_in.element_size() / 1e6
-    out = {"h2d_engine_gbs": round(gb / timed(eng_in, None), 1),
-           "h2d_kernel_gbs": round(gb / timed(ker_in, None), 1),
-           "d2h_engine_gbs": round(gb / timed(None, eng_out), 1),
-           "d2h_kernel_gbs": round(gb / timed(None, ker_out), 1)}
+    gb_in = sum(h.numel() * h.element_size() for h in host_in) / 1e6
+    gb_out = sum(h.numel() * h.element_size() for h in host_out) / 1e6
+    out = {"h2d_engine_gbs": round(gb_in / timed(eng_in, None), 1),
+           "h2d_kernel_gbs": round(gb_in / timed(ker_in, None), 1),
+           "d2h_engine_gbs": round(gb_out / timed(None, eng_out), 1),
+           "d2h_kernel_gbs": round(gb_out / timed(None, ker_out), 1)}
     pairs = {"torch": (eng_in, eng_out), "library-in": (ker_in, eng_out),
              "library-out": (eng_in, ker_out), "library": (ker_in, ker_out)}
     both = {m: timed(*fns) for m, fns in pairs.items()}
     for m, t in both.items():
-        out[f"both_{m}_gbs_each"] = round(gb / t, 1)
+        out[f"both_{m}_gbs_each"] = round(max(gb_in, gb_out) / t, 1)
     return out, min(both, key=both.get)
 
 
@@ -455,7 +470,7 @@ def run_ours(args):
         link_ctas = args.e2e_ctas or max(1, torch.cuda.get_device_properties(dev).multi_processor_count // 2)
         e2e_mode, calib = args.e2e_copy, None
         if e2e_mode == "auto":
-            calib, e2e_mode = _calibrate_link(rv, hx[0], xs[0], ys[0], hy[0], link_ctas)
+            calib, e2e_mode = _calibrate_link(rv, hx, xs, ys, hy, link_ctas)
         ev = lambda: torch.cuda.Event()
         done_in = [ev() for _ in range(e2e_steps)]
         done_comp = [ev() for _ in range(e2e_steps)]
