@@ -234,8 +234,9 @@ def _cpu_oracle_all_cores(sample: int, seed_config: int = 2, inputs=None):
 
 def _bind_near_gpu(dev):
     """Pin this process to the host cores the GPU's PCI function reports as local (sysfs
-    local_cpulist), so that pinned host buffers allocated afterwards sit in the memory next
-    to the GPU's host link. Returns what was done, for the JSON line."""
+    local_cpulist), so that pinned host buffers allocated next sit in the memory next to
+    the GPU's host link (the caller restores the affinity afterwards). Returns what was
+    done, for the JSON line."""
     import torch
     pr = torch.cuda.get_device_properties(dev)
     dom, bus, slot = (getattr(pr, k, None) for k in ("pci_domain_id", "pci_bus_id", "pci_device_id"))
@@ -460,9 +461,11 @@ def run_ours(args):
     e2e_ms, e2e_steps, calib = None, max(2, min(args.steps, 8)), None
     host_numa = None
     if not args.kernel_only:
+        cpus_before = os.sched_getaffinity(0)
         host_numa = _bind_near_gpu(dev)
         hx = [x.cpu().pin_memory() for x in xs]
         hy = [torch.empty(count, dtype=torch.bfloat16).pin_memory() for _ in range(A)]
+        os.sched_setaffinity(0, cpus_before)   # the buffers stay where they were placed
         sets = [(xs, ys), ([torch.empty_like(x) for x in xs], [torch.empty_like(y) for y in ys])]
         s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
         # host-link copies: the library's kernel with half a CTA per SM (it reaches the
