@@ -172,15 +172,15 @@ struct TI32 {
 // Whole tile on the 16-byte vector path: every thread loads kUnroll vectors per
 // source (in batches that keep at most 8 loads in flight per thread), reduces and
 // stores them. base is the tile's first element.
-template <class P, int NSRC, bool COH>
+template <class P, int NSRC, bool COH, int U = kUnroll>
 __device__ __forceinline__ void reduce_full_tile(const Seg& s, int64_t base, float scale) {
   constexpr int L = P::kLanes;
-  constexpr int UB = NSRC <= 2 ? kUnroll : kUnroll / 2;
+  constexpr int UB = (NSRC <= 2 || U < 2) ? U : U / 2;
   using Acc = typename P::Acc;
   const int64_t v0 = base / L + threadIdx.x;
   const bool do_scale = (s.flags & kFlagScale) != 0;
 #pragma unroll
-  for (int u0 = 0; u0 < kUnroll; u0 += UB) {
+  for (int u0 = 0; u0 < U; u0 += UB) {
     uint4 v[NSRC][UB];
 #pragma unroll
     for (int u = 0; u < UB; ++u)
@@ -209,31 +209,31 @@ __device__ __forceinline__ void reduce_full_tile(const Seg& s, int64_t base, flo
   }
 }
 
-template <bool COH>
+template <bool COH, int U = kUnroll>
 __device__ __forceinline__ void copy_full_tile(const Seg& s, int64_t vbase) {
   const int64_t v0 = vbase + threadIdx.x;
-  uint4 v[kUnroll];
+  uint4 v[U];
 #pragma unroll
-  for (int u = 0; u < kUnroll; ++u)
+  for (int u = 0; u < U; ++u)
     v[u] = Mem<COH>::v4(static_cast<const uint4*>(s.src[0]) + v0 + u * kThreads);
 #pragma unroll
-  for (int u = 0; u < kUnroll; ++u)
+  for (int u = 0; u < U; ++u)
 #pragma unroll
     for (int d = 0; d < kMaxDst; ++d)
       if (d < s.ndst) st_v4(static_cast<uint4*>(s.dst[d]) + v0 + u * kThreads, v[u]);
 }
 
-template <class P, bool COH>
+template <class P, bool COH, int U = kUnroll>
 __device__ __forceinline__ void run_full_tile(const Seg& s, int64_t base, float scale) {
   if (s.op == kOpCopy) {
-    copy_full_tile<COH>(s, base / P::kLanes);
+    copy_full_tile<COH, U>(s, base / P::kLanes);
     return;
   }
   switch (s.nsrc) {
-    case 1: reduce_full_tile<P, 1, COH>(s, base, scale); break;
-    case 2: reduce_full_tile<P, 2, COH>(s, base, scale); break;
-    case 3: reduce_full_tile<P, 3, COH>(s, base, scale); break;
-    default: reduce_full_tile<P, 4, COH>(s, base, scale); break;
+    case 1: reduce_full_tile<P, 1, COH, U>(s, base, scale); break;
+    case 2: reduce_full_tile<P, 2, COH, U>(s, base, scale); break;
+    case 3: reduce_full_tile<P, 3, COH, U>(s, base, scale); break;
+    default: reduce_full_tile<P, 4, COH, U>(s, base, scale); break;
   }
 }
 
@@ -721,6 +721,11 @@ __global__ void __launch_bounds__(kThreads, MODE == kModeRealign ? 4 : 5)
 // uniform). For calls small enough that the fixed cost of a launch per pass dominates.
 
 constexpr int kMaxFusedPasses = 4;
+// The one-launch kernel's tiles hold U vectors per thread: 4 (16 KiB), or 2 (8 KiB) for a
+// call whose 16 KiB tiles number at most twice its grid, so that CTAs have a tile each.
+// On GB300 8 KiB tiles took 4 MiB-per-rank 4-active calls 13-16% faster (allreduce 14.5 ->
+// 12.6 us, reduce-scatter 12.4 -> 10.4 us) and made larger ones up to 14% slower.
+constexpr int kFusedUnrollSmall = 2;
 constexpr int kFusedCap = 384;  // 48 + 384 * 80 bytes of parameters, under the 32 KiB limit
 // Calls with more segments than this fuse only when some of them need realigning (whose
 // per-pass form costs a second launch per pass) and their traffic is at most
@@ -741,10 +746,10 @@ struct FusedArgs {
 // 4 CTAs per SM (64 registers): with its realigning path the kernel spills at 48, and on
 // GB300 the 4-CTA build was as fast or faster on every small call measured (a 16 MiB
 // 2-active allreduce 22.7 -> 20.6 us).
-template <class P>
+template <class P, int U>
 __global__ void __launch_bounds__(kThreads, 4) relay_fused_kernel(const __grid_constant__ FusedArgs args) {
   namespace cg = cooperative_groups;
-  constexpr int64_t kTile = kTileBytes / P::kE;
+  constexpr int64_t kTile = (int64_t)kThreads * U * kVecBytes / P::kE;
   for (int p = 0; p < args.npass; ++p) {
     for (int t = blockIdx.x; t < args.ntiles[p]; t += gridDim.x) {
       int lo = args.seg0[p], hi = args.seg0[p + 1] - 1;
@@ -755,7 +760,7 @@ __global__ void __launch_bounds__(kThreads, 4) relay_fused_kernel(const __grid_c
       const Seg& s = args.seg[lo];
       const int64_t base = (int64_t)(t - s.tile0) * kTile;
       const int64_t len = min(kTile, s.n - base);
-      if ((s.flags & kFlagVector) && len == kTile) run_full_tile<P, true>(s, base, args.scale);
+      if ((s.flags & kFlagVector) && len == kTile) run_full_tile<P, true, U>(s, base, args.scale);
       else if (s.flags & kFlagRealign) run_partial_realign_tile<P, true>(s, base, len, args.scale);
       else run_partial_tile<P, true>(s, base, len, args.scale);
     }
@@ -858,12 +863,12 @@ cudaError_t launch_typed(const std::vector<Seg>& segs, float scale, cudaStream_t
   return cudaSuccess;
 }
 
-template <class P>
+template <class P, int U>
 int fused_blocks_per_sm() {
   static int cached = 0;
   if (cached == 0) {
     int nb = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, relay_fused_kernel<P>, kThreads, 0) !=
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, relay_fused_kernel<P, U>, kThreads, 0) !=
             cudaSuccess ||
         nb <= 0)
       nb = 1;
@@ -883,13 +888,42 @@ bool cooperative_supported() {
   return v != 0;
 }
 
+// Fill the tile counts of `a` for tiles of U vectors per thread; returns the largest
+// phase's tile count, or -1 if a count would overflow.
+int fused_tiles(FusedArgs& a, int E, int U) {
+  const int64_t tile = (int64_t)kThreads * U * kVecBytes / E;
+  int max_tiles = 0;
+  for (int p = 0; p < a.npass; ++p) {
+    int64_t tiles = 0;
+    for (int i = a.seg0[p]; i < a.seg0[p + 1]; ++i) {
+      a.seg[i].tile0 = (int32_t)tiles;
+      tiles += (a.seg[i].n + tile - 1) / tile;
+    }
+    if (tiles > INT32_MAX) return -1;
+    a.ntiles[p] = (int32_t)tiles;
+    max_tiles = std::max<int>(max_tiles, (int)tiles);
+  }
+  return max_tiles;
+}
+
 template <class P>
-cudaError_t launch_fused_typed(FusedArgs& a, int max_tiles, cudaStream_t stream) {
-  const int64_t cap = (int64_t)sm_count() * fused_blocks_per_sm<P>();
+cudaError_t launch_fused_typed(FusedArgs& a, cudaStream_t stream, bool* ok) {
+  *ok = true;
+  const int64_t cap = (int64_t)sm_count() * fused_blocks_per_sm<P, kUnroll>();
+  int max_tiles = fused_tiles(a, P::kE, kUnroll);
+  int64_t total = 0;
+  for (int p = 0; p < a.npass; ++p) total += a.ntiles[p];
+  const bool small = total <= 2 * cap;
+  if (small) max_tiles = fused_tiles(a, P::kE, kFusedUnrollSmall);
+  if (max_tiles < 0) {
+    *ok = false;
+    return cudaSuccess;
+  }
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(max_tiles, cap));
   void* params[] = {&a};
-  cudaError_t e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(relay_fused_kernel<P>),
-                                              dim3(grid), dim3(kThreads), params, 0, stream);
+  const void* fn = small ? reinterpret_cast<const void*>(relay_fused_kernel<P, kFusedUnrollSmall>)
+                         : reinterpret_cast<const void*>(relay_fused_kernel<P, kUnroll>);
+  cudaError_t e = cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(kThreads), params, 0, stream);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -905,8 +939,7 @@ bool launch_fused(int dtype, const std::vector<Pass>& passes, float scale, cudaS
   static thread_local FusedArgs a;
   static thread_local std::vector<Seg> segs;
   const int E = esize_of(dtype);
-  const int64_t tile = kTileBytes / E;
-  int n = 0, max_tiles = 0;
+  int n = 0;
   bool realign = false;
   int64_t traffic = 0;
   a.npass = (int32_t)phases.size();
@@ -914,28 +947,22 @@ bool launch_fused(int dtype, const std::vector<Pass>& passes, float scale, cudaS
   for (size_t p = 0; p < phases.size(); ++p) {
     split_for_alignment(phases[p].segs, E, &segs);
     a.seg0[p] = n;
-    int64_t tiles = 0;
     for (const Seg& sg : segs) {
       if (seg_mixed(sg) || n >= kFusedCap) return false;
       realign |= (sg.flags & kFlagRealign) != 0;
       traffic += sg.n * E * (sg.nsrc + sg.ndst);
-      a.seg[n] = sg;
-      a.seg[n].tile0 = (int32_t)tiles;
-      tiles += (sg.n + tile - 1) / tile;
-      ++n;
+      a.seg[n++] = sg;
     }
-    if (tiles > INT32_MAX) return false;
-    a.ntiles[p] = (int32_t)tiles;
-    max_tiles = std::max<int>(max_tiles, (int)tiles);
   }
   if (!forced && n > kFusedPlainCap && (!realign || traffic > kFusedManyBytes)) return false;
   a.seg0[phases.size()] = n;
+  bool ok = true;
   switch (dtype) {
-    case RELAY_F32: *err = launch_fused_typed<TF32>(a, max_tiles, stream); break;
-    case RELAY_BF16: *err = launch_fused_typed<TBF16>(a, max_tiles, stream); break;
-    default: *err = launch_fused_typed<TI32>(a, max_tiles, stream); break;
+    case RELAY_F32: *err = launch_fused_typed<TF32>(a, stream, &ok); break;
+    case RELAY_BF16: *err = launch_fused_typed<TBF16>(a, stream, &ok); break;
+    default: *err = launch_fused_typed<TI32>(a, stream, &ok); break;
   }
-  return true;
+  return ok;
 }
 
 namespace {
