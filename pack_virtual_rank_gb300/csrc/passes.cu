@@ -729,11 +729,12 @@ constexpr int kFusedUnrollSmall = 2;
 constexpr int kFusedCap = 384;  // 48 + 384 * 80 bytes of parameters, under the 32 KiB limit
 // Calls with more segments than this fuse only when some of them need realigning (whose
 // per-pass form costs a second launch per pass) and their traffic is at most
-// kFusedManyBytes: on GB300 a 54 MiB-per-rank aligned all-to-all (172 segments, 241 MB of
-// traffic) ran 42 us pass by pass and 49 us fused, a misaligned one 67 us and 70 us, while
-// a misaligned 13 MiB one ran 45 us pass by pass and 23 us fused.
+// kFusedManyBytes. On GB300 (CUDA-graph replays, warm L2) 4-active all-to-alls of 172
+// segments ran: aligned, 4.5 MiB per rank, 14.5 us pass by pass and 16.5 us fused;
+// misaligned, 4.3 MiB (55 MiB of traffic), 22.7 us either way in bf16 and 24.7 vs 22.7 us
+// in int32; misaligned, 8.7 MiB (110 MiB), 30.8 vs 35.9 us; 17.4 MiB, 51.5 vs 70 us.
 constexpr int kFusedPlainCap = 128;
-constexpr int64_t kFusedManyBytes = 128ll << 20;
+constexpr int64_t kFusedManyBytes = 64ll << 20;
 
 struct FusedArgs {
   int32_t npass;
