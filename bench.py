@@ -764,6 +764,27 @@ def run_sweep(args):
                 e1.record()
                 torch.cuda.synchronize()
                 whole.append(e0.elapsed_time(e1))
+        # the same call replayed from a CUDA graph: device time only, without the host's
+        # planning and launch work that the timing around a direct call includes
+        whole_graph = []
+        if not args.graph:
+            s_g = torch.cuda.Stream()
+            torch.cuda.synchronize()
+            g_call = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_call, stream=s_g):
+                call(opts0)
+            g_call.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            for _ in range(reps):
+                flush.fill_(1.0)
+                flush_read.sum()
+                e0.record()
+                g_call.replay()
+                e1.record()
+                torch.cuda.synchronize()
+                whole_graph.append(e0.elapsed_time(e1))
+            del g_call
         # the same with the one-launch path forced at every size
         fused = []
         if not args.graph:
@@ -798,6 +819,10 @@ def run_sweep(args):
             fm = statistics.median(fused)
             row.update({"ms_call_fused_forced": round(fm, 4),
                         "frac_call_fused_forced": round(tot_b / fm / 1e6 / peak, 3)})
+        if whole_graph:
+            gm = statistics.median(whole_graph)
+            row.update({"ms_call_default_policy_graph": round(gm, 4),
+                        "frac_call_default_policy_graph": round(tot_b / gm / 1e6 / peak, 3)})
         if whole:
             wm = statistics.median(whole)
             row.update({"ms_call_default_policy": round(wm, 4),
