@@ -684,10 +684,15 @@ __device__ __noinline__ void run_mixed_tile(const Seg& s, int64_t base, int64_t 
 // its vectorized partial tiles it spilled at 48, and on GB300 the 4-CTA build ran 1 GiB
 // all-to-alls as fast as the spill-free 5-CTA one without them, and misaligned 54-135 MiB
 // all-to-alls 10-22% faster.
-constexpr int kModeMain = 0, kModeRealign = 1, kModeMixed = 2;
+// kModeRealignAll runs a whole misaligned copy pass in one launch: its aligned copies take
+// the realigning path with a zero shift. It runs 3 CTAs per SM (4 spilled) and is used only
+// for passes of at most kRealignAllBytes: on GB300 the one launch ran a 54 MiB-per-rank
+// misaligned all-to-all 14% faster than two, but 1 GiB ones 7% slower.
+constexpr int kModeMain = 0, kModeRealign = 1, kModeMixed = 2, kModeRealignAll = 3;
+constexpr int64_t kRealignAllBytes = 256ll << 20;
 
 template <class P, int CAP, int MODE>
-__global__ void __launch_bounds__(kThreads, MODE == kModeRealign ? 4 : 5)
+__global__ void __launch_bounds__(kThreads, MODE == kModeRealignAll ? 3 : MODE == kModeRealign ? 4 : 5)
     relay_pass_kernel(const __grid_constant__ PassArgs<CAP> args) {
   constexpr int64_t kTile = kTileBytes / P::kE;
   for (int t = blockIdx.x; t < args.ntiles; t += gridDim.x) {
@@ -707,10 +712,14 @@ __global__ void __launch_bounds__(kThreads, MODE == kModeRealign ? 4 : 5)
       else if (full && (s.flags & kFlagSrc1F32) && s.nsrc == 2) mixed_final_full(s, base, args.scale);
       else run_mixed_tile<P>(s, base, len, args.scale);
     }
-    else if (MODE != kModeRealign && (s.flags & kFlagVector) && len == kTile)
+    else if ((MODE == kModeMain || MODE == kModeMixed) && (s.flags & kFlagVector) && len == kTile)
       run_full_tile<P, false>(s, base, args.scale);
     else if (MODE == kModeRealign && len == kTile) run_realign_tile<P>(s, base, args.scale);
     else if (MODE == kModeRealign) run_realign_tail<P>(s, base, len, args.scale);
+    else if (MODE == kModeRealignAll && (s.flags & kFlagRealign) && len == kTile)
+      run_realign_tile<P>(s, base, args.scale);
+    else if (MODE == kModeRealignAll && (s.flags & kFlagRealign))
+      run_realign_tail<P>(s, base, len, args.scale);
     else run_partial_tile<P, false>(s, base, len, args.scale);
   }
 }
@@ -973,6 +982,25 @@ cudaError_t launch_split(const std::vector<Seg>& direct, const std::vector<Seg>&
                          const std::vector<Seg>& mixed, float scale, cudaStream_t stream,
                          int max_ctas) {
   cudaError_t e = cudaSuccess;
+  if (!realigned.empty() && !direct.empty()) {
+    bool copies_only = true;
+    int64_t bytes = 0;
+    for (const Seg& sg : direct) {
+      copies_only &= sg.op == kOpCopy;
+      bytes += sg.n * P::kE * (sg.nsrc + sg.ndst);
+    }
+    for (const Seg& sg : realigned) bytes += sg.n * P::kE * (sg.nsrc + sg.ndst);
+    if (copies_only && bytes <= kRealignAllBytes) {
+      // one launch: an aligned copy is a realigned one with a zero shift
+      static thread_local std::vector<Seg> all;
+      all.assign(realigned.begin(), realigned.end());
+      for (Seg sg : direct) {
+        if (sg.flags & kFlagVector) sg.flags = (uint8_t)((sg.flags & ~kFlagVector) | kFlagRealign);
+        all.push_back(sg);
+      }
+      return launch_typed<P, kModeRealignAll>(all, scale, stream, max_ctas);
+    }
+  }
   if (!direct.empty()) e = launch_typed<P, kModeMain>(direct, scale, stream, max_ctas);
   if (e == cudaSuccess && !realigned.empty())
     e = launch_typed<P, kModeRealign>(realigned, scale, stream, max_ctas);
