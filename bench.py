@@ -474,44 +474,55 @@ def run_ours(args):
         e2e_mode, calib = args.e2e_copy, None
         if e2e_mode == "auto":
             calib, e2e_mode = _calibrate_link(rv, hx, xs, ys, hy, link_ctas)
-        ev = lambda: torch.cuda.Event()
-        done_in = [ev() for _ in range(e2e_steps)]
-        done_comp = [ev() for _ in range(e2e_steps)]
-        done_out = [ev() for _ in range(e2e_steps)]
-        barrier()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        s_in.wait_stream(stream)
-        s_out.wait_stream(stream)
-        for k in range(e2e_steps):
-            bx, by = sets[k % 2]
-            with torch.cuda.stream(s_in):
+        def pipeline(mode, steps):
+            """`steps` end-to-end steps, copies done the `mode` way; returns ms."""
+            ev = lambda: torch.cuda.Event()
+            done_in = [ev() for _ in range(steps)]
+            done_comp = [ev() for _ in range(steps)]
+            done_out = [ev() for _ in range(steps)]
+            barrier()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            s_in.wait_stream(stream)
+            s_out.wait_stream(stream)
+            for k in range(steps):
+                bx, by = sets[k % 2]
+                with torch.cuda.stream(s_in):
+                    if k >= 2:
+                        s_in.wait_event(done_comp[k - 2])   # set k%2's inputs are free again
+                    for a in range(A):
+                        if mode in ("torch", "library-out"):
+                            bx[a].copy_(hx[a], non_blocking=True)
+                        else:
+                            rv.relay_copy(bx[a], hx[a], max_ctas=link_ctas, stream=s_in)
+                    done_in[k].record(s_in)
+                stream.wait_event(done_in[k])
                 if k >= 2:
-                    s_in.wait_event(done_comp[k - 2])   # set k%2's inputs are free again
-                for a in range(A):
-                    if e2e_mode in ("torch", "library-out"):
-                        bx[a].copy_(hx[a], non_blocking=True)
-                    else:
-                        rv.relay_copy(bx[a], hx[a], max_ctas=link_ctas, stream=s_in)
-                done_in[k].record(s_in)
-            stream.wait_event(done_in[k])
-            if k >= 2:
-                stream.wait_event(done_out[k - 2])      # set k%2's outputs were copied out
-            rv.relay_allreduce(bx + [None] * (R - A), by + [None] * (R - A), scratch, count,
-                               rv.BF16, A, R, SCALE, stream=stream)
-            done_comp[k].record(stream)
-            with torch.cuda.stream(s_out):
-                s_out.wait_event(done_comp[k])
-                for a in range(A):
-                    if e2e_mode in ("library", "library-out"):
-                        rv.relay_copy(hy[a], by[a], max_ctas=link_ctas, stream=s_out)
-                    else:
-                        hy[a].copy_(by[a], non_blocking=True)
-                done_out[k].record(s_out)
-        stream.wait_event(done_out[e2e_steps - 1])
-        e1.record(stream)
-        barrier()
-        e2e_ms = e0.elapsed_time(e1)
+                    stream.wait_event(done_out[k - 2])      # set k%2's outputs were copied out
+                rv.relay_allreduce(bx + [None] * (R - A), by + [None] * (R - A), scratch, count,
+                                   rv.BF16, A, R, SCALE, stream=stream)
+                done_comp[k].record(stream)
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(done_comp[k])
+                    for a in range(A):
+                        if mode in ("library", "library-out"):
+                            rv.relay_copy(hy[a], by[a], max_ctas=link_ctas, stream=s_out)
+                        else:
+                            hy[a].copy_(by[a], non_blocking=True)
+                    done_out[k].record(s_out)
+            stream.wait_event(done_out[steps - 1])
+            e1.record(stream)
+            barrier()
+            return e0.elapsed_time(e1)
+
+        if args.e2e_copy == "auto":
+            # the pipeline itself, 3 steps per way of copying, outside the timed region: on
+            # some boxes a copy engine runs at a third of its rate when the other direction
+            # is idle, which the single- and paired-copy rates alone do not predict
+            trial = {m: pipeline(m, 3) for m in ("torch", "library-in", "library-out", "library")}
+            calib["pipeline_3_steps_ms"] = {m: round(t, 2) for m, t in trial.items()}
+            e2e_mode = min(trial, key=trial.get)
+        e2e_ms = pipeline(e2e_mode, e2e_steps)
         del sets
 
     ms, e2e_ms = slowest_rank([ms, e2e_ms if e2e_ms is not None else 0.0], world)
@@ -592,9 +603,8 @@ def run_ours(args):
                            "torch": "copy engines both ways"}[e2e_mode]
                           + ("" if e2e_mode == "torch" else f" ({link_ctas} CTAs)")
                           + ("" if calib is None else
-                             ", the fastest pairing of the two directions running at once on "
-                             "this GPU (calibration outside the timed region, GB/s: "
-                             + ", ".join(f"{k} {v}" for k, v in calib.items()) + ")")},
+                             ", the fastest way in a 3-step trial of the pipeline on this GPU "
+                             "(calibration outside the timed region: " + json.dumps(calib) + ")")},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks,
         }
