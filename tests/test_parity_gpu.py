@@ -62,13 +62,16 @@ def test_small_sizes_every_schedule(coll, A, dtype, launch):
 @pytest.mark.parametrize("coll", [rv.ALLREDUCE, rv.REDUCE_SCATTER, rv.ALL_GATHER, rv.ALL_TO_ALL])
 @pytest.mark.parametrize("dtype", [rv.F32, rv.BF16])
 @pytest.mark.parametrize("shift", [1, 3])
-def test_unaligned_buffers(coll, dtype, shift):
+@pytest.mark.parametrize("launch", [0, rv.FLAG_SEPARATE_PASSES])
+def test_unaligned_buffers(coll, dtype, shift, launch):
     """Buffers that are element- but not 16-byte-aligned: all sharing one offset
-    (vector path after a peeled prologue) and with mixed offsets (per-element path)."""
+    (vector path after a peeled prologue) and with mixed offsets (per-element path), in the
+    one-launch kernel and pass by pass (where misaligned copy passes run in one launch of
+    the realign-all mode)."""
     for A in (2, 4):
         count = 5000 + 3
         sched = rv.SCHEDULE_RELAY
-        opts = rv.make_opts(schedule=sched, flags=rv.FLAG_CHECK_HAZARDS)
+        opts = rv.make_opts(schedule=sched, flags=rv.FLAG_CHECK_HAZARDS | launch)
         plan = rv.relay_plan(coll, count, dtype, A, 8, opts)
         xs = hz.make_inputs(11, A, plan.input_elems, dtype, "cuda")
         td = hz.TORCH[dtype]
