@@ -739,9 +739,10 @@ constexpr int kFusedCap = 384;  // 48 + 384 * 80 bytes of parameters, under the 
 // Calls with more segments than this fuse only when some of them need realigning (whose
 // per-pass form costs a second launch per pass) and their traffic is at most
 // kFusedManyBytes. On GB300 (CUDA-graph replays, warm L2) 4-active all-to-alls of 172
-// segments ran: aligned, 4.5 MiB per rank, 14.5 us pass by pass and 16.5 us fused;
-// misaligned, 4.3 MiB (55 MiB of traffic), 22.7 us either way in bf16 and 24.7 vs 22.7 us
-// in int32; misaligned, 8.7 MiB (110 MiB), 30.8 vs 35.9 us; 17.4 MiB, 51.5 vs 70 us.
+// segments (sizes are the workload count per rank; the input is a third of it) ran: aligned,
+// 13.5 MiB, 14.5 us pass by pass and 16.5 us fused; misaligned, 13 MiB (55 MiB of
+// traffic), 22.7 us either way in bf16 and 24.7 vs 22.7 us in int32; misaligned, 27 MiB
+// (110 MiB of traffic), 30.8 vs 35.9 us; 54 MiB, 51.5 vs 70 us.
 constexpr int kFusedPlainCap = 128;
 constexpr int64_t kFusedManyBytes = 64ll << 20;
 
