@@ -616,7 +616,7 @@ def run_ours(args):
 
 
 def _sweep_points():
-    """The five reference workloads at a spread of their sizes (bytes per rank)."""
+    """The five workloads of the metric at a spread of their sizes (bytes per rank)."""
     MB = 1 << 20
     pts = [("allreduce", 2, "f32", 65536 * 4, "relay")]
     pts += [("allreduce", 2, "bf16", b, "auto") for b in
@@ -997,7 +997,7 @@ def main():
                     help="COLLECTIVE:A:DTYPE:COUNT[:relay] run under the default launch policy "
                          "for profiler captures (not a bench line)")
     ap.add_argument("--sweep", action="store_true",
-                    help="per-collective, per-count pass table of the five reference workloads "
+                    help="per-collective, per-count pass table of the five workloads "
                          "(not a bench line)")
     ap.add_argument("--sweep-out", default=None, help="write the sweep table as JSON here")
     ap.add_argument("--graph", action="store_true",

@@ -1,4 +1,4 @@
-"""GPU parity at the full sizes of the five reference workloads.
+"""GPU parity at the full sizes of the five workloads the throughput metric is quoted on.
 
 Outputs up to 16 MiB per rank are compared element by element with the oracle; larger
 ones are compared on windows around every chunk, slice and direct-region boundary
