@@ -40,6 +40,8 @@ CPU_SAMPLE = 1 << 24         # elements per rank in one step of the reference ar
 CPU_BASELINE_SAMPLE = 1 << 27  # elements per rank of the bench's own CPU-baseline leg
 PROFILE = os.path.join(ROOT, "profiles", "relay_pass_kernel_allreduce_a2_bf16_1g.md")
 KERNEL_SRC = os.path.join(ROOT, "pack_virtual_rank_gb300", "csrc", "passes.cu")
+KERNEL_HDR = os.path.join(ROOT, "pack_virtual_rank_gb300", "csrc", "program.h")
+HOST_SIDE_MARK = "// ------------------------------------------------------------------- host side --"
 
 
 def _dist():
@@ -85,10 +87,16 @@ def _theoretical_hbm_gbs(dev):
 
 
 def kernel_code_sha() -> str:
-    """First 16 hex digits of the SHA-256 of the kernel source's code: comments removed and
-    every run of whitespace folded to one space, so that an edit to a comment does not void
-    the recorded counters while any change to the code does."""
-    text = open(KERNEL_SRC).read()
+    """First 16 hex digits of the SHA-256 of the kernels' code: the segment layout and tile
+    constants (program.h) and the device part of passes.cu (everything before its host-side
+    section), with comments removed and every run of whitespace folded to one space. An edit
+    to a comment or to the host-side launch code keeps the recorded counters; any change to
+    what the kernels execute voids them."""
+    src = open(KERNEL_SRC).read()
+    cut = src.find(HOST_SIDE_MARK)
+    if cut >= 0:
+        src = src[:cut]
+    text = open(KERNEL_HDR).read() + "\n" + src
     text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
     text = re.sub(r"//[^\n]*", " ", text)
     text = " ".join(text.split())

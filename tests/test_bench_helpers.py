@@ -9,15 +9,24 @@ import oracle as orc
 import synth
 
 
-def test_kernel_code_sha_ignores_comments_only(tmp_path, monkeypatch):
-    src = tmp_path / "k.cu"
-    src.write_text("// header\n__global__ void k(int* p) {\n  p[0] = 1;  // store\n}\n")
+def test_kernel_code_sha_ignores_comments_and_host_code(tmp_path, monkeypatch):
+    src, hdr = tmp_path / "k.cu", tmp_path / "k.h"
+    mark = bench.HOST_SIDE_MARK
+    hdr.write_text("constexpr int kTile = 4;\n")
+    src.write_text("// header\n__global__ void k(int* p) {\n  p[0] = 1;  // store\n}\n"
+                   + mark + "\nvoid launch() { k<<<1, 1>>>(nullptr); }\n")
     monkeypatch.setattr(bench, "KERNEL_SRC", str(src))
+    monkeypatch.setattr(bench, "KERNEL_HDR", str(hdr))
     h0 = bench.kernel_code_sha()
-    src.write_text("/* another\n header */\n__global__ void k(int* p) {\n    p[0] = 1;\n}\n")
-    assert bench.kernel_code_sha() == h0          # comments and layout only
-    src.write_text("__global__ void k(int* p) {\n  p[0] = 2;\n}\n")
-    assert bench.kernel_code_sha() != h0          # a code change voids the counters
+    src.write_text("/* another\n header */\n__global__ void k(int* p) {\n    p[0] = 1;\n}\n"
+                   + mark + "\nvoid launch() { k<<<2, 1>>>(nullptr); }\n")
+    assert bench.kernel_code_sha() == h0          # comments, layout and host code only
+    src.write_text("__global__ void k(int* p) {\n  p[0] = 2;\n}\n" + mark + "\n")
+    assert bench.kernel_code_sha() != h0          # a device-code change voids the counters
+    src.write_text("__global__ void k(int* p) {\n  p[0] = 1;\n}\n" + mark + "\n")
+    assert bench.kernel_code_sha() == h0
+    hdr.write_text("constexpr int kTile = 8;\n")
+    assert bench.kernel_code_sha() != h0          # so does a change to the shared constants
 
 
 def test_all_cores_split_gives_the_single_call_result():
