@@ -874,18 +874,21 @@ cudaError_t launch_typed(const std::vector<Seg>& segs, float scale, cudaStream_t
   return cudaSuccess;
 }
 
+// Resident CTAs per SM of the one-launch kernel on the current device (the cooperative
+// grid must fit), cached per device.
 template <class P, int U>
 int fused_blocks_per_sm() {
-  static int cached = 0;
-  if (cached == 0) {
-    int nb = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, relay_fused_kernel<P, U>, kThreads, 0) !=
-            cudaSuccess ||
-        nb <= 0)
-      nb = 1;
-    cached = nb;
-  }
-  return cached;
+  static int cached[kMaxDevices] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+  if (dev >= 0 && dev < kMaxDevices && cached[dev] > 0) return cached[dev];
+  int nb = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, relay_fused_kernel<P, U>, kThreads, 0) !=
+          cudaSuccess ||
+      nb <= 0)
+    nb = 1;
+  if (dev >= 0 && dev < kMaxDevices) cached[dev] = nb;
+  return nb;
 }
 
 bool cooperative_supported() {
