@@ -524,12 +524,17 @@ def run_ours(args):
             return e0.elapsed_time(e1)
 
         if args.e2e_copy == "auto":
-            # the pipeline itself, 3 steps per way of copying, outside the timed region: on
-            # some boxes a copy engine runs at a third of its rate when the other direction
-            # is idle, which the single- and paired-copy rates alone do not predict
-            trial = {m: pipeline(m, 3) for m in ("torch", "library-in", "library-out", "library")}
-            calib["pipeline_3_steps_ms"] = {m: round(t, 2) for m, t in trial.items()}
-            e2e_mode = min(trial, key=trial.get)
+            # the pipeline itself, 3 steps per way of copying, twice in turn, outside the
+            # timed region; each way is scored by its slower trial. On some boxes the copy
+            # engines slow down several-fold inside the pipeline, and not steadily, which the
+            # single- and paired-copy rates alone do not predict.
+            modes = ("torch", "library-in", "library-out", "library")
+            trials = {m: [] for m in modes}
+            for _ in range(2):
+                for m in modes:
+                    trials[m].append(pipeline(m, 3))
+            calib["pipeline_3_steps_ms"] = {m: [round(t, 2) for t in ts] for m, ts in trials.items()}
+            e2e_mode = min(modes, key=lambda m: max(trials[m]))
         e2e_ms = pipeline(e2e_mode, e2e_steps)
         del sets
 
