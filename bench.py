@@ -38,7 +38,7 @@ SCALE = 0.5
 WORKLOAD = "allreduce A=2 of R=8, bf16 (fp32 accumulate), 1 GiB per rank, scale 1/2"
 CPU_SAMPLE = 1 << 24         # elements per rank in one step of the reference arm
 CPU_BASELINE_SAMPLE = 1 << 27  # elements per rank of the bench's own CPU-baseline leg
-PROFILE = os.path.join(ROOT, "profiles", "relay_pass_kernel_allreduce_a2_bf16_1g.md")
+PROFILE = os.path.join(ROOT, "profiles", "relay_pass_kernel_allreduce_a2_bf16_1g.json")
 KERNEL_SRC = os.path.join(ROOT, "pack_virtual_rank_gb300", "csrc", "passes.cu")
 KERNEL_HDR = os.path.join(ROOT, "pack_virtual_rank_gb300", "csrc", "program.h")
 HOST_SIDE_MARK = "// ------------------------------------------------------------------- host side --"
@@ -104,26 +104,26 @@ def kernel_code_sha() -> str:
 
 
 def _profiled_traffic():
-    """Per-launch DRAM bytes of the dominant pass from the committed ncu summary, or
-    None when the kernel source changed since the counters were taken."""
-    try:
-        text = open(PROFILE).read()
-    except OSError:
-        return None, None
+    """Per-launch DRAM bytes of each pass of the bench workload from the committed ncu
+    counters (a small JSON file beside the profile summary), or None when the kernels'
+    code changed since the counters were taken."""
     sha = kernel_code_sha()
-    m_sha = re.search(r"kernel_code_sha256_16:\s*([0-9a-f]+)", text)
-    out = {}
-    for m in re.finditer(r"traffic_bytes_per_launch\[(\w+)\]:\s*([0-9]+)", text):
-        out[m.group(1)] = int(m.group(2))
-    if not m_sha or m_sha.group(1) != sha:
+    try:
+        with open(PROFILE) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
         return None, sha
-    return out, sha
+    if rec.get("kernel_code_sha256_16") != sha:
+        return None, sha
+    return {k: int(v) for k, v in rec.get("traffic_bytes_per_launch", {}).items()}, sha
 
 
 class Clocks:
-    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region.
+    summary() covers every sample; window(t0, t1) only those taken between two
+    time.time() readings (each sample carries nvidia-smi's local-time timestamp)."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -154,31 +154,49 @@ class Clocks:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
-    def summary(self):
+    def _samples(self):
+        """(unix time, sm MHz, max MHz, active reasons) of every sample so far."""
+        import datetime
         if self.proc is None:
-            self.out.close()
-            os.unlink(self.out.name)
-            return None
-        self.out.seek(0)
-        sm, mx, reasons = [], [], set()
+            return []
+        self.out.flush()
+        with open(self.out.name) as f:
+            text = f.read()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.out.read().splitlines():
+        rows = []
+        for line in text.splitlines():
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                sm.append(float(parts[1]))
-                mx.append(float(parts[2]))
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                sm, mx = float(parts[2]), float(parts[3])
             except ValueError:
                 continue
-            for nm, v in zip(names, parts[5:9]):
-                if v.lower() == "active":
-                    reasons.add(nm)
-        os.unlink(self.out.name)
-        if not sm:
+            rows.append((ts, sm, mx, {nm for nm, v in zip(names, parts[6:10])
+                                      if v.lower() == "active"}))
+        return rows
+
+    @staticmethod
+    def _stats(rows):
+        if not rows:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
-                "reasons": sorted(reasons)}
+        return {"sm_mhz": statistics.median(r[1] for r in rows),
+                "sm_max_mhz": max(r[2] for r in rows), "samples": len(rows),
+                "reasons": sorted(set().union(*(r[3] for r in rows)))}
+
+    def window(self, t0, t1):
+        """Clock summary of the samples taken between unix times t0 and t1."""
+        return self._stats([r for r in self._samples() if t0 <= r[0] <= t1])
+
+    def summary(self):
+        rows = self._samples()
+        self.out.close()
+        try:
+            os.unlink(self.out.name)
+        except OSError:
+            pass
+        return self._stats(rows)
 
 
 def _cpu_oracle(sample: int, seed_config: int = 2, inputs=None):
@@ -370,17 +388,29 @@ def whole_job_gbs(bytes_per_step, steps, world, ms):
     return bytes_per_step * steps * world / (ms / 1e3) / 1e9
 
 
+def relay_allreduce_a2_bytes(g, esize):
+    """Algorithmic bytes (read + written) of the 2-active relay allreduce's passes, from
+    the oracle's plan `g` (chunk c, direct regions dirA and dirB, H helpers):
+      group 1: each active sends H relay chunks and dirA: 2(H*c + dirA) read and written;
+      group 2: each helper reads two slots and writes the reduced chunk to both actives
+               (2c + 2c), each active sends dirB: 4*H*c + 4*dirB;
+      active reduce: each active reads its own and the received dirA + dirB and writes
+               the result: 6 (dirA + dirB).
+    With dirA = dirB = c and H = 6 that is 68 c elements per call."""
+    assert g["kind"] == 0 and g["A"] == 2, "relay schedule, 2 actives"
+    H, c, da, db = g["H"], g["chunk"], g["dirA"], g["dirB"]
+    elems = 4 * (H * c + da) + 4 * H * c + 4 * db + 6 * (da + db)
+    return elems * esize
+
+
 def run_reference(args):
     rank, world, _ = _dist()
     if rank != 0:
         return 0
-    import pack_virtual_rank_gb300.build as b
-    b.build()
-    import pack_virtual_rank_gb300 as rv
     import oracle
     oracle.build()
-    plan = rv.relay_plan(rv.ALLREDUCE, CPU_SAMPLE, rv.BF16, A, R)
-    nbytes, _ = _bytes_per_step(plan, rv)
+    g, _ = oracle.plan(oracle.AR, A, R, CPU_SAMPLE, 2)
+    nbytes = relay_allreduce_a2_bytes(g, 2)
     for _ in range(args.warmup):
         _cpu_oracle(CPU_SAMPLE)
     ts = [_cpu_oracle(CPU_SAMPLE) for _ in range(args.steps)]
@@ -461,6 +491,14 @@ def run_ours(args):
     clocks = clk.summary()
     per_pass = [statistics.mean(ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(args.steps))
                 for i in range(npass)]
+
+    # every other workload of the metric at one size, timed the same way with its own
+    # clock record (rank 0 only: replicas add nothing to a per-collective table)
+    per_wl = None
+    if rank == 0 and count == COUNT and not args.kernel_only and not args.no_per_workload:
+        with Clocks(local) as clk_wl:
+            per_wl = run_per_workload(rv, synth, dev, args.steps, args.warmup, _peaks()[0], clk_wl)
+        clk_wl.summary()
 
     # end to end: every step copies its inputs in from pinned host memory, runs the same
     # public call, and copies its results back to pinned host memory. Two device buffer
@@ -623,11 +661,149 @@ def run_ours(args):
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks,
         }
+        if per_wl is not None:
+            head = {"workload": "2: allreduce A=2 of R=8, bf16, 1 GiB per rank (the headline above)",
+                    "collective": "allreduce", "A": A, "R": R, "dtype": "bf16", "count": count,
+                    "schedule": line["config"]["schedule"], "bytes_per_call": nbytes,
+                    "calls_timed": args.steps, "ms": round(ms / args.steps, 5),
+                    "gbs": round(nbytes / (ms / args.steps) / 1e6, 1),
+                    "frac": round(nbytes / (ms / args.steps) / 1e6 / peak, 4),
+                    "timing": "back-to-back calls, pass events, inputs larger than L2",
+                    "clocks": clocks, "passes": line["passes"]}
+            line["per_workload"] = [per_wl[0], head] + per_wl[1:]
         print(json.dumps(line))
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
     return 0
+
+
+MB = 1 << 20
+
+
+def per_workload_points():
+    """One size of each workload the metric names, at the top of its range, plus the odd
+    segmentCount the all-to-all workload asks for: (label, collective, A, dtype, count,
+    schedule). count is the collective's own count (allreduce: elements per rank;
+    reduce-scatter: recvCount; all-gather: sendCount; all-to-all: segmentCount)."""
+    return [
+        ("1: allreduce A=2 of R=8, fp32, 65536 elements, relay forced",
+         "allreduce", 2, "f32", 65536, "relay"),
+        ("3: reduce-scatter A=2 of R=8, fp32, 512 MB of input per rank",
+         "reduce_scatter", 2, "f32", 512 * MB // 4 // 2, "auto"),
+        ("3: reduce-scatter A=2 of R=8, int32, 512 MB of input per rank",
+         "reduce_scatter", 2, "i32", 512 * MB // 4 // 2, "auto"),
+        ("4: allreduce A=4 of R=8, bf16, 1 GiB per rank",
+         "allreduce", 4, "bf16", 1024 * MB // 2, "auto"),
+        ("4: reduce-scatter A=4 of R=8 (flat, fp32 partial), bf16, 1 GiB of input per rank",
+         "reduce_scatter", 4, "bf16", 1024 * MB // 2 // 4, "auto"),
+        ("5: all-gather A=4 of R=8, bf16, 1 GiB per rank",
+         "all_gather", 4, "bf16", 1024 * MB // 2, "relay"),
+        ("5: all-gather A=4 of R=8, int32, 1 GiB per rank",
+         "all_gather", 4, "i32", 1024 * MB // 4, "relay"),
+        ("5: all-to-all A=4 of R=8, bf16, 1 GiB workload count (segmentCount = count/12)",
+         "all_to_all", 4, "bf16", 1024 * MB // 2 // 12, "relay"),
+        ("5: all-to-all A=4 of R=8, bf16, 1 GiB workload count, odd segmentCount",
+         "all_to_all", 4, "bf16", 1024 * MB // 2 // 12 + 1, "relay"),
+        ("5: all-to-all A=4 of R=8, int32, 1 GiB workload count (odd segmentCount)",
+         "all_to_all", 4, "i32", 1024 * MB // 4 // 12, "relay"),
+    ]
+
+
+def run_per_workload(rv, synth, dev, steps, warmup, peak, clk, min_window_s=0.3):
+    """Each per_workload_points() entry timed on the device like the headline: warm-up
+    calls, then rounds of `steps` calls, each call recording CUDA events before every pass
+    and after the last, until at least `min_window_s` has passed so that the clock
+    sampler sees the timed window. Calls whose buffers fit twice in L2 run one call per
+    timed window after a flush (a buffer twice the L2 written, another read), timed around
+    the call as a user makes it (the library's default launch policy, no pass events);
+    larger ones run back to back (their inputs exceed L2)."""
+    import torch
+    colls = {"allreduce": rv.ALLREDUCE, "reduce_scatter": rv.REDUCE_SCATTER,
+             "all_gather": rv.ALL_GATHER, "all_to_all": rv.ALL_TO_ALL}
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2 // 4, dtype=torch.float32, device=dev)
+    flush_read = torch.ones(2 * l2 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    out = []
+    for label, name, Ap, dt, count, sched in per_workload_points():
+        coll, d = colls[name], rv.dtype_code(dt)
+        opts0 = rv.make_opts(schedule=rv.SCHEDULE_RELAY if sched == "relay" else rv.SCHEDULE_AUTO)
+        plan = rv.relay_plan(coll, count, d, Ap, R, opts0)
+        passes = rv.relay_plan_passes(plan)
+        nbytes = sum(q["bytes_read"] + q["bytes_written"] for q in passes)
+        xs = [synth.rank_input(9, r, plan.input_elems, dt, device=dev) for r in range(Ap)]
+        ys = [torch.empty(plan.output_elems, dtype=xs[0].dtype, device=dev) for _ in range(Ap)]
+        scratch = rv.alloc_scratch(plan, dev)
+        scale = 1.0 if (d == rv.I32 or coll in (rv.ALL_GATHER, rv.ALL_TO_ALL)) else 1.0 / Ap
+        fn = rv.COLLECTIVES[coll]
+        a0 = (xs + [None] * (R - Ap), ys + [None] * (R - Ap), scratch, count, d, Ap, R)
+
+        def call(o):
+            if coll in (rv.ALLREDUCE, rv.REDUCE_SCATTER):
+                fn(*a0, scale, o)
+            else:
+                fn(*a0, o)
+        working = sum(x.numel() * x.element_size() for x in xs + ys)
+        small = working <= 2 * l2
+        for _ in range(warmup):
+            call(opts0)
+        torch.cuda.synchronize()
+        per_call, per_pass, n_calls = [], [[] for _ in passes], 0
+        t0 = time.time()
+        total_ms = 0.0
+        while True:
+            if small:
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                for _ in range(steps):
+                    flush.fill_(1.0)
+                    flush_read.sum()
+                    e0.record(stream)
+                    call(opts0)
+                    e1.record(stream)
+                    torch.cuda.synchronize()
+                    per_call.append(e0.elapsed_time(e1))
+            else:
+                ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(passes) + 1)]
+                      for _ in range(steps)]
+                ops = [rv.make_opts(schedule=opts0.schedule, pass_events=e) for e in ev]
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for k in range(steps):
+                    call(ops[k])
+                e1.record(stream)
+                torch.cuda.synchronize()
+                total_ms += e0.elapsed_time(e1)
+                for k in range(steps):
+                    for i in range(len(passes)):
+                        per_pass[i].append(ev[k][i].elapsed_time(ev[k][i + 1]))
+            n_calls += steps
+            if time.time() - t0 >= min_window_s:
+                break
+        t1 = time.time()
+        ms = statistics.median(per_call) if small else total_ms / n_calls
+        gbs = nbytes / ms / 1e6
+        row = {"workload": label, "collective": name, "A": Ap, "R": R, "dtype": dt, "count": count,
+               "schedule": ["relay", "zero_chunk", "direct", "legacy"][plan.kind],
+               "bytes_per_call": nbytes, "calls_timed": n_calls, "ms": round(ms, 5),
+               "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+               "timing": ("median of single calls, each after an L2 flush, default launch "
+                          "policy" if small else
+                          "back-to-back calls, pass events, inputs larger than L2"),
+               "clocks": clk.window(t0, t1) if clk is not None else None}
+        if not small:
+            row["passes"] = {}
+            for q, ts in zip(passes, per_pass):
+                b = q["bytes_read"] + q["bytes_written"]
+                m = statistics.mean(ts)
+                row["passes"][q["name"]] = {"ms": round(m, 5), "gbs": round(b / m / 1e6, 1),
+                                            "frac": round(b / m / 1e6 / peak, 4)}
+        out.append(row)
+        del xs, ys, scratch, a0
+        torch.cuda.empty_cache()
+    del flush, flush_read
+    torch.cuda.empty_cache()
+    return out
 
 
 def _sweep_points():
@@ -725,6 +901,7 @@ def run_sweep(args):
     print(json.dumps({"device_copy_gbs_this_run": round(copy_gbs, 1), "measured_peak_gbs": peak}),
           flush=True)
     rows = []
+    clk = Clocks(0).__enter__()   # one sampler for the whole sweep; each row its window
     for name, A, dt, nbytes, sched in _sweep_points():
         coll, d = colls[name], dts[dt]
         E = rv.ESIZE[d]
@@ -750,6 +927,8 @@ def run_sweep(args):
                 fn(*a, opts)
         for _ in range(3):
             call(opts0)
+        torch.cuda.synchronize()
+        t_row0 = time.time()
         reps = args.steps
         times = [[] for _ in passes]
         totals = []
@@ -853,6 +1032,7 @@ def run_sweep(args):
             row.update({"ms_call_default_policy": round(wm, 4),
                         "gbs_call_default_policy": round(tot_b / wm / 1e6, 1),
                         "frac_call_default_policy": round(tot_b / wm / 1e6 / peak, 3)})
+        row["clocks"] = clk.window(t_row0, time.time())
         key = (name, A, dt, sched)
         if sched in ("auto", "relay") and nbytes == max(b for n2, a2, d2, b, s2 in _sweep_points()
                                                         if (n2, a2, d2, s2) == key):
@@ -861,13 +1041,19 @@ def run_sweep(args):
         print(json.dumps(row), flush=True)
         del xs, ys, scratch, graph
         torch.cuda.empty_cache()
+    t_rest = time.time()
     rows += _sweep_fused_groups(rv, synth, dev, peak, flush, flush_read, args.steps)
     rows += _sweep_flat_pack(rv, dev, peak, flush, flush_read, args.steps)
+    rest_clocks = clk.window(t_rest, time.time())
+    for row in rows:
+        row.setdefault("clocks", rest_clocks)
+    clk.__exit__(None, None, None)
+    sweep_clocks = clk.summary()
     if args.sweep_out:
         with open(args.sweep_out, "w") as f:
             json.dump({"peak_gbs": peak, "device_copy_gbs_this_run": round(copy_gbs, 1),
                        "hbm_theoretical_gbs": _theoretical_hbm_gbs(dev),
-                       "rows": rows}, f, indent=1)
+                       "clocks": sweep_clocks, "rows": rows}, f, indent=1)
     return 0
 
 
@@ -1023,7 +1209,10 @@ def main():
     ap.add_argument("--e2e-ctas", type=int, default=0,
                     help="CTA cap of the end-to-end leg's relay_copy launches (0: half the SMs)")
     ap.add_argument("--kernel-only", action="store_true",
-                    help="time the device passes only (no end-to-end leg, no CPU baseline)")
+                    help="time the device passes only (no end-to-end leg, no CPU baseline, "
+                         "no per-workload table)")
+    ap.add_argument("--no-per-workload", action="store_true",
+                    help="skip the per-workload table (every other workload at one size)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)   # at least 3 untimed steps before timing
     if args.impl == "reference":

@@ -86,15 +86,20 @@ typedef enum {
  * segments and records no pass events runs as ONE cooperative launch whose passes are
  * separated by grid-wide barriers; any other call launches each pass separately. */
 #define RELAY_FUSED_MAX_BYTES (256ll << 20)
-#define RELAY_FLAG_PAYLOAD_PARTIAL 16 /* 4-active reduce-scatter, bf16 payload: carry each
-                                      helper's partial to its owner in the payload type,
-                                      one payload-sized chunk per return hop as in the link
-                                      model (item 6). The partial is then rounded to bf16
-                                      before the owner adds its own value: a second rounding
-                                      that can move results several ulps off the exact sum.
-                                      Without this flag the partial crosses in fp32 (twice
-                                      the bytes of that hop, H*chunk more owner scratch) and
-                                      results stay within half an ulp of the exact sum. */
+#define RELAY_FLAG_PAYLOAD_PARTIAL 16 /* 4-active reduce-scatter, bf16 payload. By default
+                                      (flag clear) each helper's partial crosses to its owner
+                                      in fp32: twice the bytes of that hop and H*chunk + 128
+                                      more elements of owner scratch; the owner adds its own
+                                      value and the partial, scales once and rounds once, so
+                                      results are within one bf16 ulp of the fp32-accumulated
+                                      sum (and of the exact sum unless a tiny term needs more
+                                      than 24 bits next to large ones). With the flag set the
+                                      partial crosses in the payload type, one payload-sized
+                                      chunk per return hop as in the link model (item 6): it
+                                      is rounded to bf16 at the helper before the owner adds,
+                                      a second rounding that can move a result several ulps
+                                      off the exact sum on cancelling inputs. fp32 and int32
+                                      payloads are unaffected. */
 
 typedef struct relay_opts {
   int32_t offload_permille;      /* A=4 allreduce / reduce-scatter / all-gather offload share;
@@ -228,9 +233,12 @@ int64_t relay_passthrough_helper_size(int64_t count_g, int A, int num_chunks);
  * scale multiplies the fp32 sum once before the cast: 1 for SUM, 1/A for AVG
  * (D115998376); int32 accepts only scale == 1 (integer AVG is undefined).
  * Arithmetic: fp32 and bf16 sum in fp32 in ascending source rank, multiply by scale
- * once, round to nearest-even into the payload type; int32 sums wrap modulo 2^32. A
- * value is rounded to the payload type wherever it crosses a link (the 4-active
- * reduce-scatter's helper partial, item 6).
+ * once, round to nearest-even into the payload type; int32 sums wrap modulo 2^32. The
+ * one partial sum that crosses a link, the 4-active relay reduce-scatter's helper partial
+ * (item 6), is summed over the A-1 non-owner sources in ascending rank; the owner then
+ * adds its own value first and the partial second. For a bf16 payload the partial
+ * crosses in fp32 unless RELAY_FLAG_PAYLOAD_PARTIAL asks for the payload type (see that
+ * flag for the rounding each choice gives).
  * count == 0 returns RELAY_OK without a launch.
  */
 relay_status_t relay_allreduce(void* const* send, void* const* recv, void* const* scratch,

@@ -6,6 +6,9 @@ itself beyond slicing.
 """
 from __future__ import annotations
 
+import concurrent.futures as cf
+import os
+
 import numpy as np
 import torch
 
@@ -63,6 +66,8 @@ def run(coll, A, R, count, dtype, scale=1.0, config=0, schedule=rv.SCHEDULE_AUTO
     c = Call()
     c.plan, c.coll, c.A, c.R, c.count, c.dtype, c.scale = plan, coll, A, R, count, dtype, scale
     c.in_place = in_place
+    read_request(c, schedule, permille, flags)
+    assert_plan_agrees(c)
     xs = inputs if inputs is not None else make_inputs(config, A, plan.input_elems, dtype, device,
                                                        gpu_generator)
     c.inputs = xs
@@ -114,11 +119,53 @@ def run(coll, A, R, count, dtype, scale=1.0, config=0, schedule=rv.SCHEDULE_AUTO
     return c
 
 
+OCOLL = {rv.ALLREDUCE: orc.AR, rv.REDUCE_SCATTER: orc.RS, rv.ALL_GATHER: orc.AG,
+         rv.ALL_TO_ALL: orc.A2A}
+OFORCE = {rv.SCHEDULE_AUTO: orc.FORCE_AUTO, rv.SCHEDULE_RELAY: orc.FORCE_RELAY,
+          rv.SCHEDULE_DIRECT: orc.FORCE_DIRECT, rv.SCHEDULE_LEGACY: orc.FORCE_LEGACY}
+
+
+def read_request(c, schedule=rv.SCHEDULE_AUTO, permille=-1, flags=0):
+    """What the oracle needs to know about a call, taken from the request and the oracle's
+    own plan only (never from the library under test):
+      c.oplan -- the oracle's planner restatement of the request;
+      c.span  -- positions of each reduce-scatter block reduced at a helper: H * chunk of
+                 the 4-active relay reduce-scatter (item 6), 0 otherwise;
+      c.wide  -- the 4-active bf16 relay reduce-scatter carries its helper partial in fp32
+                 unless the request sets FLAG_PAYLOAD_PARTIAL (the library's documented
+                 default); every other call has no partial."""
+    pm = 500 if permille < 0 else permille
+    c.oplan, _ = orc.plan(OCOLL[c.coll], c.A, c.R, c.count, rv.ESIZE[c.dtype], permille=pm,
+                          force=OFORCE[schedule])
+    relay_rs4 = (c.coll == rv.REDUCE_SCATTER and c.A > 2 and c.oplan["kind"] == orc.KIND_RELAY)
+    c.span = c.oplan["H"] * c.oplan["chunk"] if relay_rs4 else 0
+    c.wide = relay_rs4 and c.dtype == rv.BF16 and not (flags & rv.FLAG_PAYLOAD_PARTIAL)
+    return c
+
+
+def assert_plan_agrees(c):
+    """The library's plan of the call equals the oracle's restatement (checked on its own,
+    apart from the results)."""
+    p, g = c.plan, c.oplan
+    assert (p.kind, p.num_groups, p.chunk) == (g["kind"], g["groups"], g["chunk"])
+    if c.A == 2:
+        assert (p.dirA_offset, p.dirA_size, p.dirB_size) == (g["dirA_off"], g["dirA"], g["dirB"])
+    else:
+        assert (p.direct_total, p.direct_g1, p.direct_g2) == (g["pD"], g["d1"], g["d2"])
+        assert (p.owner_slice, p.owner_slice_last) == (g["owner_slice"], g["owner_last"])
+    assert p.wide_partial == int(c.wide)
+
+
+def out_elems(c) -> int:
+    """Output elements per active, from the request: A blocks for all-gather and
+    all-to-all, one for allreduce and reduce-scatter (D115998376, D115998385, D115998370)."""
+    return c.A * c.count if c.coll in (rv.ALL_GATHER, rv.ALL_TO_ALL) else c.count
+
+
 def helper_span(c) -> int:
-    """Positions of each reduce-scatter block reduced at a helper (4-active relay)."""
-    if c.coll == rv.REDUCE_SCATTER and c.A > 2 and c.plan.kind == rv.KIND_RELAY:
-        return c.plan.relay_total
-    return 0
+    """Positions of each reduce-scatter block reduced at a helper (4-active relay), from
+    the oracle's plan."""
+    return c.span
 
 
 def expected(c, xs_host, rank, i0, i1):
@@ -128,7 +175,7 @@ def expected(c, xs_host, rank, i0, i1):
         r64, r32, rq = orc.allreduce(d, xs_host, c.scale, i0, i1)
         return rq, r32, r64
     if c.coll == rv.REDUCE_SCATTER:
-        rs = orc.reduce_scatter_wide if c.plan.wide_partial else orc.reduce_scatter
+        rs = orc.reduce_scatter_wide if c.wide else orc.reduce_scatter
         r64, r32, rq = rs(d, xs_host, n, rank, c.scale, helper_span(c), i0, i1)
         return rq, r32, r64
     if c.coll == rv.ALL_GATHER:
@@ -147,7 +194,10 @@ def bf16_ulp(x: np.ndarray) -> np.ndarray:
 
 def check_window(c, rank, i0, i1, xs_host):
     """Compare output window [i0, i1) of active `rank` with the oracle."""
-    got = host(c.recv[rank][i0:i1])
+    _compare_window(c, rank, i0, i1, xs_host, host(c.recv[rank][i0:i1]))
+
+
+def _compare_window(c, rank, i0, i1, xs_host, got):
     q, r32, r64 = expected(c, xs_host, rank, i0, i1)
     if c.dtype == rv.I32 or r32 is None:
         assert np.array_equal(got, q), _first_diff(got, q, i0)
@@ -195,7 +245,7 @@ def check_all(c):
     """Full comparison of every active output, inputs unchanged, canaries intact."""
     xs_host = [host(x) for x in c.inputs]
     for a in range(c.A):
-        check_window(c, a, 0, c.plan.output_elems, xs_host)
+        check_window(c, a, 0, out_elems(c), xs_host)
     check_common(c, xs_host)
 
 
@@ -210,28 +260,28 @@ def check_common(c, xs_host):
 def boundaries(c):
     """Output positions where the schedule switches region: chunk, slice and direct
     boundaries and the ends, for sampled checks of large outputs."""
-    p = c.plan
-    pts = {0, p.output_elems}
-    n = p.count
-    if p.A == 2:
-        cs = p.chunk
-        for h in range(p.H + 2):
+    g = c.oplan
+    total = out_elems(c)
+    pts = {0, total}
+    n = c.count
+    if c.A == 2:
+        cs = g["chunk"]
+        for h in range(g["H"] + 2):
             pts.add(h * cs)
-        pts.update({p.dirA_offset, p.dirA_offset + p.dirA_size,
-                    p.dirA_offset + p.dirA_size + p.dirB_size})
+        pts.update({g["dirA_off"], g["dirA_off"] + g["dirA"], g["dirA_off"] + g["dirA"] + g["dirB"]})
     else:
-        oc = p.chunk
-        for h in range(p.H + 1):
+        oc = g["chunk"]
+        for h in range(g["H"] + 1):
             pts.add(h * oc)
-        P = p.relay_total
-        pts.update({P, P + p.direct_g1, P + p.owner_slice, P + 2 * p.owner_slice,
-                    P + 3 * p.owner_slice, n})
-    blocks = p.output_elems // max(n, 1)
+        P = g["H"] * oc
+        pts.update({P, P + g["d1"], P + g["owner_slice"], P + 2 * g["owner_slice"],
+                    P + 3 * g["owner_slice"], n})
+    blocks = total // max(n, 1)
     out = set()
     for b in range(max(blocks, 1)):
         for q in pts:
             v = b * n + q if blocks > 1 else q
-            if 0 <= v <= p.output_elems:
+            if 0 <= v <= total:
                 out.add(v)
     return sorted(out)
 
@@ -241,7 +291,7 @@ def check_sampled(c, width=512, seed=0, n_random=8):
     block boundaries. For each window only the input ranges it depends on are fetched,
     laid out as a tiny input whose oracle result is exactly that window."""
     rng = np.random.default_rng(seed)
-    total, n = c.plan.output_elems, c.count
+    total, n = out_elems(c), c.count
     centres = boundaries(c) + [int(v) for v in rng.integers(0, max(total, 1), n_random)]
     for a in range(c.A):
         for ctr in centres:
@@ -267,7 +317,7 @@ def _check_block_window(c, rank, k, lo, hi):
             t[rank * w:(rank + 1) * w] = host(x[rank * n + lo: rank * n + hi])
             tiny.append(t)
         span = max(0, min(helper_span(c) - lo, w))
-        rs = orc.reduce_scatter_wide if c.plan.wide_partial else orc.reduce_scatter
+        rs = orc.reduce_scatter_wide if c.wide else orc.reduce_scatter
         exp = rs(d, tiny, w, rank, c.scale, span)[2]
     elif c.coll == rv.ALL_GATHER:
         tiny = [np.zeros(w, dtype=NP[d]) for _ in range(A)]
@@ -286,3 +336,63 @@ def _check_block_window(c, rank, k, lo, hi):
 
 
 NP = {rv.F32: np.float32, rv.BF16: np.uint16, rv.I32: np.int32}
+
+
+FULL_WINDOW = 1 << 22     # output elements per oracle window of check_full
+
+
+def _threads():
+    try:
+        return max(1, min(16, len(os.sched_getaffinity(0))))
+    except AttributeError:
+        return max(1, min(16, os.cpu_count() or 1))
+
+
+def check_full(c):
+    """Every output element of every active compared with the oracle, at any size.
+
+    The outputs and inputs are copied to the host once; the output is cut into windows of
+    FULL_WINDOW elements (split at block boundaries) and each window is compared with the
+    oracle's result for that window on a pool of host threads (the oracle's C calls release
+    the GIL). Allreduce and reduce-scatter windows go through check_window (bit-exact plus
+    the stated tolerances); all-gather and all-to-all windows feed the oracle the input
+    ranges the window depends on, laid out as a small input whose whole result is that
+    window. Canaries and untouched inputs are checked as in check_all."""
+    xs_host = [host(x) for x in c.inputs]
+    total, n = out_elems(c), c.count
+    got = [host(c.recv[a]) for a in range(c.A)]
+    windows = []
+    i0 = 0
+    while i0 < total:
+        k = i0 // n if n else 0
+        i1 = min(total, i0 + FULL_WINDOW, (k + 1) * n)
+        windows.append((k, i0, i1))
+        i0 = i1
+
+    def one(w):
+        k, lo, hi = w
+        if c.coll == rv.ALLREDUCE:
+            # every active holds the same result: the oracle's window once, then the
+            # other actives bit for bit against the first
+            _compare_window(c, 0, lo, hi, xs_host, got[0][lo:hi])
+            for a in range(1, c.A):
+                assert np.array_equal(got[a][lo:hi], got[0][lo:hi]), _first_diff(
+                    got[a][lo:hi], got[0][lo:hi], lo)
+            return
+        if c.coll == rv.REDUCE_SCATTER:
+            for a in range(c.A):
+                _compare_window(c, a, lo, hi, xs_host, got[a][lo:hi])
+            return
+        bl, bh = lo - k * n, hi - k * n
+        for a in range(c.A):
+            if c.coll == rv.ALL_GATHER:
+                exp = orc.all_gather([x[bl:bh] for x in xs_host], bh - bl)[k * (bh - bl):(k + 1) * (bh - bl)]
+            else:
+                tiny = [np.concatenate([x[dd * n + bl: dd * n + bh] for dd in range(c.A)])
+                        for x in xs_host]
+                exp = orc.all_to_all(tiny, bh - bl, a)[k * (bh - bl):(k + 1) * (bh - bl)]
+            assert np.array_equal(got[a][lo:hi], exp), _first_diff(got[a][lo:hi], exp, lo)
+
+    with cf.ThreadPoolExecutor(_threads()) as ex:
+        list(ex.map(one, windows))
+    check_common(c, xs_host)

@@ -56,3 +56,64 @@ def test_whole_job_throughput_counts_every_replica():
     # 2 replicas each moving 1 GB per step, 10 steps, slowest rank 20 ms: 1000 GB/s
     assert abs(bench.whole_job_gbs(1e9, 10, 2, 20.0) - 1000.0) < 1e-9
     assert os.path.exists(bench.PROFILE)
+
+
+def test_reference_arm_bytes_from_the_oracle_plan():
+    # the reference arm counts the relay allreduce's pass bytes from the oracle's plan
+    # alone; they must equal what the library reports for the same schedule
+    import pack_virtual_rank_gb300 as rv
+    for count in (1 << 24, 65536, 1 << 20, (1 << 22) + 4099, bench.CPU_SAMPLE):
+        g, _ = orc.plan(orc.AR, 2, 8, count, 2, force=orc.FORCE_RELAY)
+        p = rv.relay_plan(rv.ALLREDUCE, count, rv.BF16, 2, 8, rv.make_opts(schedule=rv.SCHEDULE_RELAY))
+        lib = sum(q["bytes_read"] + q["bytes_written"] for q in rv.relay_plan_passes(p))
+        assert bench.relay_allreduce_a2_bytes(g, 2) == lib
+    g, _ = orc.plan(orc.AR, 2, 8, 1 << 24, 2)
+    assert bench.relay_allreduce_a2_bytes(g, 2) == 68 * g["chunk"] * 2
+
+
+def test_reference_arm_does_not_load_the_product_library():
+    import inspect
+    src = inspect.getsource(bench.run_reference)
+    assert "pack_virtual_rank_gb300" not in src and "rv." not in src
+
+
+def test_clock_windows(tmp_path):
+    import datetime
+    c = bench.Clocks(0, enabled=False)
+    t0 = datetime.datetime(2026, 1, 2, 3, 4, 5).timestamp()
+    lines = []
+    for k in range(10):
+        ts = datetime.datetime.fromtimestamp(t0 + 0.1 * k).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+        reason = "Active" if k == 7 else "Not Active"
+        lines.append(f"{ts}, 0, {1900 + k}, 2070, 900.0, 0x0, Not Active, Not Active, "
+                     f"Not Active, {reason}")
+    c.out.write("\n".join(lines + ["garbage line"]) + "\n")
+    c.proc = object()                      # as if nvidia-smi had been started
+    w = c.window(t0 + 0.15, t0 + 0.55)      # samples 2..5
+    assert w["samples"] == 4 and w["reasons"] == [] and w["sm_mhz"] == 1903.5
+    w = c.window(t0, t0 + 1.0)
+    assert w["samples"] == 10 and w["reasons"] == ["sw_power_cap"] and w["sm_max_mhz"] == 2070
+    assert c.summary()["samples"] == 10
+
+
+def test_per_workload_points_cover_the_metric():
+    pts = bench.per_workload_points()
+    have = {(name, A, dt) for _, name, A, dt, _, _ in pts}
+    assert ("allreduce", 2, "f32") in have
+    assert {("reduce_scatter", 2, "f32"), ("reduce_scatter", 2, "i32")} <= have
+    assert {("allreduce", 4, "bf16"), ("reduce_scatter", 4, "bf16")} <= have
+    assert {(c, 4, d) for c in ("all_gather", "all_to_all") for d in ("bf16", "i32")} <= have
+    odd = [cnt for _, name, _, _, cnt, _ in pts if name == "all_to_all" and cnt % 2 == 1]
+    assert len(odd) >= 2          # bf16 and int32 with an odd segmentCount
+
+
+def test_traffic_record_is_keyed_to_the_kernel_code(tmp_path, monkeypatch):
+    import json
+    rec = tmp_path / "t.json"
+    rec.write_text(json.dumps({"kernel_code_sha256_16": bench.kernel_code_sha(),
+                               "traffic_bytes_per_launch": {"group1": 5}}))
+    monkeypatch.setattr(bench, "PROFILE", str(rec))
+    assert bench._profiled_traffic()[0] == {"group1": 5}
+    rec.write_text(json.dumps({"kernel_code_sha256_16": "0" * 16,
+                               "traffic_bytes_per_launch": {"group1": 5}}))
+    assert bench._profiled_traffic()[0] is None

@@ -55,10 +55,12 @@ def test_fused_groups_match_oracle(coll, A, dtype):
             c = hz.Call()
             c.plan, c.coll, c.A, c.R, c.count, c.dtype, c.scale = (plans[g], coll, A, R, counts[g],
                                                                     dtype, scale)
+            hz.read_request(c, sched, -1, 0)
+            hz.assert_plan_agrees(c)
             gx = [xs[g * A + a] for a in range(A)]
             c.recv = recv[g * A:(g + 1) * A]
             for a in range(A):
-                hz.check_window(c, a, 0, plans[g].output_elems, gx)
+                hz.check_window(c, a, 0, hz.out_elems(c), gx)
         for gd in guards:
             assert gd.guards_intact()
         for r in range(R):

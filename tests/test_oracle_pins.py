@@ -380,3 +380,49 @@ def test_default_crossovers(orc):
     # item 3: A=2 allreduce small messages take one full exchange (one group)
     g = orc.plan(orc.AR, 2, 8, 32 * 1024, 2)[0]
     assert g["kind"] == orc.KIND_DIRECT and g["groups"] == 1
+
+
+# ----------------------------------------------- per-entry tables and contracts ----
+
+_COLL = {"ar": 0, "rs": 1, "ag": 2, "a2a": 3}
+
+
+def _expand(rows, A, R, G):
+    """The golden link table: every (group, sender, receiver) entry the rows name."""
+    t = np.zeros((G, R, R), np.uint64)
+
+    def ranks(spec):
+        if spec == "A":
+            return range(A)
+        if spec == "H":
+            return range(A, R)
+        return [int(spec)]
+    for grp, src, dst, v in rows:
+        for s in ranks(src):
+            for d in ranks(dst):
+                if s != d:
+                    t[int(grp) - 1, s, d] = int(v)
+    return t
+
+
+@pytest.mark.parametrize("coll", ["ar", "rs", "ag", "a2a"])
+def test_a4_link_table_every_entry(orc, coll):
+    # items 4-7: every entry of each group's table, including those below the group's
+    # maximum, worked by hand at one count on a 7-rank node (3 helpers)
+    rows = [r[1:] for r in _rows("link_tables.txt") if r[0] == coll]
+    _, gv = orc.plan(_COLL[coll], 4, 7, 3_000_000, 2, permille=500, force=orc.FORCE_RELAY)
+    got = orc.link_elems(gv)
+    exp = _expand(rows, 4, 7, 2)
+    assert got.shape == exp.shape
+    assert np.array_equal(got, exp), np.argwhere(got != exp)[:5]
+
+
+def test_helper_contract_literals(orc):
+    # every branch of the contract: A=2 with num_chunks = (R-A)+1, and the four 4-active
+    # collectives, against values worked by hand
+    n = 0
+    for coll, A, R, count, exp in _rows("helper_contracts.txt"):
+        assert orc.relay_helper_contract(_COLL[coll], int(A), int(R), int(count)) == int(exp), \
+            (coll, A, R, count)
+        n += 1
+    assert n == 11

@@ -97,9 +97,11 @@ def test_unaligned_buffers(coll, dtype, shift, launch):
         c = hz.Call()
         c.plan, c.coll, c.A, c.R, c.count, c.dtype = plan, coll, A, 8, count, dtype
         c.scale, c.inputs, c.recv = _scale(coll, A, dtype), xs, recv
+        hz.read_request(c, sched, -1, launch)
+        hz.assert_plan_agrees(c)
         xs_host = [hz.host(x) for x in xs]
         for a in range(A):
-            hz.check_window(c, a, 0, plan.output_elems, xs_host)
+            hz.check_window(c, a, 0, hz.out_elems(c), xs_host)
 
 
 def test_many_helpers_split_launches():
@@ -144,7 +146,7 @@ def test_special_values():
             xs_host = [hz.host(x) for x in ins]
             for a in range(A):
                 got = hz.host(c.recv[a])
-                q = hz.expected(c, xs_host, a, 0, c.plan.output_elems)[0]
+                q = hz.expected(c, xs_host, a, 0, hz.out_elems(c))[0]
                 # overflowing pairs make -inf too, so 4-term sums can be NaN: any NaN
                 # matches any NaN (the encoding of a NaN is not part of the contract);
                 # every other value must match bit for bit
@@ -284,9 +286,9 @@ def test_reduce_scatter_partial_precision():
         for flags in (0, rv.FLAG_SEPARATE_PASSES, rv.FLAG_PAYLOAD_PARTIAL):
             c = hz.run(rv.REDUCE_SCATTER, 4, 8, m, rv.BF16, 0.25, config=19,
                        schedule=rv.SCHEDULE_RELAY, in_place=in_place, flags=flags)
-            assert c.plan.wide_partial == (0 if flags & rv.FLAG_PAYLOAD_PARTIAL else 1)
+            assert c.wide == (not flags & rv.FLAG_PAYLOAD_PARTIAL)
             hz.check_all(c)
-            if c.plan.wide_partial:
+            if c.wide:
                 xs = [hz.host(x) for x in c.inputs]
                 for o in range(4):
                     r64 = orc.reduce_scatter(rv.BF16, xs, m, o, 0.25, 0)[0]
