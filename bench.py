@@ -791,6 +791,40 @@ def run_per_workload(rv, synth, dev, steps, warmup, peak, clk, min_window_s=0.3)
                           "policy" if small else
                           "back-to-back calls, pass events, inputs larger than L2"),
                "clocks": clk.window(t0, t1) if clk is not None else None}
+        if small:
+            # the same call captured in a CUDA graph: (a) one replay per timed window after
+            # an L2 flush, timed around the replay (includes the graph launch); (b) 20 calls
+            # in one graph replayed back to back, per call (warm L2, no host in the way)
+            row["launch"] = rv.last_launch()
+            s_g = torch.cuda.Stream()
+            torch.cuda.synchronize()
+            g1, g20 = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g1, stream=s_g):
+                call(opts0)
+            with torch.cuda.graph(g20, stream=s_g):
+                for _ in range(20):
+                    call(opts0)
+            g1.replay()
+            g20.replay()
+            torch.cuda.synchronize()
+            rep = []
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            for _ in range(max(steps, 20)):
+                flush.fill_(1.0)
+                flush_read.sum()
+                e0.record(stream)
+                g1.replay()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                rep.append(e0.elapsed_time(e1))
+            e0.record(stream)
+            for _ in range(5):
+                g20.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            row["graph_replay_ms"] = round(statistics.median(rep), 5)
+            row["graph_back_to_back_ms_per_call"] = round(e0.elapsed_time(e1) / 100, 5)
+            del g1, g20
         if not small:
             row["passes"] = {}
             for q, ts in zip(passes, per_pass):

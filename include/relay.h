@@ -81,10 +81,21 @@ typedef enum {
 #define RELAY_FLAG_SEPARATE_PASSES 4 /* one launch per pass even for small calls */
 #define RELAY_FLAG_FUSED_PASSES 8  /* one cooperative launch for the whole call whenever it
                                       qualifies, whatever its size */
-/* Launch policy: a call of at most RELAY_FUSED_MAX_BYTES of pass traffic that has at most
- * 4 passes and 384 segments (after alignment splitting), has no mixed-width (fp32 partial)
- * segments and records no pass events runs as ONE cooperative launch whose passes are
- * separated by grid-wide barriers; any other call launches each pass separately. */
+#define RELAY_FLAG_CHAINED 32      /* one chained launch for the whole call whenever its
+                                      program allows it, whatever its size */
+/* Launch policy. A call that records pass events, or sets RELAY_FLAG_SEPARATE_PASSES,
+ * launches each pass separately. Any other call of at most RELAY_FUSED_MAX_BYTES of pass
+ * traffic runs as ONE launch:
+ *   - chained, where its program allows: the segments of all passes are cut into pieces
+ *     so that each dependency between passes links identical element ranges; pieces that
+ *     touch the same bytes, one of them writing, form a group; one CTA runs tile t of
+ *     every piece of a group in pass order with a block barrier between passes. No CTA
+ *     waits for another. It takes programs without mixed-width (fp32 partial) segments
+ *     whose pieces number at most 384 after cutting;
+ *   - else cooperative: at most 4 passes and 384 segments after alignment splitting, no
+ *     mixed-width segments; passes separated by grid-wide barriers;
+ *   - else pass by pass.
+ * relay_last_launch() names the form the calling thread's last call took. */
 #define RELAY_FUSED_MAX_BYTES (256ll << 20)
 #define RELAY_FLAG_PAYLOAD_PARTIAL 16 /* 4-active reduce-scatter, bf16 payload. By default
                                       (flag clear) each helper's partial crosses to its owner
@@ -348,6 +359,10 @@ relay_status_t relay_allreduce_noalloc(void* const* send, void* const* recv, siz
 
 /* Human-readable text of the last error this thread's calls produced. */
 const char* relay_last_error(void);
+/* How the calling thread's last collective call was launched: "chained: G groups, P
+ * pieces", "cooperative" or "passes" (see the launch policy above); "dry run" for a
+ * RELAY_FLAG_DRY_RUN call that would not run chained, "none" before the first call. */
+const char* relay_last_launch(void);
 int relay_abi_version(void);
 
 #ifdef __cplusplus

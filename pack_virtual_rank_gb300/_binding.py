@@ -26,6 +26,7 @@ FLAG_DRY_RUN = 2
 FLAG_SEPARATE_PASSES = 4
 FLAG_FUSED_PASSES = 8
 FLAG_PAYLOAD_PARTIAL = 16
+FLAG_CHAINED = 32
 ESIZE = {F32: 4, BF16: 2, I32: 4}
 PASS_NAMES = ("group1", "group2", "group3", "active_reduce", "pack", "helper_forward", "unpack")
 
@@ -80,6 +81,7 @@ def lib():
     L.relay_opts_init.restype = None
     L.relay_abi_version.restype = i32
     L.relay_last_error.restype = ctypes.c_char_p
+    L.relay_last_launch.restype = ctypes.c_char_p
     L.relay_plan.argtypes = [i32, sz, i32, i32, i32, P(RelayOpts), P(RelayPlan)]
     L.relay_plan.restype = i32
     L.relay_plan_link_bytes.argtypes = [P(RelayPlan), P(ctypes.c_uint64), sz]
@@ -129,6 +131,12 @@ def lib():
 def _check(status: int):
     if status != OK:
         raise RelayError(status, lib().relay_last_error().decode(errors="replace"))
+
+
+def last_launch() -> str:
+    """How this thread's last collective call was launched: "chained", "cooperative" or
+    "passes" ("dry run" for a dry run that would not run chained)."""
+    return lib().relay_last_launch().decode()
 
 
 def dtype_code(dtype) -> int:

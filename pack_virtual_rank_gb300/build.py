@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "librelay.so")
 
-SOURCES = ["plan.cpp", "program.cpp", "abi.cpp", "passes.cu", "noalloc.cu"]
+SOURCES = ["plan.cpp", "program.cpp", "chain.cpp", "abi.cpp", "passes.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -16,6 +16,7 @@ namespace relay {
 namespace {
 
 thread_local std::string g_last_error;
+thread_local std::string g_last_launch = "none";
 
 relay_status_t fail(relay_status_t st, const std::string& msg) {
   g_last_error = msg;
@@ -190,25 +191,52 @@ relay_status_t execute(const std::vector<Pass>& passes, const std::vector<Range>
       if (find_hazard(ps, E, &why))
         return fail(RELAY_ERR_UNSUPPORTED, "internal (one-launch phase): " + why);
   }
-  if (flags & RELAY_FLAG_DRY_RUN) return RELAY_OK;
-
-  // small calls: the whole call in one cooperative launch (no pass events there)
+  // Launch policy. Pass events need the per-pass launches. Otherwise a call of at most
+  // RELAY_FUSED_MAX_BYTES of pass traffic (or any call, when forced) runs as one chained
+  // launch where its program allows it, else as one cooperative launch, else pass by pass.
   const bool events_wanted = opts && opts->pass_events;
-  if (!events_wanted && !(flags & RELAY_FLAG_SEPARATE_PASSES)) {
-    int64_t bytes = 0;
-    for (const Pass& ps : passes)
-      for (const Seg& sg : ps.segs) {
-        for (int k = 0; k < sg.nsrc; ++k) bytes += seg_src_bytes(sg, k, E);
-        bytes += seg_dst_bytes(sg, E) * sg.ndst;
-      }
-    if ((flags & RELAY_FLAG_FUSED_PASSES) || bytes <= RELAY_FUSED_MAX_BYTES) {
-      cudaError_t e = cudaSuccess;
-      if (launch_fused(dtype, passes, scale, stream, &e, (flags & RELAY_FLAG_FUSED_PASSES) != 0)) {
-        if (e != cudaSuccess) return fail(RELAY_ERR_CUDA, cudaGetErrorString(e));
-        return RELAY_OK;
-      }
+  const bool one_launch = !events_wanted && !(flags & RELAY_FLAG_SEPARATE_PASSES);
+  int64_t bytes = 0;
+  for (const Pass& ps : passes)
+    for (const Seg& sg : ps.segs) {
+      for (int k = 0; k < sg.nsrc; ++k) bytes += seg_src_bytes(sg, k, E);
+      bytes += seg_dst_bytes(sg, E) * sg.ndst;
+    }
+  const bool small = bytes <= RELAY_FUSED_MAX_BYTES;
+  const bool try_chain = one_launch && passes.size() > 1 && !(flags & RELAY_FLAG_FUSED_PASSES) &&
+                         ((flags & RELAY_FLAG_CHAINED) || small);
+  ChainPlan chain;
+  bool chained = false;
+  if (try_chain) {
+    chained = build_chain(passes, E, &chain, &why);
+    if (chained && (flags & RELAY_FLAG_CHECK_HAZARDS) && !check_chain(chain, E, &why))
+      return fail(RELAY_ERR_UNSUPPORTED, "internal (chained launch): " + why);
+  }
+  const std::string chain_desc =
+      chained ? "chained: " + std::to_string(chain.gn.size()) + " groups, " +
+                    std::to_string(chain.segs.size()) + " pieces"
+              : std::string();
+  if (flags & RELAY_FLAG_DRY_RUN) {
+    g_last_launch = chained ? chain_desc : "dry run";
+    return RELAY_OK;
+  }
+  if (chained) {
+    cudaError_t e = cudaSuccess;
+    if (launch_chain(dtype, chain, scale, stream, &e)) {
+      if (e != cudaSuccess) return fail(RELAY_ERR_CUDA, cudaGetErrorString(e));
+      g_last_launch = chain_desc;
+      return RELAY_OK;
     }
   }
+  if (one_launch && ((flags & RELAY_FLAG_FUSED_PASSES) || small)) {
+    cudaError_t e = cudaSuccess;
+    if (launch_fused(dtype, passes, scale, stream, &e, (flags & RELAY_FLAG_FUSED_PASSES) != 0)) {
+      if (e != cudaSuccess) return fail(RELAY_ERR_CUDA, cudaGetErrorString(e));
+      g_last_launch = "cooperative";
+      return RELAY_OK;
+    }
+  }
+  g_last_launch = "passes";
 
   cudaEvent_t* events = nullptr;
   unsigned record_flags = cudaEventRecordDefault;
@@ -337,6 +365,8 @@ void relay_opts_init(relay_opts_t* o) {
 int relay_abi_version(void) { return RELAY_ABI_VERSION; }
 
 const char* relay_last_error(void) { return g_last_error.c_str(); }
+
+const char* relay_last_launch(void) { return g_last_launch.c_str(); }
 
 relay_status_t relay_plan(relay_coll_t coll, size_t count, relay_dtype_t dtype, int A, int R,
                           const relay_opts_t* opts, relay_plan_t* out) {

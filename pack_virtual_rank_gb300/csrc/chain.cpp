@@ -1,0 +1,215 @@
+// chain.cpp -- host side of the chained launch: a whole call in one ordinary launch, with
+// no grid-wide barrier and no wait of one CTA on another.
+//
+// A call's passes run in order because pass p+1 reads what pass p wrote (a relay chunk
+// landing in a helper's slot, then the helper's reduction of that slot), or writes what an
+// earlier pass read (in-place forms). Every such dependency here is elementwise: element i
+// of a consumer touches exactly element i of its producer. So the segments of all passes
+// can be cut into pieces whose dependent ranges coincide, the pieces that touch the same
+// bytes (one of them writing) joined into a group, and each group tiled: one CTA runs tile
+// t of every piece of a group, in pass order, with a block barrier between passes. Nothing
+// one CTA reads or writes is touched by another CTA, so no CTA ever waits for another,
+// and the schedule's transfers and reductions still run exactly as the passes state them.
+//
+// Page: "Link-balance the sharded relay schedules (up to 3.2x vs NCCL)", items 3 and 5:
+// in the latency-bound regime a group boundary costs a round trip; here it costs a block
+// barrier inside the CTA that holds both sides of it.
+#include <algorithm>
+#include <numeric>
+#include <string>
+#include <vector>
+
+#include "program.h"
+
+namespace relay {
+namespace {
+
+struct Piece {
+  Seg s;
+  int pass;
+  int order;  // position among all pieces in build order (keeps groups deterministic)
+};
+
+struct Operand {
+  uintptr_t lo, hi;  // bytes [lo, hi)
+  int piece;
+  bool write;
+};
+
+void operands(const std::vector<Piece>& ps, int E, std::vector<Operand>* out) {
+  out->clear();
+  for (int i = 0; i < (int)ps.size(); ++i) {
+    const Seg& s = ps[i].s;
+    const uintptr_t bytes = (uintptr_t)s.n * (uintptr_t)E;
+    for (int k = 0; k < s.nsrc; ++k) {
+      const uintptr_t lo = reinterpret_cast<uintptr_t>(s.src[k]);
+      out->push_back(Operand{lo, lo + bytes, i, false});
+    }
+    for (int d = 0; d < s.ndst; ++d) {
+      const uintptr_t lo = reinterpret_cast<uintptr_t>(s.dst[d]);
+      out->push_back(Operand{lo, lo + bytes, i, true});
+    }
+  }
+  std::sort(out->begin(), out->end(), [](const Operand& a, const Operand& b) {
+    return a.lo != b.lo ? a.lo < b.lo : a.hi < b.hi;
+  });
+}
+
+// Every pair of operands of different pieces that overlap, at least one of them written:
+// fn(a, b). Operands are sorted by start, so the partners of operand i are the ones after
+// it that start before it ends.
+template <class Fn>
+void for_each_conflict(const std::vector<Operand>& ops, Fn fn) {
+  for (size_t i = 0; i < ops.size(); ++i)
+    for (size_t j = i + 1; j < ops.size() && ops[j].lo < ops[i].hi; ++j)
+      if (ops[i].piece != ops[j].piece && (ops[i].write || ops[j].write)) fn(ops[i], ops[j]);
+}
+
+int find(std::vector<int>& parent, int x) {
+  while (parent[x] != x) {
+    parent[x] = parent[parent[x]];
+    x = parent[x];
+  }
+  return x;
+}
+
+Seg advance(const Seg& s, int64_t e, int64_t n, int E) {
+  Seg t = s;
+  for (int k = 0; k < t.nsrc; ++k) t.src[k] = static_cast<const char*>(t.src[k]) + e * E;
+  for (int d = 0; d < t.ndst; ++d) t.dst[d] = static_cast<char*>(t.dst[d]) + e * E;
+  t.n = n;
+  return t;
+}
+
+}  // namespace
+
+bool build_chain(const std::vector<Pass>& passes, int E, ChainPlan* out, std::string* why) {
+  auto fail = [&](const std::string& m) {
+    if (why) *why = m;
+    return false;
+  };
+  if (passes.size() > 200) return fail("too many passes");
+  std::vector<Piece> ps;
+  for (size_t p = 0; p < passes.size(); ++p)
+    for (const Seg& s : passes[p].segs) {
+      if (s.n <= 0) continue;
+      if (seg_mixed(s)) return fail("mixed-width segments");
+      ps.push_back(Piece{s, (int)p, (int)ps.size()});
+    }
+  if (ps.empty()) return fail("nothing to run");
+
+  // 1. Refine: cut pieces until every conflicting pair of operands covers the same bytes.
+  std::vector<Operand> ops;
+  for (int round = 0;; ++round) {
+    if (round > 64 || ps.size() > (size_t)kChainMaxPieces) return fail("does not refine");
+    operands(ps, E, &ops);
+    std::vector<std::vector<int64_t>> cuts(ps.size());
+    bool bad = false;
+    for_each_conflict(ops, [&](const Operand& a, const Operand& b) {
+      if (ps[a.piece].pass == ps[b.piece].pass) bad = true;  // a race inside one pass
+      if (a.lo == b.lo && a.hi == b.hi) return;
+      const uintptr_t lo = std::max(a.lo, b.lo), hi = std::min(a.hi, b.hi);
+      for (const Operand* x : {&a, &b}) {
+        if ((lo - x->lo) % E || (hi - x->lo) % E) bad = true;
+        if (x->lo < lo) cuts[x->piece].push_back((int64_t)((lo - x->lo) / E));
+        if (x->hi > hi) cuts[x->piece].push_back((int64_t)((hi - x->lo) / E));
+      }
+    });
+    if (bad) return fail("overlap that is not elementwise");
+    bool any = false;
+    std::vector<Piece> next;
+    next.reserve(ps.size());
+    for (size_t i = 0; i < ps.size(); ++i) {
+      std::vector<int64_t>& c = cuts[i];
+      c.push_back(0);
+      c.push_back(ps[i].s.n);
+      std::sort(c.begin(), c.end());
+      c.erase(std::unique(c.begin(), c.end()), c.end());
+      any |= c.size() > 2;
+      for (size_t k = 0; k + 1 < c.size(); ++k)
+        next.push_back(Piece{advance(ps[i].s, c[k], c[k + 1] - c[k], E), ps[i].pass, 0});
+    }
+    for (size_t i = 0; i < next.size(); ++i) next[i].order = (int)i;
+    ps.swap(next);
+    if (!any) break;
+  }
+
+  // 2. Join conflicting pieces into groups.
+  std::vector<int> parent(ps.size());
+  std::iota(parent.begin(), parent.end(), 0);
+  for_each_conflict(ops, [&](const Operand& a, const Operand& b) {
+    const int ra = find(parent, a.piece), rb = find(parent, b.piece);
+    if (ra != rb) parent[std::max(ra, rb)] = std::min(ra, rb);
+  });
+  std::vector<std::vector<int>> members(ps.size());
+  for (int i = 0; i < (int)ps.size(); ++i) members[find(parent, i)].push_back(i);
+
+  // 3. Lay the groups out, each in pass order (build order within a pass).
+  out->segs.clear();
+  out->level.clear();
+  out->gfirst.clear();
+  out->gn.clear();
+  for (auto& m : members) {
+    if (m.empty()) continue;
+    std::stable_sort(m.begin(), m.end(), [&](int a, int b) { return ps[a].pass < ps[b].pass; });
+    const int64_t n = ps[m[0]].s.n;
+    out->gfirst.push_back((int32_t)out->segs.size());
+    out->gn.push_back(n);
+    for (int i : m) {
+      if (ps[i].s.n != n) return fail("a group's pieces differ in length");
+      out->segs.push_back(ps[i].s);
+      out->level.push_back((uint8_t)ps[i].pass);
+    }
+  }
+  out->gfirst.push_back((int32_t)out->segs.size());
+  return true;
+}
+
+// An independent re-check of a chained program (host hazard checks): no two pieces of
+// different groups touch the same bytes with either writing, and no two pieces of one
+// group's pass do. Quadratic in the pieces, so only run when the caller asks for checks.
+bool check_chain(const ChainPlan& c, int E, std::string* why) {
+  const int G = (int)c.gn.size();
+  std::vector<int> group(c.segs.size());
+  for (int g = 0; g < G; ++g)
+    for (int i = c.gfirst[g]; i < c.gfirst[g + 1]; ++i) {
+      group[i] = g;
+      if (c.segs[i].n != c.gn[g]) {
+        *why = "chained group " + std::to_string(g) + " has pieces of different lengths";
+        return false;
+      }
+      if (i > c.gfirst[g] && c.level[i] < c.level[i - 1]) {
+        *why = "chained group " + std::to_string(g) + " is not in pass order";
+        return false;
+      }
+    }
+  auto rng = [&](const void* p, int64_t n) {
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+    return std::make_pair(lo, lo + (uintptr_t)(n * E));
+  };
+  auto ov = [](std::pair<uintptr_t, uintptr_t> a, std::pair<uintptr_t, uintptr_t> b) {
+    return a.first < b.second && b.first < a.second;
+  };
+  for (size_t i = 0; i < c.segs.size(); ++i)
+    for (size_t j = 0; j < c.segs.size(); ++j) {
+      if (i == j) continue;
+      const bool same_group = group[i] == group[j];
+      if (same_group && c.level[i] != c.level[j]) continue;  // ordered by the block barrier
+      const Seg &a = c.segs[i], &b = c.segs[j];
+      for (int d = 0; d < a.ndst; ++d) {
+        const auto w = rng(a.dst[d], a.n);
+        bool hit = false;
+        for (int k = 0; k < b.nsrc; ++k) hit |= ov(w, rng(b.src[k], b.n));
+        for (int k = 0; k < b.ndst; ++k) hit |= ov(w, rng(b.dst[k], b.n));
+        if (hit) {
+          *why = "chained pieces " + std::to_string(i) + " and " + std::to_string(j) +
+                 (same_group ? " of one pass of a group" : " of different groups") +
+                 " touch the same bytes, one of them writing";
+          return false;
+        }
+      }
+    }
+  return true;
+}
+
+}  // namespace relay

@@ -143,6 +143,25 @@ cudaError_t launch_pass(int dtype, const Pass& pass, float scale, cudaStream_t s
 bool launch_fused(int dtype, const std::vector<Pass>& passes, float scale, cudaStream_t stream,
                   cudaError_t* err, bool forced = false);
 
+// The chained launch: a whole call in one ordinary launch whose CTAs never wait for one
+// another. The passes' segments are cut into pieces so that every dependency between
+// passes links identical element ranges, pieces that touch the same bytes (one writing)
+// form a group, and one CTA runs tile t of every piece of a group in pass order, with a
+// block barrier between passes -- chain.cpp (analysis), passes.cu (kernel).
+constexpr int kChainMaxPieces = 384;
+struct ChainPlan {
+  std::vector<Seg> segs;        // every group's pieces contiguous, in pass order
+  std::vector<uint8_t> level;   // pass of each piece
+  std::vector<int32_t> gfirst;  // first piece of each group, then one past the last
+  std::vector<int64_t> gn;      // elements of each piece of the group
+};
+bool build_chain(const std::vector<Pass>& passes, int E, ChainPlan* out, std::string* why);
+bool check_chain(const ChainPlan& c, int E, std::string* why);
+// Launches the chained kernel; false (nothing launched) when the program does not fit one
+// launch's parameters.
+bool launch_chain(int dtype, const ChainPlan& c, float scale, cudaStream_t stream,
+                  cudaError_t* err);
+
 // Record `msg` as this thread's last error and return `st` -- abi.cpp.
 relay_status_t report_error(relay_status_t st, const std::string& msg);
 

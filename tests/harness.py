@@ -115,6 +115,7 @@ def run(coll, A, R, count, dtype, scale=1.0, config=0, schedule=rv.SCHEDULE_AUTO
            opts)
     else:
         fn(send + [None] * (R - A), recv + [None] * (R - A), scratch, count, dtype, A, R, opts)
+    c.launch = rv.last_launch()
     torch.cuda.synchronize()
     return c
 

@@ -1,7 +1,8 @@
 """Every count from 0 to 4096 for the 2-active collectives on the relay schedule (the
 zero-chunk fallback below 1024, the relay geometry above), bit-exact against the oracle,
 with a poisoned band past each output that must stay untouched. Small calls run as one
-cooperative launch; every 5th count also runs pass by pass."""
+chained launch; every 5th count also runs pass by pass, every 7th as one cooperative
+launch."""
 import numpy as np
 import pytest
 import torch
@@ -38,7 +39,9 @@ def test_every_count_up_to_4096(coll, dtype, scale):
     dev = torch.device("cuda")
     opts = {0: rv.make_opts(schedule=rv.SCHEDULE_RELAY, flags=rv.FLAG_CHECK_HAZARDS),
             1: rv.make_opts(schedule=rv.SCHEDULE_RELAY,
-                            flags=rv.FLAG_CHECK_HAZARDS | rv.FLAG_SEPARATE_PASSES)}
+                            flags=rv.FLAG_CHECK_HAZARDS | rv.FLAG_SEPARATE_PASSES),
+            2: rv.make_opts(schedule=rv.SCHEDULE_RELAY,
+                            flags=rv.FLAG_CHECK_HAZARDS | rv.FLAG_FUSED_PASSES)}
     plans = [rv.relay_plan(coll, n, dtype, A, R, opts[0]) for n in range(MAXN + 1)]
     # every buffer sized for the largest need over all counts (the zero-chunk fallback
     # needs more active scratch than the relay geometry above it)
@@ -59,7 +62,7 @@ def test_every_count_up_to_4096(coll, dtype, scale):
         # input and output sizes from the request (D115998376, D115998385, D115998370)
         n_in = A * n if coll in (rv.REDUCE_SCATTER, rv.ALL_TO_ALL) else n
         n_out = A * n if coll in (rv.ALL_GATHER, rv.ALL_TO_ALL) else n
-        for policy in ((0, 1) if n % 5 == 0 else (0,)):
+        for policy in (0,) + ((1,) if n % 5 == 0 else ()) + ((2,) if n % 7 == 0 else ()):
             for y in recv:
                 y.view(torch.uint8).fill_(0xA5)
             args = ([s[:n_in] for s in send] + [None] * (R - A),
@@ -79,4 +82,4 @@ def test_every_count_up_to_4096(coll, dtype, scale):
                 tail = _bits(recv[a][n_out:n_out + BAND]).view(np.uint8)
                 assert np.all(tail == 0xA5), f"count {n}: bytes past the output were written"
             checked += 1
-    assert checked == (MAXN + 1) + (MAXN // 5 + 1)
+    assert checked == (MAXN + 1) + (MAXN // 5 + 1) + (MAXN // 7 + 1)

@@ -33,11 +33,12 @@ def _scale(coll, A, dtype):
 @pytest.mark.parametrize("dtype", [rv.F32, rv.BF16, rv.I32])
 @pytest.mark.parametrize("A", [2, 4])
 @pytest.mark.parametrize("coll", [rv.ALLREDUCE, rv.REDUCE_SCATTER, rv.ALL_GATHER, rv.ALL_TO_ALL])
-@pytest.mark.parametrize("launch", [0, rv.FLAG_SEPARATE_PASSES])
+@pytest.mark.parametrize("launch", [0, rv.FLAG_SEPARATE_PASSES, rv.FLAG_FUSED_PASSES])
 def test_small_sizes_every_schedule(coll, A, dtype, launch):
     """Every count around the 128-element alignment and chunk boundaries, every
     schedule, R = A+1 (one helper) and R = 8, in-place and out-of-place; small calls run
-    as one cooperative launch by default and pass by pass when asked."""
+    as one chained launch by default, pass by pass or as one cooperative launch when
+    asked."""
     n = 0
     for R in (A + 1, 8):
         for count in SMALL_COUNTS:
@@ -62,7 +63,7 @@ def test_small_sizes_every_schedule(coll, A, dtype, launch):
 @pytest.mark.parametrize("coll", [rv.ALLREDUCE, rv.REDUCE_SCATTER, rv.ALL_GATHER, rv.ALL_TO_ALL])
 @pytest.mark.parametrize("dtype", [rv.F32, rv.BF16])
 @pytest.mark.parametrize("shift", [1, 3])
-@pytest.mark.parametrize("launch", [0, rv.FLAG_SEPARATE_PASSES])
+@pytest.mark.parametrize("launch", [0, rv.FLAG_SEPARATE_PASSES, rv.FLAG_FUSED_PASSES])
 def test_unaligned_buffers(coll, dtype, shift, launch):
     """Buffers that are element- but not 16-byte-aligned: all sharing one offset
     (vector path after a peeled prologue) and with mixed offsets (per-element path), in the
@@ -265,15 +266,62 @@ def test_pass_events_inside_a_cuda_graph():
 
 
 @pytest.mark.parametrize("coll", [rv.ALLREDUCE, rv.REDUCE_SCATTER, rv.ALL_GATHER, rv.ALL_TO_ALL])
-def test_fused_launch_at_sizes_past_its_default(coll):
-    """The one-launch path forced on calls of many tiles per pass (grid barriers between
-    passes; loads through L2) matches the oracle like the per-pass path."""
+@pytest.mark.parametrize("form", [rv.FLAG_FUSED_PASSES, rv.FLAG_CHAINED])
+def test_one_launch_at_sizes_past_its_default(coll, form):
+    """The one-launch forms forced on calls of many tiles per pass (cooperative: grid
+    barriers between passes; chained: every dependency inside one CTA; both load
+    through L2 what the launch wrote) match the oracle like the per-pass path."""
     for A in (2, 4):
         for count in (3 << 20, (1 << 21) + 129):
             scale = _scale(coll, A, rv.BF16)
-            c = hz.run(coll, A, 8, count, rv.BF16, scale, config=17,
-                       schedule=rv.SCHEDULE_RELAY, flags=rv.FLAG_FUSED_PASSES)
-            hz.check_all(c)
+            for in_place in (False, True):
+                if in_place and coll == rv.ALL_TO_ALL:
+                    continue
+                c = hz.run(coll, A, 8, count, rv.BF16, scale, config=17, in_place=in_place,
+                           schedule=rv.SCHEDULE_RELAY, flags=form | rv.FLAG_PAYLOAD_PARTIAL)
+                want = "chained" if form == rv.FLAG_CHAINED else "cooperative"
+                assert c.launch.startswith(want), c.launch
+                hz.check_all(c)
+
+
+def test_default_launch_forms():
+    """Small calls run chained by default; pass events, RELAY_FLAG_SEPARATE_PASSES and
+    mixed-width programs (a bf16 4-active reduce-scatter's fp32 partial) run pass by
+    pass; RELAY_FLAG_FUSED_PASSES runs the cooperative launch; large calls run pass by
+    pass."""
+    c = hz.run(rv.ALLREDUCE, 2, 8, 65536, rv.F32, 0.5, config=1, schedule=rv.SCHEDULE_RELAY)
+    assert c.launch == "chained: 10 groups, 26 pieces"
+    hz.check_all(c)
+    c = hz.run(rv.ALLREDUCE, 2, 8, 65536, rv.F32, 0.5, config=1, schedule=rv.SCHEDULE_RELAY,
+               in_place=True)
+    assert c.launch == "chained: 8 groups, 26 pieces"
+    hz.check_all(c)
+    c = hz.run(rv.ALLREDUCE, 2, 8, 65536, rv.F32, 0.5, schedule=rv.SCHEDULE_RELAY,
+               flags=rv.FLAG_SEPARATE_PASSES)
+    assert c.launch == "passes"
+    c = hz.run(rv.ALLREDUCE, 2, 8, 65536, rv.F32, 0.5, schedule=rv.SCHEDULE_RELAY,
+               flags=rv.FLAG_FUSED_PASSES)
+    assert c.launch == "cooperative"
+    c = hz.run(rv.REDUCE_SCATTER, 4, 8, 40_000, rv.BF16, 0.25, schedule=rv.SCHEDULE_RELAY)
+    assert c.wide and c.launch == "passes"
+    hz.check_all(c)
+    c = hz.run(rv.ALLREDUCE, 4, 8, 1 << 27, rv.BF16, 0.25)      # 1.9 GiB of pass traffic
+    assert c.launch == "passes"
+
+
+@pytest.mark.parametrize("case", ["ar2", "a2a_odd"])
+def test_chained_at_scale_full(case):
+    """The chained launch forced on calls of 64-128 MiB per rank, every output element
+    compared with the oracle: many tiles per group, L2 holding what each CTA just wrote."""
+    if case == "ar2":
+        c = hz.run(rv.ALLREDUCE, 2, 8, (1 << 26) + 3, rv.BF16, 0.5, config=2,
+                   flags=rv.FLAG_CHAINED, gpu_generator=True)
+    else:
+        c = hz.run(rv.ALL_TO_ALL, 4, 8, (1 << 24) // 3, rv.I32, config=5,
+                   schedule=rv.SCHEDULE_RELAY, flags=rv.FLAG_CHAINED, gpu_generator=True)
+    assert c.launch.startswith("chained")
+    assert case == "ar2" or c.count % 2 == 1
+    hz.check_full(c)
 
 
 def test_reduce_scatter_partial_precision():
