@@ -82,19 +82,20 @@ typedef enum {
 #define RELAY_FLAG_FUSED_PASSES 8  /* one cooperative launch for the whole call whenever it
                                       qualifies, whatever its size */
 #define RELAY_FLAG_CHAINED 32      /* one chained launch for the whole call whenever its
-                                      program allows it, whatever its size */
+                                      program allows it, whatever its size and depth */
 /* Launch policy. A call that records pass events, or sets RELAY_FLAG_SEPARATE_PASSES,
- * launches each pass separately. Any other call of at most RELAY_FUSED_MAX_BYTES of pass
- * traffic runs as ONE launch:
- *   - chained, where its program allows: the segments of all passes are cut into pieces
- *     so that each dependency between passes links identical element ranges; pieces that
- *     touch the same bytes, one of them writing, form a group; one CTA runs tile t of
- *     every piece of a group in pass order with a block barrier between passes. No CTA
- *     waits for another. It takes programs without mixed-width (fp32 partial) segments
- *     whose pieces number at most 384 after cutting;
- *   - else cooperative: at most 4 passes and 384 segments after alignment splitting, no
- *     mixed-width segments; passes separated by grid-wide barriers;
- *   - else pass by pass.
+ * launches each pass separately. Any other call runs as ONE chained launch where its
+ * program allows: the segments of all passes are cut into pieces so that each dependency
+ * between passes links identical element ranges; pieces that touch the same bytes, one of
+ * them writing, form a group; one CTA runs tile t of every piece of a group in pass order
+ * with a block barrier between passes. No CTA waits for another, and a consumer reads
+ * from L2 what its own CTA just wrote. It takes programs without mixed-width (fp32
+ * partial) segments whose pieces number at most 384 after cutting; past
+ * RELAY_FUSED_MAX_BYTES of pass traffic, only those whose groups span at most two passes
+ * (the coalesced 4-active all-to-all's three-pass chains run faster pass by pass). Else a
+ * call of at most RELAY_FUSED_MAX_BYTES runs as one cooperative launch (at most 4 passes
+ * and 384 segments after alignment splitting, no mixed-width segments; passes separated
+ * by grid-wide barriers), and anything else pass by pass.
  * relay_last_launch() names the form the calling thread's last call took. */
 #define RELAY_FUSED_MAX_BYTES (256ll << 20)
 #define RELAY_FLAG_PAYLOAD_PARTIAL 16 /* 4-active reduce-scatter, bf16 payload. By default
@@ -356,6 +357,28 @@ relay_status_t relay_copy(void* dst, const void* src, size_t count, relay_dtype_
 relay_status_t relay_allreduce_noalloc(void* const* send, void* const* recv, size_t count,
                                        relay_dtype_t dtype, int A, int R, float scale,
                                        const relay_opts_t* opts, cudaStream_t stream);
+
+/*
+ * relay_device_status -- reads and clears the device's fault word. Passes whose sources
+ * sit off the 16-byte grid stage each tile's source bytes in shared memory with a bulk
+ * copy and wait for it on an mbarrier (the schedule's strided pack/unpack, item 7). That
+ * wait is bounded (200 ms of the global timer); if it ever runs out, the kernel records a
+ * fault, leaves that tile unwritten and returns instead of hanging. Call this after
+ * synchronizing the streams that ran collectives: RELAY_ERR_CUDA if a wait gave up since
+ * the last call (or a CUDA call failed), RELAY_OK otherwise. Synchronous.
+ */
+relay_status_t relay_device_status(void);
+
+/*
+ * relay_test_staged_wait -- a test of that bounded wait: one staged copy of `count`
+ * elements (at most one 16 KiB tile) from `src` to `dst` (device memory, dst 16-byte
+ * aligned) whose barrier expects `extra_bytes` more than its copy brings. With
+ * extra_bytes > 0 the wait runs out, the copy's destination is left unwritten, and the
+ * next relay_device_status() reports RELAY_ERR_CUDA; the context stays usable. With 0 it
+ * is an ordinary copy. The page has no counterpart.
+ */
+relay_status_t relay_test_staged_wait(void* dst, const void* src, size_t count,
+                                      relay_dtype_t dtype, int extra_bytes, cudaStream_t stream);
 
 /* Human-readable text of the last error this thread's calls produced. */
 const char* relay_last_error(void);

@@ -122,6 +122,10 @@ def lib():
     L.relay_unpack_flat.restype = i32
     L.relay_copy.argtypes = [vp, vp, sz, i32, i32, vp]
     L.relay_copy.restype = i32
+    L.relay_device_status.argtypes = []
+    L.relay_device_status.restype = i32
+    L.relay_test_staged_wait.argtypes = [vp, vp, sz, i32, i32, vp]
+    L.relay_test_staged_wait.restype = i32
     if L.relay_abi_version() != 1:
         raise RuntimeError("librelay.so ABI version mismatch")
     _lib = L
@@ -131,6 +135,12 @@ def lib():
 def _check(status: int):
     if status != OK:
         raise RelayError(status, lib().relay_last_error().decode(errors="replace"))
+
+
+def device_status() -> None:
+    """Raise if a bounded wait in a relay kernel gave up since the last check (reads and
+    clears the device's fault word; synchronous)."""
+    _check(lib().relay_device_status())
 
 
 def last_launch() -> str:

@@ -203,12 +203,14 @@ relay_status_t execute(const std::vector<Pass>& passes, const std::vector<Range>
       bytes += seg_dst_bytes(sg, E) * sg.ndst;
     }
   const bool small = bytes <= RELAY_FUSED_MAX_BYTES;
-  const bool try_chain = one_launch && passes.size() > 1 && !(flags & RELAY_FLAG_FUSED_PASSES) &&
-                         ((flags & RELAY_FLAG_CHAINED) || small);
+  const bool try_chain = one_launch && passes.size() > 1 && !(flags & RELAY_FLAG_FUSED_PASSES);
   ChainPlan chain;
   bool chained = false;
   if (try_chain) {
     chained = build_chain(passes, E, &chain, &why);
+    // past the small-call size, only chains of at most kChainLargeMaxDepth passes
+    if (chained && !small && !(flags & RELAY_FLAG_CHAINED) && chain.depth > kChainLargeMaxDepth)
+      chained = false;
     if (chained && (flags & RELAY_FLAG_CHECK_HAZARDS) && !check_chain(chain, E, &why))
       return fail(RELAY_ERR_UNSUPPORTED, "internal (chained launch): " + why);
   }
@@ -621,7 +623,33 @@ relay_status_t relay_copy(void* dst, const void* src, size_t count, relay_dtype_
   sg.nsrc = sg.ndst = 1;
   ps.segs.push_back(sg);
   ps.meta.push_back(SegMeta{-1, 0, {0, -1, -1, -1}});
-  const cudaError_t e = launch_pass(dtype, ps, 1.0f, stream, max_ctas);
+  // either side may be host memory: keep to the register path (no bulk copies)
+  const cudaError_t e = launch_pass(dtype, ps, 1.0f, stream, max_ctas, false);
+  if (e != cudaSuccess) return fail(RELAY_ERR_CUDA, cudaGetErrorString(e));
+  return RELAY_OK;
+}
+
+relay_status_t relay_device_status(void) {
+  unsigned fault = 0;
+  const cudaError_t e = read_device_fault(&fault);
+  if (e != cudaSuccess) return fail(RELAY_ERR_CUDA, cudaGetErrorString(e));
+  if (fault)
+    return fail(RELAY_ERR_CUDA,
+                "a bounded wait in a relay kernel gave up (a bulk copy into shared memory did "
+                "not land in time); the affected tiles were not written");
+  return RELAY_OK;
+}
+
+relay_status_t relay_test_staged_wait(void* dst, const void* src, size_t count,
+                                      relay_dtype_t dtype, int extra_bytes, cudaStream_t stream) {
+  if (dtype < RELAY_F32 || dtype > RELAY_I32) return fail(RELAY_ERR_INVALID_ARGUMENT, "unknown dtype");
+  if (dst == nullptr || src == nullptr || count == 0 || count > (size_t)(tile_elems(esize_of(dtype))) ||
+      extra_bytes < 0 || extra_bytes > (1 << 20))
+    return fail(RELAY_ERR_INVALID_ARGUMENT, "one tile of device memory, 0 <= extra_bytes <= 1 MiB");
+  const int E = esize_of(dtype);
+  if ((reinterpret_cast<uintptr_t>(dst) & 15u) || reinterpret_cast<uintptr_t>(src) % E)
+    return fail(RELAY_ERR_INVALID_ARGUMENT, "dst must be 16-byte aligned, src element-aligned");
+  const cudaError_t e = launch_staged_wait_test(dst, src, (int64_t)count, dtype, extra_bytes, stream);
   if (e != cudaSuccess) return fail(RELAY_ERR_CUDA, cudaGetErrorString(e));
   return RELAY_OK;
 }

@@ -17,6 +17,7 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <type_traits>
 
 #include "program.h"
 
@@ -28,7 +29,8 @@ struct PassArgs {
   int32_t nseg;
   int32_t ntiles;
   float scale;
-  int32_t pad;
+  int32_t extra_tx;  // staged kernel: bytes its barrier expects beyond the copies (0; a test
+                     // sets it to make a wait run out)
   Seg seg[CAP];
 };
 
@@ -688,7 +690,8 @@ __device__ __noinline__ void run_mixed_tile(const Seg& s, int64_t base, int64_t 
 // the realigning path with a zero shift. It runs 3 CTAs per SM (4 spilled) and is used only
 // for passes of at most kRealignAllBytes: on GB300 the one launch ran a 54 MiB-per-rank
 // misaligned all-to-all 14% faster than two, but 1 GiB ones 7% slower.
-constexpr int kModeMain = 0, kModeRealign = 1, kModeMixed = 2, kModeRealignAll = 3;
+constexpr int kModeMain = 0, kModeRealign = 1, kModeMixed = 2, kModeRealignAll = 3,
+              kModeStaged = 4;
 constexpr int64_t kRealignAllBytes = 256ll << 20;
 
 template <class P, int CAP, int MODE>
@@ -721,6 +724,200 @@ __global__ void __launch_bounds__(kThreads, MODE == kModeRealignAll ? 3 : MODE =
     else if (MODE == kModeRealignAll && (s.flags & kFlagRealign))
       run_realign_tail<P>(s, base, len, args.scale);
     else run_partial_tile<P, false>(s, base, len, args.scale);
+  }
+}
+
+// ------------------------------------------------- TMA-staged realignment kernel --
+// A pass whose sources sit off the 16-byte grid (an all-to-all with an odd segmentCount, an
+// odd recvCount) in one launch: per 16 KiB tile of destination, one thread bulk-copies the
+// 16-byte blocks that hold the tile's source bytes into shared memory (cp.async.bulk, an
+// mbarrier counting the bytes), and the CTA then funnel-shifts each vector out of two
+// adjacent shared blocks and stores it 16-byte aligned. Copies and two-source reductions
+// whose pointers are already aligned take the same path with a zero shift, so the whole
+// pass is one launch. Data in flight sits in shared memory rather than registers, so the
+// kernel runs 6 CTAs per SM where the register-realigning one ran 3-4.
+
+// A tile's source bytes plus the block they spill into, per source.
+constexpr uint32_t kStageBytes = (uint32_t)kTileBytes + 16;
+// Bound of one mbarrier wait, in nanoseconds of the global timer. A bulk copy of 16 KiB
+// lands in microseconds; a wait that runs out records a fault and gives up.
+constexpr uint64_t kStageWaitNs = 200ull * 1000 * 1000;
+
+// Set (bit 0) when a bounded wait of the staged kernel gave up; read and cleared on the
+// host by relay_device_status().
+__device__ unsigned g_relay_fault;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, unsigned parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for phase `parity` of the barrier, for at most `limit_ns`. False when it gave up.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, unsigned parity, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_ns() - t0 > limit_ns) return false;
+  return true;
+}
+
+__device__ __forceinline__ uint4 lds_v4(uint32_t a) {
+  uint4 r;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "r"(a));
+  return r;
+}
+
+// The 16 bytes at shared byte offset sig + 16 v of a staged source.
+__device__ __forceinline__ uint4 staged_vec(uint32_t base, unsigned sig, int v) {
+  const uint4 lo = lds_v4(base + 16u * (uint32_t)v);
+  return sig == 0 ? lo : shift_pair(lo, lds_v4(base + 16u * (uint32_t)(v + 1)), sig);
+}
+
+// One element of a staged source, widened like P::load1.
+template <class P>
+__device__ __forceinline__ typename P::Acc staged_elem(uint32_t a) {
+  uint32_t w;
+  if (P::kE == 4) {
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w) : "r"(a));
+  } else {
+    uint16_t h;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h) : "r"(a));
+    w = (uint32_t)h << 16;
+  }
+  if constexpr (std::is_same<typename P::Acc, float>::value) return __uint_as_float(w);
+  else return (typename P::Acc)w;
+}
+
+template <class P, int CAP>
+__global__ void __launch_bounds__(kThreads, 6) relay_staged_kernel(const __grid_constant__ PassArgs<CAP> args) {
+  extern __shared__ __align__(16) unsigned char stage[];
+  using Acc = typename P::Acc;
+  constexpr int L = P::kLanes;
+  constexpr int64_t kTile = kTileBytes / P::kE;
+  // dynamic shared memory: one slot of kStageBytes per source (a launch of copies holds
+  // one, of two-source reductions two); the barrier counting the copied bytes is static
+  __shared__ __align__(8) uint64_t bar_word;
+  const uint32_t bar = smem_u32(&bar_word);
+  const uint32_t s0 = smem_u32(stage);
+  if (threadIdx.x == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  __syncthreads();
+  unsigned phase = 0;
+  for (int t = blockIdx.x; t < args.ntiles; t += gridDim.x, phase ^= 1u) {
+    int lo = 0, hi = args.nseg - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (args.seg[mid].tile0 <= t) lo = mid; else hi = mid - 1;
+    }
+    const Seg& s = args.seg[lo];
+    const int64_t base = (int64_t)(t - s.tile0) * kTile;
+    const int len = (int)min(kTile, s.n - base);
+    const int nsrc = s.op == kOpCopy ? 1 : s.nsrc;
+    unsigned sig[2] = {0u, 0u};
+    uintptr_t a0[2] = {0, 0};
+    uint32_t bytes[2] = {0u, 0u};
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      if (k >= nsrc) break;
+      // the 16-byte blocks holding the tile's source bytes
+      const uintptr_t p = reinterpret_cast<uintptr_t>(s.src[k]) + (uintptr_t)(base * P::kE);
+      sig[k] = (unsigned)(p & 15u);
+      a0[k] = p & ~(uintptr_t)15;
+      bytes[k] = (uint32_t)(((p + (uintptr_t)len * P::kE + 15) & ~(uintptr_t)15) - a0[k]);
+    }
+    if (threadIdx.x == 0) {
+      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+                   "r"(bytes[0] + bytes[1] + (uint32_t)args.extra_tx)
+                   : "memory");
+#pragma unroll
+      for (int k = 0; k < 2; ++k)
+        if (k < nsrc)
+          asm volatile(
+              "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+                  "r"(s0 + (uint32_t)k * kStageBytes), "l"(a0[k]), "r"(bytes[k]), "r"(bar)
+              : "memory");
+    }
+    const bool landed = mbar_wait_bounded(bar, phase, kStageWaitNs);
+    if (__syncthreads_or(!landed)) {
+      // a copy did not land in time: record it, give the copies one more bounded wait so
+      // that nothing is still writing this CTA's shared memory, and leave (every thread)
+      if (threadIdx.x == 0) atomicOr(&g_relay_fault, 1u);
+      mbar_wait_bounded(bar, phase, kStageWaitNs);
+      return;
+    }
+    const int nvec = len / L;
+    const bool do_scale = (s.flags & kFlagScale) != 0;
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int v = (int)threadIdx.x + u * kThreads;
+      if (v >= nvec) break;
+      uint4 r = staged_vec(s0, sig[0], v);
+      if (s.op != kOpCopy) {
+        Acc acc[L], t2[L];
+        P::unpack(r, acc);
+        if (nsrc == 2) {
+          P::unpack(staged_vec(s0 + kStageBytes, sig[1], v), t2);
+#pragma unroll
+          for (int i = 0; i < L; ++i) acc[i] = P::add(acc[i], t2[i]);
+        }
+        if (do_scale) {
+#pragma unroll
+          for (int i = 0; i < L; ++i) acc[i] = P::scale(acc[i], args.scale);
+        }
+        r = P::pack(acc);
+      }
+#pragma unroll 1
+      for (int d = 0; d < s.ndst; ++d)
+        st_v4(reinterpret_cast<uint4*>(static_cast<char*>(s.dst[d]) + base * P::kE) + v, r);
+    }
+    // the last < L elements of a segment's final tile, one at a time from shared memory
+    for (int e = nvec * L + (int)threadIdx.x; e < len; e += kThreads) {
+      const uint32_t o0 = s0 + sig[0] + (uint32_t)(e * P::kE);
+      if (s.op == kOpCopy) {
+        if (P::kE == 4) {
+          uint32_t x;
+          asm volatile("ld.shared.u32 %0, [%1];" : "=r"(x) : "r"(o0));
+#pragma unroll 1
+          for (int d = 0; d < s.ndst; ++d) st_u32(static_cast<char*>(s.dst[d]) + (base + e) * P::kE, x);
+        } else {
+          uint16_t x;
+          asm volatile("ld.shared.u16 %0, [%1];" : "=h"(x) : "r"(o0));
+#pragma unroll 1
+          for (int d = 0; d < s.ndst; ++d) st_u16(static_cast<char*>(s.dst[d]) + (base + e) * P::kE, x);
+        }
+        continue;
+      }
+      Acc acc = staged_elem<P>(o0);
+      if (nsrc == 2)
+        acc = P::add(acc, staged_elem<P>(s0 + kStageBytes + sig[1] + (uint32_t)(e * P::kE)));
+      if (do_scale) acc = P::scale(acc, args.scale);
+#pragma unroll 1
+      for (int d = 0; d < s.ndst; ++d) P::store1(static_cast<char*>(s.dst[d]) + (base + e) * P::kE, acc);
+    }
+    // every thread is done with this tile's shared bytes before the next copy lands there
+    __syncthreads();
   }
 }
 
@@ -979,7 +1176,7 @@ __device__ __noinline__ void run_piece(const Seg& s, int64_t base, int64_t len, 
 }
 
 template <class P, int CAP>
-__global__ void __launch_bounds__(kThreads, 4) relay_chain_kernel(const __grid_constant__ ChainArgs<CAP> a) {
+__global__ void __launch_bounds__(kThreads, 5) relay_chain_kernel(const __grid_constant__ ChainArgs<CAP> a) {
   const int t = blockIdx.x;
   // the last group whose first task is <= t (uniform across the CTA)
   int lo = 0, hi = a.ngroup - 1;
@@ -1057,27 +1254,34 @@ int sm_count() {
 
 template <class P, int CAP, int MODE>
 cudaError_t launch_cap(const Seg* segs, int nseg, float scale, cudaStream_t stream,
-                       int max_ctas) {
+                       int max_ctas, int extra_tx = 0) {
   static thread_local PassArgs<CAP> a;  // up to ~30 KiB: keep it off the stack
   constexpr int64_t kTile = kTileBytes / P::kE;
   int64_t tiles = 0;
+  int max_src = 1;
   for (int i = 0; i < nseg; ++i) {
     a.seg[i] = segs[i];
     a.seg[i].tile0 = (int32_t)tiles;
     tiles += (segs[i].n + kTile - 1) / kTile;
+    if (segs[i].op != kOpCopy) max_src = std::max<int>(max_src, segs[i].nsrc);
   }
   if (tiles > INT32_MAX) return cudaErrorInvalidValue;
   a.nseg = nseg;
   a.ntiles = (int32_t)tiles;
   a.scale = scale;
-  a.pad = 0;
+  a.extra_tx = extra_tx;
   // one CTA per tile: the block scheduler starts a new tile on an SM the moment one of
   // its 5 resident CTAs finishes, which on GB300 streams ~11% faster than a persistent
   // grid walking the tiles (that grid's CTAs load, then store, tile after tile in step).
   // A capped grid (copies over the host link) walks the tiles instead.
   const int64_t want = max_ctas > 0 ? std::min<int64_t>(tiles, max_ctas) : tiles;
   const int grid = (int)std::max<int64_t>(1, want);
-  relay_pass_kernel<P, CAP, MODE><<<grid, kThreads, 0, stream>>>(a);
+  if constexpr (MODE == kModeStaged) {
+    if (max_src > 2) return cudaErrorInvalidValue;  // the staged kernel holds two sources
+    relay_staged_kernel<P, CAP><<<grid, kThreads, (size_t)max_src * kStageBytes, stream>>>(a);
+  } else {
+    relay_pass_kernel<P, CAP, MODE><<<grid, kThreads, 0, stream>>>(a);
+  }
   return cudaGetLastError();
 }
 
@@ -1274,8 +1478,27 @@ namespace {
 template <class P>
 cudaError_t launch_split(const std::vector<Seg>& direct, const std::vector<Seg>& realigned,
                          const std::vector<Seg>& mixed, float scale, cudaStream_t stream,
-                         int max_ctas) {
+                         int max_ctas, bool staged) {
   cudaError_t e = cudaSuccess;
+  if (!realigned.empty() && staged) {
+    // the TMA-staged kernel takes the realigned segments and, for a pass of at most
+    // kRealignAllBytes, also its aligned copies and one- or two-source reductions (with a
+    // zero shift), so that such a pass is one launch; the rest stay on the main kernel
+    int64_t bytes = 0;
+    for (const Seg& sg : direct) bytes += sg.n * P::kE * (sg.nsrc + sg.ndst);
+    for (const Seg& sg : realigned) bytes += sg.n * P::kE * (sg.nsrc + sg.ndst);
+    static thread_local std::vector<Seg> st, rest;
+    st.assign(realigned.begin(), realigned.end());
+    rest.clear();
+    for (const Seg& sg : direct) {
+      const bool fits = (sg.flags & kFlagVector) && (sg.op == kOpCopy || sg.nsrc <= 2);
+      (fits && bytes <= kRealignAllBytes ? st : rest).push_back(sg);
+    }
+    if (!rest.empty()) e = launch_typed<P, kModeMain>(rest, scale, stream, max_ctas);
+    if (e == cudaSuccess) e = launch_typed<P, kModeStaged>(st, scale, stream, max_ctas);
+    if (e == cudaSuccess && !mixed.empty()) e = launch_typed<P, kModeMixed>(mixed, scale, stream, max_ctas);
+    return e;
+  }
   if (!realigned.empty() && !direct.empty()) {
     bool copies_only = true;
     int64_t bytes = 0;
@@ -1308,7 +1531,7 @@ cudaError_t launch_split(const std::vector<Seg>& direct, const std::vector<Seg>&
 // after the others; the launches of one pass touch disjoint memory, so their order does
 // not matter.
 cudaError_t launch_pass(int dtype, const Pass& pass, float scale, cudaStream_t stream,
-                        int max_ctas) {
+                        int max_ctas, bool staged) {
   static thread_local std::vector<Seg> plain, segs, direct, realigned, mixed;
   plain.clear();
   mixed.clear();
@@ -1337,10 +1560,33 @@ cudaError_t launch_pass(int dtype, const Pass& pass, float scale, cudaStream_t s
     direct.clear();
   }
   switch (dtype) {
-    case RELAY_F32: return launch_split<TF32>(direct, realigned, mixed, scale, stream, max_ctas);
-    case RELAY_BF16: return launch_split<TBF16>(direct, realigned, mixed, scale, stream, max_ctas);
-    default: return launch_split<TI32>(direct, realigned, mixed, scale, stream, max_ctas);
+    case RELAY_F32: return launch_split<TF32>(direct, realigned, mixed, scale, stream, max_ctas, staged);
+    case RELAY_BF16: return launch_split<TBF16>(direct, realigned, mixed, scale, stream, max_ctas, staged);
+    default: return launch_split<TI32>(direct, realigned, mixed, scale, stream, max_ctas, staged);
   }
+}
+
+cudaError_t launch_staged_wait_test(void* dst, const void* src, int64_t count, int dtype,
+                                    int extra_bytes, cudaStream_t stream) {
+  Seg sg{};
+  sg.src[0] = src;
+  sg.dst[0] = dst;
+  sg.n = count;
+  sg.op = kOpCopy;
+  sg.nsrc = sg.ndst = 1;
+  switch (dtype) {
+    case RELAY_F32: return launch_cap<TF32, 8, kModeStaged>(&sg, 1, 1.0f, stream, 0, extra_bytes);
+    case RELAY_BF16: return launch_cap<TBF16, 8, kModeStaged>(&sg, 1, 1.0f, stream, 0, extra_bytes);
+    default: return launch_cap<TI32, 8, kModeStaged>(&sg, 1, 1.0f, stream, 0, extra_bytes);
+  }
+}
+
+cudaError_t read_device_fault(unsigned* fault) {
+  // reads and clears the word (synchronous copies on the default stream)
+  cudaError_t e = cudaMemcpyFromSymbol(fault, g_relay_fault, sizeof *fault);
+  if (e != cudaSuccess || *fault == 0) return e;
+  const unsigned zero = 0;
+  return cudaMemcpyToSymbol(g_relay_fault, &zero, sizeof zero);
 }
 
 }  // namespace relay

@@ -132,8 +132,18 @@ void build_multi_program(const std::vector<relay_plan_t>& plans, const std::vect
 // Launch one pass on `stream` -- passes.cu. Splits into several launches when the
 // segment table exceeds one launch's parameter capacity.
 // max_ctas > 0 caps each launch's grid (its CTAs then walk the tiles); 0 is one CTA per tile.
+// staged: realigned segments may take the TMA-staged kernel (bulk copies into shared
+// memory); false keeps them on the register path (buffers that may be host memory).
 cudaError_t launch_pass(int dtype, const Pass& pass, float scale, cudaStream_t stream,
-                        int max_ctas = 0);
+                        int max_ctas = 0, bool staged = true);
+
+// One TMA-staged copy of `count` elements whose barrier expects `extra_bytes` more than
+// its copies bring, so that every wait runs out (a test of the bounded wait) -- passes.cu.
+cudaError_t launch_staged_wait_test(void* dst, const void* src, int64_t count, int dtype,
+                                    int extra_bytes, cudaStream_t stream);
+// Read and clear the device's fault word (bit 0: a bounded wait in a kernel gave up) --
+// passes.cu. Synchronous.
+cudaError_t read_device_fault(unsigned* fault);
 
 // Launch every pass of a small call as one cooperative kernel with grid barriers between
 // the passes -- passes.cu. Returns false (and launches nothing) when the call does not
@@ -154,7 +164,13 @@ struct ChainPlan {
   std::vector<uint8_t> level;   // pass of each piece
   std::vector<int32_t> gfirst;  // first piece of each group, then one past the last
   std::vector<int64_t> gn;      // elements of each piece of the group
+  int depth = 0;                // most passes any group spans (block barriers + 1)
 };
+// Calls of more pass traffic than RELAY_FUSED_MAX_BYTES run chained by default when no
+// group spans more than this many passes: on GB300 a 2-pass chain (producer and consumer
+// in one CTA, the consumer's reads served from L2) beat the per-pass launches by 4-27% at
+// 64 MiB-1 GiB per rank, while the 3-pass all-to-all chains lost up to 20%.
+constexpr int kChainLargeMaxDepth = 2;
 bool build_chain(const std::vector<Pass>& passes, int E, ChainPlan* out, std::string* why);
 bool check_chain(const ChainPlan& c, int E, std::string* why);
 // Launches the chained kernel; false (nothing launched) when the program does not fit one

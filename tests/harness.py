@@ -117,6 +117,7 @@ def run(coll, A, R, count, dtype, scale=1.0, config=0, schedule=rv.SCHEDULE_AUTO
         fn(send + [None] * (R - A), recv + [None] * (R - A), scratch, count, dtype, A, R, opts)
     c.launch = rv.last_launch()
     torch.cuda.synchronize()
+    rv.device_status()          # no bounded wait in any kernel gave up
     return c
 
 

@@ -287,8 +287,8 @@ def test_one_launch_at_sizes_past_its_default(coll, form):
 def test_default_launch_forms():
     """Small calls run chained by default; pass events, RELAY_FLAG_SEPARATE_PASSES and
     mixed-width programs (a bf16 4-active reduce-scatter's fp32 partial) run pass by
-    pass; RELAY_FLAG_FUSED_PASSES runs the cooperative launch; large calls run pass by
-    pass."""
+    pass; RELAY_FLAG_FUSED_PASSES runs the cooperative launch; large calls run chained
+    when no group spans more than two passes, else pass by pass."""
     c = hz.run(rv.ALLREDUCE, 2, 8, 65536, rv.F32, 0.5, config=1, schedule=rv.SCHEDULE_RELAY)
     assert c.launch == "chained: 10 groups, 26 pieces"
     hz.check_all(c)
@@ -306,6 +306,9 @@ def test_default_launch_forms():
     assert c.wide and c.launch == "passes"
     hz.check_all(c)
     c = hz.run(rv.ALLREDUCE, 4, 8, 1 << 27, rv.BF16, 0.25)      # 1.9 GiB of pass traffic
+    assert c.launch.startswith("chained")
+    c = hz.run(rv.ALL_TO_ALL, 4, 8, (1 << 29) // 12, rv.BF16, schedule=rv.SCHEDULE_RELAY,
+               gpu_generator=True)                              # 3-pass chains, 1.5 GB
     assert c.launch == "passes"
 
 
