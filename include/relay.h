@@ -91,8 +91,9 @@ typedef enum {
  * with a block barrier between passes. No CTA waits for another, and a consumer reads
  * from L2 what its own CTA just wrote. It takes programs without mixed-width (fp32
  * partial) segments whose pieces number at most 384 after cutting; past
- * RELAY_FUSED_MAX_BYTES of pass traffic, only those whose groups span at most two passes
- * (the coalesced 4-active all-to-all's three-pass chains run faster pass by pass). Else a
+ * RELAY_FUSED_MAX_BYTES of pass traffic, every such program but the coalesced 4-active
+ * all-to-all (its pack, forward and unpack chains of single copies run faster pass by
+ * pass; the others gain 4-25% from reading their producers' output from L2). Else a
  * call of at most RELAY_FUSED_MAX_BYTES runs as one cooperative launch (at most 4 passes
  * and 384 segments after alignment splitting, no mixed-width segments; passes separated
  * by grid-wide barriers), and anything else pass by pass.

@@ -208,9 +208,11 @@ relay_status_t execute(const std::vector<Pass>& passes, const std::vector<Range>
   bool chained = false;
   if (try_chain) {
     chained = build_chain(passes, E, &chain, &why);
-    // past the small-call size, only chains of at most kChainLargeMaxDepth passes
-    if (chained && !small && !(flags & RELAY_FLAG_CHAINED) && chain.depth > kChainLargeMaxDepth)
-      chained = false;
+    // past the small-call size, not the coalesced all-to-all (its pack, forward and
+    // unpack chains of single copies ran faster pass by pass)
+    bool unpack = false;
+    for (const Pass& ps : passes) unpack |= ps.kind == RELAY_PASS_UNPACK;
+    if (chained && !small && !(flags & RELAY_FLAG_CHAINED) && unpack) chained = false;
     if (chained && (flags & RELAY_FLAG_CHECK_HAZARDS) && !check_chain(chain, E, &why))
       return fail(RELAY_ERR_UNSUPPORTED, "internal (chained launch): " + why);
   }

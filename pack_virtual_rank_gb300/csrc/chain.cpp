@@ -162,12 +162,6 @@ bool build_chain(const std::vector<Pass>& passes, int E, ChainPlan* out, std::st
     }
   }
   out->gfirst.push_back((int32_t)out->segs.size());
-  out->depth = 0;
-  for (size_t g = 0; g + 1 < out->gfirst.size(); ++g) {
-    int d = 1;
-    for (int i = out->gfirst[g] + 1; i < out->gfirst[g + 1]; ++i) d += out->level[i] != out->level[i - 1];
-    out->depth = std::max(out->depth, d);
-  }
   return true;
 }
 

@@ -164,13 +164,7 @@ struct ChainPlan {
   std::vector<uint8_t> level;   // pass of each piece
   std::vector<int32_t> gfirst;  // first piece of each group, then one past the last
   std::vector<int64_t> gn;      // elements of each piece of the group
-  int depth = 0;                // most passes any group spans (block barriers + 1)
 };
-// Calls of more pass traffic than RELAY_FUSED_MAX_BYTES run chained by default when no
-// group spans more than this many passes: on GB300 a 2-pass chain (producer and consumer
-// in one CTA, the consumer's reads served from L2) beat the per-pass launches by 4-27% at
-// 64 MiB-1 GiB per rank, while the 3-pass all-to-all chains lost up to 20%.
-constexpr int kChainLargeMaxDepth = 2;
 bool build_chain(const std::vector<Pass>& passes, int E, ChainPlan* out, std::string* why);
 bool check_chain(const ChainPlan& c, int E, std::string* why);
 // Launches the chained kernel; false (nothing launched) when the program does not fit one
