@@ -1480,10 +1480,17 @@ cudaError_t launch_split(const std::vector<Seg>& direct, const std::vector<Seg>&
                          const std::vector<Seg>& mixed, float scale, cudaStream_t stream,
                          int max_ctas, bool staged) {
   cudaError_t e = cudaSuccess;
-  if (!realigned.empty() && staged) {
-    // the TMA-staged kernel takes the realigned segments and, for a pass of at most
-    // kRealignAllBytes, also its aligned copies and one- or two-source reductions (with a
-    // zero shift), so that such a pass is one launch; the rest stay on the main kernel
+  bool realigned_reduce = false;
+  for (const Seg& sg : realigned) realigned_reduce |= sg.op != kOpCopy;
+  if (!realigned.empty() && staged && realigned_reduce) {
+    // A pass with realigned reductions: the TMA-staged kernel takes the realigned segments
+    // and, for a pass of at most kRealignAllBytes, also its aligned copies and one- or
+    // two-source reductions (with a zero shift), so that such a pass is one launch; the
+    // rest stay on the main kernel. On GB300 this ran an odd-count 2-active reduce-scatter
+    // at 32 MB per rank 8-11% faster than the register-realigning kernel; passes of
+    // realigned copies only (the all-to-all's pack and unpack) ran 3-30% slower staged at
+    // 13.5-135 MB (a few waves each, where every CTA's barrier set-up and bulk-copy latency
+    // shows) and level at 512 MB-1 GiB, so they keep the register path below.
     int64_t bytes = 0;
     for (const Seg& sg : direct) bytes += sg.n * P::kE * (sg.nsrc + sg.ndst);
     for (const Seg& sg : realigned) bytes += sg.n * P::kE * (sg.nsrc + sg.ndst);

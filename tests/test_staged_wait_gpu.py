@@ -35,8 +35,9 @@ def test_staged_wait_runs_out_and_is_reported():
     assert b"bounded wait" in L.relay_last_error()
     assert bool((dst == -1).all())                     # the tile was left unwritten
     assert L.relay_device_status() == rv.OK            # reading cleared the word
-    # the context is still usable: a collective through the staged kernel
-    c = hz.run(rv.ALL_TO_ALL, 4, 8, 40_001, rv.BF16, schedule=rv.SCHEDULE_RELAY,
+    # the context is still usable: a collective whose closing reduction realigns one of its
+    # sources (odd recvCount) runs through the staged kernel
+    c = hz.run(rv.REDUCE_SCATTER, 2, 8, 300_001, rv.F32, 0.5, schedule=rv.SCHEDULE_RELAY,
                flags=rv.FLAG_SEPARATE_PASSES)
     hz.check_all(c)
 
