@@ -492,6 +492,23 @@ def run_ours(args):
     per_pass = [statistics.mean(ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(args.steps))
                 for i in range(npass)]
 
+    # the same steps under the library's default launch policy (no pass events: one chained
+    # launch per call, each CTA running a tile's producers and consumers in pass order)
+    for _ in range(args.warmup):
+        rv.relay_allreduce(send, recv, scratch, count, rv.BF16, A, R, SCALE)
+    default_form = rv.last_launch()
+    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    with Clocks(local, enabled=not args.kernel_only) as clk_d:
+        barrier()
+        d0.record(stream)
+        for k in range(args.steps):
+            rv.relay_allreduce(send, recv, scratch, count, rv.BF16, A, R, SCALE)
+        d1.record(stream)
+        barrier()
+    default_ms = d0.elapsed_time(d1)
+    default_clocks = clk_d.summary()
+
     # every other workload of the metric at one size, timed the same way with its own
     # clock record (rank 0 only: replicas add nothing to a per-collective table)
     per_wl = None
@@ -578,7 +595,8 @@ def run_ours(args):
         e2e_ms = pipeline(e2e_mode, e2e_steps)
         del sets
 
-    ms, e2e_ms = slowest_rank([ms, e2e_ms if e2e_ms is not None else 0.0], world)
+    ms, e2e_ms, default_ms = slowest_rank([ms, e2e_ms if e2e_ms is not None else 0.0, default_ms],
+                                          world)
 
     if rank == 0:
         peak, peak_kind = _peaks()
@@ -660,6 +678,17 @@ def run_ours(args):
                              "(calibration outside the timed region: " + json.dumps(calib) + ")")},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks,
+            "default_path": {
+                "launch": default_form, "ms_per_step": round(default_ms / args.steps, 4),
+                "value": round(whole_job_gbs(nbytes, args.steps, world, default_ms), 2),
+                "unit": "GB/s",
+                "frac": round(whole_job_gbs(nbytes, args.steps, world, default_ms) / world / peak, 4),
+                "note": "the same steps without pass events, under the library's default launch "
+                        "policy; the same algorithmic bytes per step. A chained launch runs each "
+                        "tile's producer and consumer passes in one CTA, so the consumers' reads "
+                        "of what their producers just wrote are served from L2: DRAM traffic is "
+                        "below the algorithmic bytes and the fraction may exceed 1",
+                "clocks": default_clocks},
         }
         if per_wl is not None:
             head = {"workload": "2: allreduce A=2 of R=8, bf16, 1 GiB per rank (the headline above)",
@@ -826,6 +855,21 @@ def run_per_workload(rv, synth, dev, steps, warmup, peak, clk, min_window_s=0.3)
             row["graph_back_to_back_ms_per_call"] = round(e0.elapsed_time(e1) / 100, 5)
             del g1, g20
         if not small:
+            # the same call under the library's default launch policy (no pass events:
+            # one chained launch where the program allows it), back to back
+            for _ in range(warmup):
+                call(opts0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record(stream)
+            for _ in range(steps):
+                call(opts0)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            dms = e0.elapsed_time(e1) / steps
+            row["default_path"] = {"launch": rv.last_launch(), "ms": round(dms, 5),
+                                   "gbs": round(nbytes / dms / 1e6, 1),
+                                   "frac": round(nbytes / dms / 1e6 / peak, 4)}
             row["passes"] = {}
             for q, ts in zip(passes, per_pass):
                 b = q["bytes_read"] + q["bytes_written"]
@@ -1179,8 +1223,9 @@ def _sweep_flat_pack(rv, dev, peak, flush, flush_read, reps):
 def run_profile_case(args):
     """A named collective run W + K times under the library's default launch policy, for
     profiler captures of kernels the bench workload does not exercise (not a bench line).
-    Case: COLLECTIVE:A:DTYPE:COUNT[:relay][:payload], COUNT in the collective's own count;
-    "payload" carries 4-active reduce-scatter partials in the payload type."""
+    Case: COLLECTIVE:A:DTYPE:COUNT[:relay][:payload][:separate][:chained], COUNT in the
+    collective's own count; "payload" carries 4-active reduce-scatter partials in the
+    payload type; "separate" launches pass by pass, "chained" forces the chained launch."""
     import torch
     import pack_virtual_rank_gb300.build as b
     b.build()
@@ -1191,8 +1236,11 @@ def run_profile_case(args):
     coll = {"allreduce": rv.ALLREDUCE, "reduce_scatter": rv.REDUCE_SCATTER,
             "all_gather": rv.ALL_GATHER, "all_to_all": rv.ALL_TO_ALL}[name]
     d = {"f32": rv.F32, "bf16": rv.BF16, "i32": rv.I32}[dt]
+    flags = ((rv.FLAG_PAYLOAD_PARTIAL if "payload" in rest else 0)
+             | (rv.FLAG_SEPARATE_PASSES if "separate" in rest else 0)
+             | (rv.FLAG_CHAINED if "chained" in rest else 0))
     opts = rv.make_opts(schedule=rv.SCHEDULE_RELAY if "relay" in rest else rv.SCHEDULE_AUTO,
-                        flags=rv.FLAG_PAYLOAD_PARTIAL if "payload" in rest else 0)
+                        flags=flags)
     dev = torch.device("cuda", 0)
     plan = rv.relay_plan(coll, count, d, Ap, R, opts)
     xs = [synth.rank_input(9, r, plan.input_elems, dt, device=dev) for r in range(Ap)]
@@ -1215,7 +1263,8 @@ def run_profile_case(args):
     ms = e0.elapsed_time(e1) / args.steps
     nbytes = sum(p["bytes_read"] + p["bytes_written"] for p in rv.relay_plan_passes(plan))
     print(json.dumps({"profile_case": args.profile_case, "passes": len(rv.relay_plan_passes(plan)),
-                      "ms_per_call": round(ms, 4), "gbs": round(nbytes / ms / 1e6, 1)}))
+                      "launch": rv.last_launch(), "ms_per_call": round(ms, 4),
+                      "gbs": round(nbytes / ms / 1e6, 1)}))
     return 0
 
 
