@@ -134,12 +134,16 @@ bool build_chain(const std::vector<Pass>& passes, int E, ChainPlan* out, std::st
     if (!any) break;
   }
 
-  // 2. Join conflicting pieces into groups.
+  // 2. Join conflicting pieces into groups. A piece whose output a later pass reads keeps
+  // its stores in L2 (no streaming hint): its own CTA reads them back right away.
   std::vector<int> parent(ps.size());
   std::iota(parent.begin(), parent.end(), 0);
+  for (Piece& p : ps) p.s.flags &= (uint8_t)~kFlagKeep;
   for_each_conflict(ops, [&](const Operand& a, const Operand& b) {
     const int ra = find(parent, a.piece), rb = find(parent, b.piece);
     if (ra != rb) parent[std::max(ra, rb)] = std::min(ra, rb);
+    if (a.write && !b.write && ps[a.piece].pass < ps[b.piece].pass) ps[a.piece].s.flags |= kFlagKeep;
+    if (b.write && !a.write && ps[b.piece].pass < ps[a.piece].pass) ps[b.piece].s.flags |= kFlagKeep;
   });
   std::vector<std::vector<int>> members(ps.size());
   for (int i = 0; i < (int)ps.size(); ++i) members[find(parent, i)].push_back(i);

@@ -90,6 +90,12 @@ __device__ __forceinline__ void st_v4(void* p, uint4 v) {
                "r"(v.w)
                : "memory");
 }
+// Default-policy 16-byte store, for data the storing CTA reads back (chained launch).
+__device__ __forceinline__ void st_v4_keep(void* p, uint4 v) {
+  asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
 __device__ __forceinline__ void st_u32(void* p, uint32_t v) {
   asm volatile("st.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
@@ -1069,8 +1075,10 @@ __device__ __forceinline__ void piece_vec(const Seg& s, int64_t b, int64_t nvec,
         r = P::pack(acc);
       }
 #pragma unroll 1
-      for (int d = 0; d < s.ndst; ++d)
-        st_v4(reinterpret_cast<uint4*>(static_cast<char*>(s.dst[d]) + b * P::kE) + vi, r);
+      for (int d = 0; d < s.ndst; ++d) {
+        uint4* q = reinterpret_cast<uint4*>(static_cast<char*>(s.dst[d]) + b * P::kE) + vi;
+        if (s.flags & kFlagKeep) st_v4_keep(q, r); else st_v4(q, r);
+      }
     }
   }
 }
@@ -1129,8 +1137,10 @@ __device__ __forceinline__ void piece_realign(const Seg& s, int64_t b, int64_t n
         r = P::pack(acc);
       }
 #pragma unroll 1
-      for (int d = 0; d < s.ndst; ++d)
-        st_v4(reinterpret_cast<uint4*>(static_cast<char*>(s.dst[d]) + b * P::kE) + vi, r);
+      for (int d = 0; d < s.ndst; ++d) {
+        uint4* q = reinterpret_cast<uint4*>(static_cast<char*>(s.dst[d]) + b * P::kE) + vi;
+        if (s.flags & kFlagKeep) st_v4_keep(q, r); else st_v4(q, r);
+      }
     }
   }
 }

@@ -37,7 +37,8 @@ enum SegFlag : uint8_t {
   kFlagVector = 2,    // every pointer 16-byte aligned (set at launch)
   kFlagRealign = 4,   // destinations aligned, sources realigned in registers (set at launch)
   kFlagOutF32 = 8,    // bf16 sources, result stored as fp32 (a wide helper partial)
-  kFlagSrc1F32 = 16   // source 1 is fp32, the rest bf16 (an owner adding a wide partial)
+  kFlagSrc1F32 = 16,  // source 1 is fp32, the rest bf16 (an owner adding a wide partial)
+  kFlagKeep = 32      // chained launch: a later pass of the same CTA reads what this stores
 };
 
 // Device-visible segment descriptor (kernel parameter space).
