@@ -127,10 +127,11 @@ class Clocks:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int, enabled: bool = True):
+    def __init__(self, gpu_index: int, enabled: bool = True, period_ms: int = 100):
         self.proc = None
         self.enabled = enabled
         self.gpu = gpu_index
+        self.period_ms = period_ms
         self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
 
     def __enter__(self):
@@ -139,7 +140,7 @@ class Clocks:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
                 stdout=self.out, stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
@@ -979,7 +980,7 @@ def run_sweep(args):
     print(json.dumps({"device_copy_gbs_this_run": round(copy_gbs, 1), "measured_peak_gbs": peak}),
           flush=True)
     rows = []
-    clk = Clocks(0).__enter__()   # one sampler for the whole sweep; each row its window
+    clk = Clocks(0, period_ms=25).__enter__()   # one sampler for the sweep; each row its window
     for name, A, dt, nbytes, sched in _sweep_points():
         coll, d = colls[name], dts[dt]
         E = rv.ESIZE[d]
@@ -1110,6 +1111,13 @@ def run_sweep(args):
             row.update({"ms_call_default_policy": round(wm, 4),
                         "gbs_call_default_policy": round(tot_b / wm / 1e6, 1),
                         "frac_call_default_policy": round(tot_b / wm / 1e6 / peak, 3)})
+        # a row whose timed calls took less than 0.15 s repeats the same call (L2 flushed
+        # before each, as timed) until they have, so that the sampler sees it running
+        while time.time() - t_row0 < 0.15:
+            flush.fill_(1.0)
+            flush_read.sum()
+            call(opts0)
+            torch.cuda.synchronize()
         row["clocks"] = clk.window(t_row0, time.time())
         key = (name, A, dt, sched)
         if sched in ("auto", "relay") and nbytes == max(b for n2, a2, d2, b, s2 in _sweep_points()

@@ -172,6 +172,49 @@ relay_status_t check_disjoint(const std::vector<Range>& ranges) {
   return RELAY_OK;
 }
 
+// The chained-launch analysis of the last few distinct programs this thread ran, keyed by
+// the exact bytes of their segment tables: a call repeated on the same buffers (the usual
+// case) skips the analysis, which costs more host time than a small call's kernel.
+struct ChainMemo {
+  std::vector<unsigned char> key;
+  ChainPlan plan;
+  bool ok = false;
+  bool checked = false;
+  std::string why;
+};
+constexpr size_t kChainMemoSize = 8;
+thread_local std::vector<ChainMemo> g_chain_memo;
+
+ChainMemo& chain_for(const std::vector<Pass>& passes, int E) {
+  thread_local std::vector<unsigned char> key;
+  key.clear();
+  auto put = [&](const void* p, size_t n) {
+    const unsigned char* b = static_cast<const unsigned char*>(p);
+    key.insert(key.end(), b, b + n);
+  };
+  put(&E, sizeof E);
+  for (const Pass& ps : passes) {
+    const size_t n = ps.segs.size();
+    put(&n, sizeof n);
+    if (n) put(ps.segs.data(), n * sizeof(Seg));
+  }
+  for (size_t i = g_chain_memo.size(); i-- > 0;)
+    if (g_chain_memo[i].key == key) {
+      if (i + 1 != g_chain_memo.size()) {
+        ChainMemo hit = std::move(g_chain_memo[i]);
+        g_chain_memo.erase(g_chain_memo.begin() + (long)i);
+        g_chain_memo.push_back(std::move(hit));
+      }
+      return g_chain_memo.back();
+    }
+  if (g_chain_memo.size() >= kChainMemoSize) g_chain_memo.erase(g_chain_memo.begin());
+  g_chain_memo.emplace_back();
+  ChainMemo& m = g_chain_memo.back();
+  m.key = key;
+  m.ok = build_chain(passes, E, &m.plan, &m.why);
+  return m;
+}
+
 // Optional host checks, then the passes in order on `stream`.
 relay_status_t execute(const std::vector<Pass>& passes, const std::vector<Range>& ranges,
                        relay_dtype_t dtype, float scale, const relay_opts_t* opts,
@@ -204,21 +247,27 @@ relay_status_t execute(const std::vector<Pass>& passes, const std::vector<Range>
     }
   const bool small = bytes <= RELAY_FUSED_MAX_BYTES;
   const bool try_chain = one_launch && passes.size() > 1 && !(flags & RELAY_FLAG_FUSED_PASSES);
-  ChainPlan chain;
+  const ChainPlan* chain = nullptr;
   bool chained = false;
   if (try_chain) {
-    chained = build_chain(passes, E, &chain, &why);
     // past the small-call size, not the coalesced all-to-all (its pack, forward and
     // unpack chains of single copies ran faster pass by pass)
     bool unpack = false;
     for (const Pass& ps : passes) unpack |= ps.kind == RELAY_PASS_UNPACK;
-    if (chained && !small && !(flags & RELAY_FLAG_CHAINED) && unpack) chained = false;
-    if (chained && (flags & RELAY_FLAG_CHECK_HAZARDS) && !check_chain(chain, E, &why))
-      return fail(RELAY_ERR_UNSUPPORTED, "internal (chained launch): " + why);
+    if (small || (flags & RELAY_FLAG_CHAINED) || !unpack) {
+      ChainMemo& m = chain_for(passes, E);
+      chained = m.ok;
+      chain = &m.plan;
+      if (chained && (flags & RELAY_FLAG_CHECK_HAZARDS) && !m.checked) {
+        if (!check_chain(m.plan, E, &why))
+          return fail(RELAY_ERR_UNSUPPORTED, "internal (chained launch): " + why);
+        m.checked = true;
+      }
+    }
   }
   const std::string chain_desc =
-      chained ? "chained: " + std::to_string(chain.gn.size()) + " groups, " +
-                    std::to_string(chain.segs.size()) + " pieces"
+      chained ? "chained: " + std::to_string(chain->gn.size()) + " groups, " +
+                    std::to_string(chain->segs.size()) + " pieces"
               : std::string();
   if (flags & RELAY_FLAG_DRY_RUN) {
     g_last_launch = chained ? chain_desc : "dry run";
@@ -226,7 +275,7 @@ relay_status_t execute(const std::vector<Pass>& passes, const std::vector<Range>
   }
   if (chained) {
     cudaError_t e = cudaSuccess;
-    if (launch_chain(dtype, chain, scale, stream, &e)) {
+    if (launch_chain(dtype, *chain, scale, stream, &e)) {
       if (e != cudaSuccess) return fail(RELAY_ERR_CUDA, cudaGetErrorString(e));
       g_last_launch = chain_desc;
       return RELAY_OK;
