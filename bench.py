@@ -41,6 +41,7 @@ CPU_BASELINE_SAMPLE = 1 << 27  # elements per rank of the bench's own CPU-baseli
 PROFILE = os.path.join(ROOT, "profiles", "relay_pass_kernel_allreduce_a2_bf16_1g.json")
 KERNEL_SRC = os.path.join(ROOT, "pack_virtual_rank_gb300", "csrc", "passes.cu")
 KERNEL_HDR = os.path.join(ROOT, "pack_virtual_rank_gb300", "csrc", "program.h")
+KERNEL_DEV = os.path.join(ROOT, "pack_virtual_rank_gb300", "csrc", "device.cuh")
 HOST_SIDE_MARK = "// ------------------------------------------------------------------- host side --"
 
 
@@ -87,16 +88,17 @@ def _theoretical_hbm_gbs(dev):
 
 
 def kernel_code_sha() -> str:
-    """First 16 hex digits of the SHA-256 of the kernels' code: the segment layout and tile
-    constants (program.h) and the device part of passes.cu (everything before its host-side
-    section), with comments removed and every run of whitespace folded to one space. An edit
-    to a comment or to the host-side launch code keeps the recorded counters; any change to
-    what the kernels execute voids them."""
+    """First 16 hex digits of the SHA-256 of the per-pass kernels' code: the segment layout
+    and tile constants (program.h), the shared device primitives (device.cuh) and the device
+    part of passes.cu (everything before its host-side section), with comments removed and
+    every run of whitespace folded to one space. An edit to a comment, to the host-side
+    launch code or to another kernel's file keeps the recorded counters; any change to what
+    these kernels execute voids them."""
     src = open(KERNEL_SRC).read()
     cut = src.find(HOST_SIDE_MARK)
     if cut >= 0:
         src = src[:cut]
-    text = open(KERNEL_HDR).read() + "\n" + src
+    text = open(KERNEL_HDR).read() + "\n" + open(KERNEL_DEV).read() + "\n" + src
     text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
     text = re.sub(r"//[^\n]*", " ", text)
     text = " ".join(text.split())

@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "librelay.so")
 
-SOURCES = ["plan.cpp", "program.cpp", "chain.cpp", "abi.cpp", "passes.cu", "noalloc.cu"]
+SOURCES = ["plan.cpp", "program.cpp", "chain.cpp", "abi.cpp", "passes.cu", "chain_kernel.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -43,6 +43,7 @@ def _stale() -> bool:
         return True
     t = os.path.getmtime(LIB)
     deps = [os.path.join(CSRC, s) for s in SOURCES] + [os.path.join(CSRC, "program.h"),
+                                                       os.path.join(CSRC, "device.cuh"),
                                                        os.path.join(INCLUDE, "relay.h"), __file__]
     return any(os.path.getmtime(d) > t for d in deps)
 

@@ -1,0 +1,308 @@
+// chain_kernel.cu -- the chained launch's kernel and its launcher (the analysis that groups the
+// pieces is chain.cpp).
+//
+// One ordinary launch for a whole call: CTA t runs tile t of one group of pieces in pass
+// order, with a block barrier between passes, so every dependency of the schedule stays
+// inside one CTA and no CTA ever waits for another.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <algorithm>
+
+#include "device.cuh"
+
+namespace relay {
+namespace {
+
+// One ordinary launch for a whole call: CTA t runs tile t of one group of pieces (chain.cpp)
+// in pass order, with a block barrier between passes, so every dependency of the schedule
+// stays inside one CTA and no CTA ever waits for another. A piece is any element range of
+// a segment; its alignment is sorted out here: a scalar head until the destinations sit on
+// a 16-byte boundary, then 16-byte vectors (sources realigned from two aligned blocks when
+// only they are off the grid), then a scalar tail.
+
+template <int CAP>
+struct ChainArgs {
+  int32_t ngroup;
+  int32_t ntask;
+  float scale;
+  int32_t tile;               // elements per task
+  Seg seg[CAP];               // tile0: first task of the piece's group
+  int16_t gfirst[CAP + 1];    // first piece of each group, then one past the last
+  uint8_t level[CAP];         // pass of each piece
+};
+
+// Elements [b, e) of a piece one at a time (copies move raw bits).
+template <class P, bool COH>
+__device__ __forceinline__ void piece_scalar(const Seg& s, int64_t b, int64_t e, float scale) {
+  using Acc = typename P::Acc;
+  const bool copy = s.op == kOpCopy;
+  const bool do_scale = (s.flags & kFlagScale) != 0;
+#pragma unroll 1
+  for (int64_t i = b + threadIdx.x; i < e; i += kThreads) {
+    const int64_t off = i * P::kE;
+    if (copy) {
+      if (P::kE == 4) {
+        const uint32_t x = Mem<COH>::u32(static_cast<const char*>(s.src[0]) + off);
+#pragma unroll 1
+        for (int d = 0; d < s.ndst; ++d) st_u32(static_cast<char*>(s.dst[d]) + off, x);
+      } else {
+        const uint16_t x = Mem<COH>::u16(static_cast<const char*>(s.src[0]) + off);
+#pragma unroll 1
+        for (int d = 0; d < s.ndst; ++d) st_u16(static_cast<char*>(s.dst[d]) + off, x);
+      }
+      continue;
+    }
+    Acc acc = P::template load1<COH>(static_cast<const char*>(s.src[0]) + off);
+#pragma unroll 1
+    for (int k = 1; k < s.nsrc; ++k)
+      acc = P::add(acc, P::template load1<COH>(static_cast<const char*>(s.src[k]) + off));
+    if (do_scale) acc = P::scale(acc, scale);
+#pragma unroll 1
+    for (int d = 0; d < s.ndst; ++d) P::store1(static_cast<char*>(s.dst[d]) + off, acc);
+  }
+}
+
+// nvec 16-byte vectors from element b on, every pointer 16-byte aligned there. Loads of a
+// batch are issued together (4 vectors per thread per source, 2 past two sources).
+template <class P, int NSRC, bool COH>
+__device__ __forceinline__ void piece_vec(const Seg& s, int64_t b, int64_t nvec, float scale) {
+  constexpr int L = P::kLanes;
+  constexpr int UB = NSRC <= 2 ? kUnroll : kUnroll / 2;
+  using Acc = typename P::Acc;
+  const bool do_scale = (s.flags & kFlagScale) != 0;
+  const uint4* src[NSRC];
+#pragma unroll
+  for (int k = 0; k < NSRC; ++k)
+    src[k] = reinterpret_cast<const uint4*>(static_cast<const char*>(s.src[k]) + b * P::kE);
+#pragma unroll 1
+  for (int64_t v0 = threadIdx.x; v0 < nvec; v0 += (int64_t)kThreads * UB) {
+    uint4 v[NSRC][UB];
+#pragma unroll
+    for (int u = 0; u < UB; ++u) {
+      const int64_t vi = v0 + (int64_t)u * kThreads;
+#pragma unroll
+      for (int k = 0; k < NSRC; ++k)
+        v[k][u] = vi < nvec ? Mem<COH>::v4(src[k] + vi) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < UB; ++u) {
+      const int64_t vi = v0 + (int64_t)u * kThreads;
+      if (vi >= nvec) continue;
+      uint4 r = v[0][u];
+      if (s.op != kOpCopy) {
+        Acc acc[L], t[L];
+        P::unpack(v[0][u], acc);
+#pragma unroll
+        for (int k = 1; k < NSRC; ++k) {
+          P::unpack(v[k][u], t);
+#pragma unroll
+          for (int i = 0; i < L; ++i) acc[i] = P::add(acc[i], t[i]);
+        }
+        if (do_scale) {
+#pragma unroll
+          for (int i = 0; i < L; ++i) acc[i] = P::scale(acc[i], scale);
+        }
+        r = P::pack(acc);
+      }
+#pragma unroll 1
+      for (int d = 0; d < s.ndst; ++d) {
+        uint4* q = reinterpret_cast<uint4*>(static_cast<char*>(s.dst[d]) + b * P::kE) + vi;
+        if (s.flags & kFlagKeep) st_v4_keep(q, r); else st_v4(q, r);
+      }
+    }
+  }
+}
+
+// The same with the destinations aligned at element b but one or two sources off the
+// 16-byte grid: each vector of such a source is funnel-shifted out of the two aligned
+// blocks it straddles (both hold bytes of the piece's own source range).
+template <class P, int NSRC, bool COH>
+__device__ __forceinline__ void piece_realign(const Seg& s, int64_t b, int64_t nvec, float scale) {
+  constexpr int L = P::kLanes;
+  constexpr int UB = 2;
+  using Acc = typename P::Acc;
+  const bool do_scale = (s.flags & kFlagScale) != 0;
+  unsigned sig[NSRC];
+  const uint4* a[NSRC];
+#pragma unroll
+  for (int k = 0; k < NSRC; ++k) {
+    const char* p = static_cast<const char*>(s.src[k]) + b * P::kE;
+    sig[k] = (unsigned)(reinterpret_cast<uintptr_t>(p) & 15u);
+    a[k] = reinterpret_cast<const uint4*>(p - sig[k]);
+  }
+#pragma unroll 1
+  for (int64_t v0 = threadIdx.x; v0 < nvec; v0 += (int64_t)kThreads * UB) {
+    uint4 v[NSRC][UB];
+#pragma unroll
+    for (int u = 0; u < UB; ++u) {
+      const int64_t vi = v0 + (int64_t)u * kThreads;
+#pragma unroll
+      for (int k = 0; k < NSRC; ++k) {
+        if (vi < nvec) {
+          v[k][u] = Mem<COH>::v4(a[k] + vi);
+          if (sig[k] != 0) v[k][u] = shift_pair(v[k][u], Mem<COH>::v4(a[k] + vi + 1), sig[k]);
+        } else {
+          v[k][u] = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < UB; ++u) {
+      const int64_t vi = v0 + (int64_t)u * kThreads;
+      if (vi >= nvec) continue;
+      uint4 r = v[0][u];
+      if (s.op != kOpCopy) {
+        Acc acc[L], t[L];
+        P::unpack(v[0][u], acc);
+#pragma unroll
+        for (int k = 1; k < NSRC; ++k) {
+          P::unpack(v[k][u], t);
+#pragma unroll
+          for (int i = 0; i < L; ++i) acc[i] = P::add(acc[i], t[i]);
+        }
+        if (do_scale) {
+#pragma unroll
+          for (int i = 0; i < L; ++i) acc[i] = P::scale(acc[i], scale);
+        }
+        r = P::pack(acc);
+      }
+#pragma unroll 1
+      for (int d = 0; d < s.ndst; ++d) {
+        uint4* q = reinterpret_cast<uint4*>(static_cast<char*>(s.dst[d]) + b * P::kE) + vi;
+        if (s.flags & kFlagKeep) st_v4_keep(q, r); else st_v4(q, r);
+      }
+    }
+  }
+}
+
+// Elements [base, base + len) of segment s, whatever the alignment of its pointers there.
+template <class P, bool COH>
+__device__ __noinline__ void run_piece(const Seg& s, int64_t base, int64_t len, float scale) {
+  constexpr int E = P::kE, L = P::kLanes;
+  auto mis = [&](const void* p) {
+    return (unsigned)((reinterpret_cast<uintptr_t>(p) + (uintptr_t)(base * E)) & 15u);
+  };
+  const unsigned md = mis(s.dst[0]);
+  bool dsame = md % E == 0;
+  for (int d = 1; d < s.ndst; ++d) dsame &= mis(s.dst[d]) == md;
+  if (!dsame) {
+    piece_scalar<P, COH>(s, base, base + len, scale);
+    return;
+  }
+  const int64_t head = min((int64_t)(((16u - md) & 15u) / E), len);
+  piece_scalar<P, COH>(s, base, base + head, scale);
+  const int64_t b1 = base + head;
+  const int64_t nvec = (len - head) / L;
+  if (nvec > 0) {
+    bool sal = true;
+    for (int k = 0; k < s.nsrc; ++k)
+      sal &= ((reinterpret_cast<uintptr_t>(s.src[k]) + (uintptr_t)(b1 * E)) & 15u) == 0;
+    if (sal) {
+      switch (s.op == kOpCopy ? 1 : s.nsrc) {
+        case 1: piece_vec<P, 1, COH>(s, b1, nvec, scale); break;
+        case 2: piece_vec<P, 2, COH>(s, b1, nvec, scale); break;
+        case 3: piece_vec<P, 3, COH>(s, b1, nvec, scale); break;
+        default: piece_vec<P, 4, COH>(s, b1, nvec, scale); break;
+      }
+    } else if (s.op == kOpCopy || s.nsrc == 1) {
+      piece_realign<P, 1, COH>(s, b1, nvec, scale);
+    } else if (s.nsrc == 2) {
+      piece_realign<P, 2, COH>(s, b1, nvec, scale);
+    } else {
+      piece_scalar<P, COH>(s, b1, b1 + nvec * L, scale);
+    }
+  }
+  piece_scalar<P, COH>(s, b1 + nvec * L, base + len, scale);
+}
+
+template <class P, int CAP>
+__global__ void __launch_bounds__(kThreads, 5) relay_chain_kernel(const __grid_constant__ ChainArgs<CAP> a) {
+  const int t = blockIdx.x;
+  // the last group whose first task is <= t (uniform across the CTA)
+  int lo = 0, hi = a.ngroup - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (a.seg[a.gfirst[mid]].tile0 <= t) lo = mid; else hi = mid - 1;
+  }
+  const int f = a.gfirst[lo], l = a.gfirst[lo + 1];
+  const int64_t base = (int64_t)(t - a.seg[f].tile0) * a.tile;
+  const int64_t len = min((int64_t)a.tile, a.seg[f].n - base);
+  int lvl = a.level[f];
+  for (int i = f; i < l; ++i) {
+    if (a.level[i] != lvl) {
+      // the previous pass's stores of this tile are visible to the whole CTA after this
+      __syncthreads();
+      lvl = a.level[i];
+    }
+    // the first pass reads only memory written before the launch; later passes read what
+    // this CTA has just written, through L2
+    if (lvl == a.level[f]) run_piece<P, false>(a.seg[i], base, len, a.scale);
+    else run_piece<P, true>(a.seg[i], base, len, a.scale);
+  }
+}
+
+template <class P, int CAP>
+cudaError_t launch_chain_cap(const ChainPlan& c, float scale, int64_t tile, cudaStream_t stream,
+                             int* ntask_out) {
+  static thread_local ChainArgs<CAP> a;  // up to ~31 KiB: keep it off the stack
+  const int G = (int)c.gn.size();
+  int64_t tasks = 0;
+  for (int g = 0; g < G; ++g) {
+    a.gfirst[g] = (int16_t)c.gfirst[g];
+    for (int i = c.gfirst[g]; i < c.gfirst[g + 1]; ++i) {
+      a.seg[i] = c.segs[i];
+      a.seg[i].tile0 = (int32_t)tasks;
+      a.level[i] = c.level[i];
+    }
+    tasks += (c.gn[g] + tile - 1) / tile;
+  }
+  a.gfirst[G] = (int16_t)c.gfirst[G];
+  a.ngroup = G;
+  a.ntask = (int32_t)tasks;
+  a.scale = scale;
+  a.tile = (int32_t)tile;
+  *ntask_out = (int)tasks;
+  relay_chain_kernel<P, CAP><<<(unsigned)tasks, kThreads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+template <class P>
+cudaError_t launch_chain_typed(const ChainPlan& c, float scale, int64_t tile, cudaStream_t stream,
+                               int* ntask) {
+  const size_t n = c.segs.size();
+  if (n <= 32) return launch_chain_cap<P, 32>(c, scale, tile, stream, ntask);
+  if (n <= 128) return launch_chain_cap<P, 128>(c, scale, tile, stream, ntask);
+  return launch_chain_cap<P, kChainMaxPieces>(c, scale, tile, stream, ntask);
+}
+
+}  // namespace
+
+// Tiles of 16 KiB, halved (down to 4 KiB, one 16-byte vector per thread) while the call
+// has fewer tasks than twice the SMs: in the latency-bound regime more, smaller tasks
+// spread the same bytes over more SMs.
+bool launch_chain(int dtype, const ChainPlan& c, float scale, cudaStream_t stream,
+                  cudaError_t* err) {
+  *err = cudaSuccess;
+  if (c.segs.empty() || c.segs.size() > (size_t)kChainMaxPieces) return false;
+  const int E = esize_of(dtype);
+  int64_t tile_bytes = kTileBytes;
+  auto tasks = [&](int64_t tb) {
+    int64_t t = 0;
+    for (int64_t n : c.gn) t += (n + tb / E - 1) / (tb / E);
+    return t;
+  };
+  while (tile_bytes > (int64_t)kThreads * kVecBytes && tasks(tile_bytes) < 2 * sm_count())
+    tile_bytes /= 2;
+  if (tasks(tile_bytes) > INT32_MAX) return false;
+  const int64_t tile = tile_bytes / E;
+  int ntask = 0;
+  switch (dtype) {
+    case RELAY_F32: *err = launch_chain_typed<TF32>(c, scale, tile, stream, &ntask); break;
+    case RELAY_BF16: *err = launch_chain_typed<TBF16>(c, scale, tile, stream, &ntask); break;
+    default: *err = launch_chain_typed<TI32>(c, scale, tile, stream, &ntask); break;
+  }
+  return true;
+}
+
+}  // namespace relay

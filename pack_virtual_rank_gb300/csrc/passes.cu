@@ -19,6 +19,7 @@
 #include <algorithm>
 #include <type_traits>
 
+#include "device.cuh"
 #include "program.h"
 
 namespace relay {
@@ -32,147 +33,6 @@ struct PassArgs {
   int32_t extra_tx;  // staged kernel: bytes its barrier expects beyond the copies (0; a test
                      // sets it to make a wait run out)
   Seg seg[CAP];
-};
-
-// ---------------------------------------------------------------- memory access --
-
-// Loads. The per-pass kernels read only what earlier launches wrote, so they use the
-// non-coherent path without allocating in L1. The fused small-call kernel reads, after a
-// grid barrier, what other CTAs of the same launch wrote: it loads through L2 only
-// (.cg), which is coherent across SMs.
-template <bool COH>
-struct Mem;
-template <>
-struct Mem<false> {
-  static __device__ __forceinline__ uint4 v4(const void* p) {
-    uint4 r;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "l"(p));
-    return r;
-  }
-  static __device__ __forceinline__ uint32_t u32(const void* p) {
-    uint32_t r;
-    asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(r) : "l"(p));
-    return r;
-  }
-  static __device__ __forceinline__ uint16_t u16(const void* p) {
-    uint16_t r;
-    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(r) : "l"(p));
-    return r;
-  }
-};
-template <>
-struct Mem<true> {
-  static __device__ __forceinline__ uint4 v4(const void* p) {
-    uint4 r;
-    asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "l"(p));
-    return r;
-  }
-  static __device__ __forceinline__ uint32_t u32(const void* p) {
-    uint32_t r;
-    asm volatile("ld.global.cg.u32 %0, [%1];" : "=r"(r) : "l"(p));
-    return r;
-  }
-  static __device__ __forceinline__ uint16_t u16(const void* p) {
-    uint16_t r;
-    asm volatile("ld.global.cg.u16 %0, [%1];" : "=h"(r) : "l"(p));
-    return r;
-  }
-};
-__device__ __forceinline__ uint4 ld_stream_v4(const void* p) { return Mem<false>::v4(p); }
-// 16-byte stores are streaming (.cs, evict first): no pass re-reads its own output, and
-// on GB300 this measured 0.4-2.7% faster than default stores with one CTA per tile.
-__device__ __forceinline__ void st_v4(void* p, uint4 v) {
-  asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
-               "r"(v.w)
-               : "memory");
-}
-// Default-policy 16-byte store, for data the storing CTA reads back (chained launch).
-__device__ __forceinline__ void st_v4_keep(void* p, uint4 v) {
-  asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
-               "r"(v.w)
-               : "memory");
-}
-__device__ __forceinline__ void st_u32(void* p, uint32_t v) {
-  asm volatile("st.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ void st_u16(void* p, uint16_t v) {
-  asm volatile("st.global.u16 [%0], %1;" ::"l"(p), "h"(v) : "memory");
-}
-
-// ------------------------------------------------------------- payload traits --
-// bf16 is the upper half of a binary32, so widening is a shift; narrowing rounds to
-// nearest-even in one cvt instruction (two lanes at a time).
-
-__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
-  uint32_t d;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
-  return d;
-}
-
-struct TF32 {
-  static constexpr int kE = 4, kLanes = 4;
-  using Acc = float;
-  static __device__ __forceinline__ void unpack(uint4 v, float* a) {
-    a[0] = __uint_as_float(v.x); a[1] = __uint_as_float(v.y);
-    a[2] = __uint_as_float(v.z); a[3] = __uint_as_float(v.w);
-  }
-  static __device__ __forceinline__ uint4 pack(const float* a) {
-    return make_uint4(__float_as_uint(a[0]), __float_as_uint(a[1]), __float_as_uint(a[2]),
-                      __float_as_uint(a[3]));
-  }
-  static __device__ __forceinline__ float add(float x, float y) { return __fadd_rn(x, y); }
-  static __device__ __forceinline__ float scale(float x, float s) { return __fmul_rn(x, s); }
-  template <bool COH>
-  static __device__ __forceinline__ float load1(const void* p) {
-    return __uint_as_float(Mem<COH>::u32(p));
-  }
-  static __device__ __forceinline__ void store1(void* p, float v) { st_u32(p, __float_as_uint(v)); }
-};
-
-struct TBF16 {
-  static constexpr int kE = 2, kLanes = 8;
-  using Acc = float;
-  static __device__ __forceinline__ void unpack(uint4 v, float* a) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      a[2 * i] = __uint_as_float(w[i] << 16);
-      a[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-    }
-  }
-  static __device__ __forceinline__ uint4 pack(const float* a) {
-    return make_uint4(bf16x2_rn(a[0], a[1]), bf16x2_rn(a[2], a[3]), bf16x2_rn(a[4], a[5]),
-                      bf16x2_rn(a[6], a[7]));
-  }
-  static __device__ __forceinline__ float add(float x, float y) { return __fadd_rn(x, y); }
-  static __device__ __forceinline__ float scale(float x, float s) { return __fmul_rn(x, s); }
-  template <bool COH>
-  static __device__ __forceinline__ float load1(const void* p) {
-    return __uint_as_float((uint32_t)Mem<COH>::u16(p) << 16);
-  }
-  static __device__ __forceinline__ void store1(void* p, float v) {
-    st_u16(p, (uint16_t)(bf16x2_rn(v, 0.0f) & 0xffffu));
-  }
-};
-
-struct TI32 {
-  static constexpr int kE = 4, kLanes = 4;
-  using Acc = uint32_t;  // two's-complement sums wrap modulo 2^32
-  static __device__ __forceinline__ void unpack(uint4 v, uint32_t* a) {
-    a[0] = v.x; a[1] = v.y; a[2] = v.z; a[3] = v.w;
-  }
-  static __device__ __forceinline__ uint4 pack(const uint32_t* a) {
-    return make_uint4(a[0], a[1], a[2], a[3]);
-  }
-  static __device__ __forceinline__ uint32_t add(uint32_t x, uint32_t y) { return x + y; }
-  static __device__ __forceinline__ uint32_t scale(uint32_t x, float) { return x; }
-  template <bool COH>
-  static __device__ __forceinline__ uint32_t load1(const void* p) { return Mem<COH>::u32(p); }
-  static __device__ __forceinline__ void store1(void* p, uint32_t v) { st_u32(p, v); }
 };
 
 // ---------------------------------------------------------------- tile bodies --
@@ -250,33 +110,8 @@ __device__ __forceinline__ void run_full_tile(const Seg& s, int64_t base, float 
 // segmentCount is not a multiple of the vector width, an odd recvCount): each lane loads
 // the aligned 16-byte vector that holds the start of its source range, takes the next
 // one from its right neighbour by a warp shuffle, and funnel-shifts the pair by the
-// source's byte offset (the full-tile path below; the one-launch kernel loads both blocks
+// source's byte offset (shift_pair, device.cuh; the one-launch kernel loads both blocks
 // itself). Reads stay inside the 16-byte blocks that hold the segment's own bytes.
-
-__device__ __forceinline__ uint4 shift_pair(uint4 lo, uint4 hi, unsigned sigma) {
-  const unsigned r = (sigma & 3u) * 8u;
-  uint32_t w0 = lo.x, w1 = lo.y, w2 = lo.z, w3 = lo.w, w4 = hi.x, w5 = hi.y, w6 = hi.z, w7 = hi.w;
-  uint4 o;
-  switch (sigma >> 2) {
-    case 0:
-      o.x = __funnelshift_r(w0, w1, r); o.y = __funnelshift_r(w1, w2, r);
-      o.z = __funnelshift_r(w2, w3, r); o.w = __funnelshift_r(w3, w4, r);
-      break;
-    case 1:
-      o.x = __funnelshift_r(w1, w2, r); o.y = __funnelshift_r(w2, w3, r);
-      o.z = __funnelshift_r(w3, w4, r); o.w = __funnelshift_r(w4, w5, r);
-      break;
-    case 2:
-      o.x = __funnelshift_r(w2, w3, r); o.y = __funnelshift_r(w3, w4, r);
-      o.z = __funnelshift_r(w4, w5, r); o.w = __funnelshift_r(w5, w6, r);
-      break;
-    default:
-      o.x = __funnelshift_r(w3, w4, r); o.y = __funnelshift_r(w4, w5, r);
-      o.z = __funnelshift_r(w5, w6, r); o.w = __funnelshift_r(w6, w7, r);
-      break;
-  }
-  return o;
-}
 
 // TAIL: a segment's last, partial tile. Only its first `nvec` whole vectors are stored; a
 // block is loaded only if it holds bytes of those vectors (the block after the last one
@@ -982,235 +817,6 @@ __global__ void __launch_bounds__(kThreads, 4) relay_fused_kernel(const __grid_c
   }
 }
 
-// ------------------------------------------------------------ chained launch --
-// One ordinary launch for a whole call: CTA t runs tile t of one group of pieces (chain.cpp)
-// in pass order, with a block barrier between passes, so every dependency of the schedule
-// stays inside one CTA and no CTA ever waits for another. A piece is any element range of
-// a segment; its alignment is sorted out here: a scalar head until the destinations sit on
-// a 16-byte boundary, then 16-byte vectors (sources realigned from two aligned blocks when
-// only they are off the grid), then a scalar tail.
-
-template <int CAP>
-struct ChainArgs {
-  int32_t ngroup;
-  int32_t ntask;
-  float scale;
-  int32_t tile;               // elements per task
-  Seg seg[CAP];               // tile0: first task of the piece's group
-  int16_t gfirst[CAP + 1];    // first piece of each group, then one past the last
-  uint8_t level[CAP];         // pass of each piece
-};
-
-// Elements [b, e) of a piece one at a time (copies move raw bits).
-template <class P, bool COH>
-__device__ __forceinline__ void piece_scalar(const Seg& s, int64_t b, int64_t e, float scale) {
-  using Acc = typename P::Acc;
-  const bool copy = s.op == kOpCopy;
-  const bool do_scale = (s.flags & kFlagScale) != 0;
-#pragma unroll 1
-  for (int64_t i = b + threadIdx.x; i < e; i += kThreads) {
-    const int64_t off = i * P::kE;
-    if (copy) {
-      if (P::kE == 4) {
-        const uint32_t x = Mem<COH>::u32(static_cast<const char*>(s.src[0]) + off);
-#pragma unroll 1
-        for (int d = 0; d < s.ndst; ++d) st_u32(static_cast<char*>(s.dst[d]) + off, x);
-      } else {
-        const uint16_t x = Mem<COH>::u16(static_cast<const char*>(s.src[0]) + off);
-#pragma unroll 1
-        for (int d = 0; d < s.ndst; ++d) st_u16(static_cast<char*>(s.dst[d]) + off, x);
-      }
-      continue;
-    }
-    Acc acc = P::template load1<COH>(static_cast<const char*>(s.src[0]) + off);
-#pragma unroll 1
-    for (int k = 1; k < s.nsrc; ++k)
-      acc = P::add(acc, P::template load1<COH>(static_cast<const char*>(s.src[k]) + off));
-    if (do_scale) acc = P::scale(acc, scale);
-#pragma unroll 1
-    for (int d = 0; d < s.ndst; ++d) P::store1(static_cast<char*>(s.dst[d]) + off, acc);
-  }
-}
-
-// nvec 16-byte vectors from element b on, every pointer 16-byte aligned there. Loads of a
-// batch are issued together (4 vectors per thread per source, 2 past two sources).
-template <class P, int NSRC, bool COH>
-__device__ __forceinline__ void piece_vec(const Seg& s, int64_t b, int64_t nvec, float scale) {
-  constexpr int L = P::kLanes;
-  constexpr int UB = NSRC <= 2 ? kUnroll : kUnroll / 2;
-  using Acc = typename P::Acc;
-  const bool do_scale = (s.flags & kFlagScale) != 0;
-  const uint4* src[NSRC];
-#pragma unroll
-  for (int k = 0; k < NSRC; ++k)
-    src[k] = reinterpret_cast<const uint4*>(static_cast<const char*>(s.src[k]) + b * P::kE);
-#pragma unroll 1
-  for (int64_t v0 = threadIdx.x; v0 < nvec; v0 += (int64_t)kThreads * UB) {
-    uint4 v[NSRC][UB];
-#pragma unroll
-    for (int u = 0; u < UB; ++u) {
-      const int64_t vi = v0 + (int64_t)u * kThreads;
-#pragma unroll
-      for (int k = 0; k < NSRC; ++k)
-        v[k][u] = vi < nvec ? Mem<COH>::v4(src[k] + vi) : make_uint4(0u, 0u, 0u, 0u);
-    }
-#pragma unroll
-    for (int u = 0; u < UB; ++u) {
-      const int64_t vi = v0 + (int64_t)u * kThreads;
-      if (vi >= nvec) continue;
-      uint4 r = v[0][u];
-      if (s.op != kOpCopy) {
-        Acc acc[L], t[L];
-        P::unpack(v[0][u], acc);
-#pragma unroll
-        for (int k = 1; k < NSRC; ++k) {
-          P::unpack(v[k][u], t);
-#pragma unroll
-          for (int i = 0; i < L; ++i) acc[i] = P::add(acc[i], t[i]);
-        }
-        if (do_scale) {
-#pragma unroll
-          for (int i = 0; i < L; ++i) acc[i] = P::scale(acc[i], scale);
-        }
-        r = P::pack(acc);
-      }
-#pragma unroll 1
-      for (int d = 0; d < s.ndst; ++d) {
-        uint4* q = reinterpret_cast<uint4*>(static_cast<char*>(s.dst[d]) + b * P::kE) + vi;
-        if (s.flags & kFlagKeep) st_v4_keep(q, r); else st_v4(q, r);
-      }
-    }
-  }
-}
-
-// The same with the destinations aligned at element b but one or two sources off the
-// 16-byte grid: each vector of such a source is funnel-shifted out of the two aligned
-// blocks it straddles (both hold bytes of the piece's own source range).
-template <class P, int NSRC, bool COH>
-__device__ __forceinline__ void piece_realign(const Seg& s, int64_t b, int64_t nvec, float scale) {
-  constexpr int L = P::kLanes;
-  constexpr int UB = 2;
-  using Acc = typename P::Acc;
-  const bool do_scale = (s.flags & kFlagScale) != 0;
-  unsigned sig[NSRC];
-  const uint4* a[NSRC];
-#pragma unroll
-  for (int k = 0; k < NSRC; ++k) {
-    const char* p = static_cast<const char*>(s.src[k]) + b * P::kE;
-    sig[k] = (unsigned)(reinterpret_cast<uintptr_t>(p) & 15u);
-    a[k] = reinterpret_cast<const uint4*>(p - sig[k]);
-  }
-#pragma unroll 1
-  for (int64_t v0 = threadIdx.x; v0 < nvec; v0 += (int64_t)kThreads * UB) {
-    uint4 v[NSRC][UB];
-#pragma unroll
-    for (int u = 0; u < UB; ++u) {
-      const int64_t vi = v0 + (int64_t)u * kThreads;
-#pragma unroll
-      for (int k = 0; k < NSRC; ++k) {
-        if (vi < nvec) {
-          v[k][u] = Mem<COH>::v4(a[k] + vi);
-          if (sig[k] != 0) v[k][u] = shift_pair(v[k][u], Mem<COH>::v4(a[k] + vi + 1), sig[k]);
-        } else {
-          v[k][u] = make_uint4(0u, 0u, 0u, 0u);
-        }
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < UB; ++u) {
-      const int64_t vi = v0 + (int64_t)u * kThreads;
-      if (vi >= nvec) continue;
-      uint4 r = v[0][u];
-      if (s.op != kOpCopy) {
-        Acc acc[L], t[L];
-        P::unpack(v[0][u], acc);
-#pragma unroll
-        for (int k = 1; k < NSRC; ++k) {
-          P::unpack(v[k][u], t);
-#pragma unroll
-          for (int i = 0; i < L; ++i) acc[i] = P::add(acc[i], t[i]);
-        }
-        if (do_scale) {
-#pragma unroll
-          for (int i = 0; i < L; ++i) acc[i] = P::scale(acc[i], scale);
-        }
-        r = P::pack(acc);
-      }
-#pragma unroll 1
-      for (int d = 0; d < s.ndst; ++d) {
-        uint4* q = reinterpret_cast<uint4*>(static_cast<char*>(s.dst[d]) + b * P::kE) + vi;
-        if (s.flags & kFlagKeep) st_v4_keep(q, r); else st_v4(q, r);
-      }
-    }
-  }
-}
-
-// Elements [base, base + len) of segment s, whatever the alignment of its pointers there.
-template <class P, bool COH>
-__device__ __noinline__ void run_piece(const Seg& s, int64_t base, int64_t len, float scale) {
-  constexpr int E = P::kE, L = P::kLanes;
-  auto mis = [&](const void* p) {
-    return (unsigned)((reinterpret_cast<uintptr_t>(p) + (uintptr_t)(base * E)) & 15u);
-  };
-  const unsigned md = mis(s.dst[0]);
-  bool dsame = md % E == 0;
-  for (int d = 1; d < s.ndst; ++d) dsame &= mis(s.dst[d]) == md;
-  if (!dsame) {
-    piece_scalar<P, COH>(s, base, base + len, scale);
-    return;
-  }
-  const int64_t head = min((int64_t)(((16u - md) & 15u) / E), len);
-  piece_scalar<P, COH>(s, base, base + head, scale);
-  const int64_t b1 = base + head;
-  const int64_t nvec = (len - head) / L;
-  if (nvec > 0) {
-    bool sal = true;
-    for (int k = 0; k < s.nsrc; ++k)
-      sal &= ((reinterpret_cast<uintptr_t>(s.src[k]) + (uintptr_t)(b1 * E)) & 15u) == 0;
-    if (sal) {
-      switch (s.op == kOpCopy ? 1 : s.nsrc) {
-        case 1: piece_vec<P, 1, COH>(s, b1, nvec, scale); break;
-        case 2: piece_vec<P, 2, COH>(s, b1, nvec, scale); break;
-        case 3: piece_vec<P, 3, COH>(s, b1, nvec, scale); break;
-        default: piece_vec<P, 4, COH>(s, b1, nvec, scale); break;
-      }
-    } else if (s.op == kOpCopy || s.nsrc == 1) {
-      piece_realign<P, 1, COH>(s, b1, nvec, scale);
-    } else if (s.nsrc == 2) {
-      piece_realign<P, 2, COH>(s, b1, nvec, scale);
-    } else {
-      piece_scalar<P, COH>(s, b1, b1 + nvec * L, scale);
-    }
-  }
-  piece_scalar<P, COH>(s, b1 + nvec * L, base + len, scale);
-}
-
-template <class P, int CAP>
-__global__ void __launch_bounds__(kThreads, 5) relay_chain_kernel(const __grid_constant__ ChainArgs<CAP> a) {
-  const int t = blockIdx.x;
-  // the last group whose first task is <= t (uniform across the CTA)
-  int lo = 0, hi = a.ngroup - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (a.seg[a.gfirst[mid]].tile0 <= t) lo = mid; else hi = mid - 1;
-  }
-  const int f = a.gfirst[lo], l = a.gfirst[lo + 1];
-  const int64_t base = (int64_t)(t - a.seg[f].tile0) * a.tile;
-  const int64_t len = min((int64_t)a.tile, a.seg[f].n - base);
-  int lvl = a.level[f];
-  for (int i = f; i < l; ++i) {
-    if (a.level[i] != lvl) {
-      // the previous pass's stores of this tile are visible to the whole CTA after this
-      __syncthreads();
-      lvl = a.level[i];
-    }
-    // the first pass reads only memory written before the launch; later passes read what
-    // this CTA has just written, through L2
-    if (lvl == a.level[f]) run_piece<P, false>(a.seg[i], base, len, a.scale);
-    else run_piece<P, true>(a.seg[i], base, len, a.scale);
-  }
-}
-
 // ------------------------------------------------------------------- host side --
 
 // Split segments so that as much as possible takes a 16-byte path. When every pointer
@@ -1251,16 +857,6 @@ void split_for_alignment(const std::vector<Seg>& in, int E, std::vector<Seg>* ou
   }
 }
 
-int sm_count() {
-  static int cached[kMaxDevices] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
-  if (dev >= 0 && dev < kMaxDevices && cached[dev] > 0) return cached[dev];
-  int n = 1;
-  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-  if (dev >= 0 && dev < kMaxDevices) cached[dev] = n;
-  return n;
-}
 
 template <class P, int CAP, int MODE>
 cudaError_t launch_cap(const Seg* segs, int nseg, float scale, cudaStream_t stream,
@@ -1382,6 +978,17 @@ cudaError_t launch_fused_typed(FusedArgs& a, cudaStream_t stream, bool* ok) {
 
 }  // namespace
 
+int sm_count() {
+  static int cached[kMaxDevices] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (dev >= 0 && dev < kMaxDevices && cached[dev] > 0) return cached[dev];
+  int n = 1;
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  if (dev >= 0 && dev < kMaxDevices) cached[dev] = n;
+  return n;
+}
+
 bool launch_fused(int dtype, const std::vector<Pass>& passes, float scale, cudaStream_t stream,
                   cudaError_t* err, bool forced) {
   *err = cudaSuccess;
@@ -1416,71 +1023,6 @@ bool launch_fused(int dtype, const std::vector<Pass>& passes, float scale, cudaS
     default: *err = launch_fused_typed<TI32>(a, stream, &ok); break;
   }
   return ok;
-}
-
-namespace {
-
-template <class P, int CAP>
-cudaError_t launch_chain_cap(const ChainPlan& c, float scale, int64_t tile, cudaStream_t stream,
-                             int* ntask_out) {
-  static thread_local ChainArgs<CAP> a;  // up to ~31 KiB: keep it off the stack
-  const int G = (int)c.gn.size();
-  int64_t tasks = 0;
-  for (int g = 0; g < G; ++g) {
-    a.gfirst[g] = (int16_t)c.gfirst[g];
-    for (int i = c.gfirst[g]; i < c.gfirst[g + 1]; ++i) {
-      a.seg[i] = c.segs[i];
-      a.seg[i].tile0 = (int32_t)tasks;
-      a.level[i] = c.level[i];
-    }
-    tasks += (c.gn[g] + tile - 1) / tile;
-  }
-  a.gfirst[G] = (int16_t)c.gfirst[G];
-  a.ngroup = G;
-  a.ntask = (int32_t)tasks;
-  a.scale = scale;
-  a.tile = (int32_t)tile;
-  *ntask_out = (int)tasks;
-  relay_chain_kernel<P, CAP><<<(unsigned)tasks, kThreads, 0, stream>>>(a);
-  return cudaGetLastError();
-}
-
-template <class P>
-cudaError_t launch_chain_typed(const ChainPlan& c, float scale, int64_t tile, cudaStream_t stream,
-                               int* ntask) {
-  const size_t n = c.segs.size();
-  if (n <= 32) return launch_chain_cap<P, 32>(c, scale, tile, stream, ntask);
-  if (n <= 128) return launch_chain_cap<P, 128>(c, scale, tile, stream, ntask);
-  return launch_chain_cap<P, kChainMaxPieces>(c, scale, tile, stream, ntask);
-}
-
-}  // namespace
-
-// Tiles of 16 KiB, halved (down to 4 KiB, one 16-byte vector per thread) while the call
-// has fewer tasks than twice the SMs: in the latency-bound regime more, smaller tasks
-// spread the same bytes over more SMs.
-bool launch_chain(int dtype, const ChainPlan& c, float scale, cudaStream_t stream,
-                  cudaError_t* err) {
-  *err = cudaSuccess;
-  if (c.segs.empty() || c.segs.size() > (size_t)kChainMaxPieces) return false;
-  const int E = esize_of(dtype);
-  int64_t tile_bytes = kTileBytes;
-  auto tasks = [&](int64_t tb) {
-    int64_t t = 0;
-    for (int64_t n : c.gn) t += (n + tb / E - 1) / (tb / E);
-    return t;
-  };
-  while (tile_bytes > (int64_t)kThreads * kVecBytes && tasks(tile_bytes) < 2 * sm_count())
-    tile_bytes /= 2;
-  if (tasks(tile_bytes) > INT32_MAX) return false;
-  const int64_t tile = tile_bytes / E;
-  int ntask = 0;
-  switch (dtype) {
-    case RELAY_F32: *err = launch_chain_typed<TF32>(c, scale, tile, stream, &ntask); break;
-    case RELAY_BF16: *err = launch_chain_typed<TBF16>(c, scale, tile, stream, &ntask); break;
-    default: *err = launch_chain_typed<TI32>(c, scale, tile, stream, &ntask); break;
-  }
-  return true;
 }
 
 namespace {

@@ -158,7 +158,7 @@ bool launch_fused(int dtype, const std::vector<Pass>& passes, float scale, cudaS
 // another. The passes' segments are cut into pieces so that every dependency between
 // passes links identical element ranges, pieces that touch the same bytes (one writing)
 // form a group, and one CTA runs tile t of every piece of a group in pass order, with a
-// block barrier between passes -- chain.cpp (analysis), passes.cu (kernel).
+// block barrier between passes -- chain.cpp (analysis), chain_kernel.cu (kernel).
 constexpr int kChainMaxPieces = 384;
 struct ChainPlan {
   std::vector<Seg> segs;        // every group's pieces contiguous, in pass order
@@ -172,6 +172,9 @@ bool check_chain(const ChainPlan& c, int E, std::string* why);
 // launch's parameters.
 bool launch_chain(int dtype, const ChainPlan& c, float scale, cudaStream_t stream,
                   cudaError_t* err);
+
+// SMs of the current device (cached per device) -- passes.cu.
+int sm_count();
 
 // Record `msg` as this thread's last error and return `st` -- abi.cpp.
 relay_status_t report_error(relay_status_t st, const std::string& msg);

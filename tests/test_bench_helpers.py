@@ -10,9 +10,11 @@ import synth
 
 
 def test_kernel_code_sha_ignores_comments_and_host_code(tmp_path, monkeypatch):
-    src, hdr = tmp_path / "k.cu", tmp_path / "k.h"
+    src, hdr, dev = tmp_path / "k.cu", tmp_path / "k.h", tmp_path / "d.cuh"
     mark = bench.HOST_SIDE_MARK
     hdr.write_text("constexpr int kTile = 4;\n")
+    dev.write_text("__device__ int f() { return 1; }  // primitive\n")
+    monkeypatch.setattr(bench, "KERNEL_DEV", str(dev))
     src.write_text("// header\n__global__ void k(int* p) {\n  p[0] = 1;  // store\n}\n"
                    + mark + "\nvoid launch() { k<<<1, 1>>>(nullptr); }\n")
     monkeypatch.setattr(bench, "KERNEL_SRC", str(src))
@@ -27,6 +29,10 @@ def test_kernel_code_sha_ignores_comments_and_host_code(tmp_path, monkeypatch):
     assert bench.kernel_code_sha() == h0
     hdr.write_text("constexpr int kTile = 8;\n")
     assert bench.kernel_code_sha() != h0          # so does a change to the shared constants
+    hdr.write_text("constexpr int kTile = 4;\n")
+    assert bench.kernel_code_sha() == h0
+    dev.write_text("__device__ int f() { return 2; }\n")
+    assert bench.kernel_code_sha() != h0          # and to the shared device primitives
 
 
 def test_all_cores_split_gives_the_single_call_result():
