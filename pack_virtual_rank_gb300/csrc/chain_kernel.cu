@@ -63,31 +63,87 @@ __device__ __forceinline__ void piece_scalar(const Seg& s, int64_t b, int64_t e,
   }
 }
 
-// nvec 16-byte vectors from element b on, every pointer 16-byte aligned there. Loads of a
-// batch are issued together (4 vectors per thread per source, 2 past two sources).
+// Vector vi of every destination, byte offset `off` into each: kept in L2 when a later
+// pass of this CTA reads it, else streamed.
+__device__ __forceinline__ void store_dsts(const Seg& s, int64_t off, int vi, uint4 r, bool keep) {
+#pragma unroll
+  for (int d = 0; d < kMaxDst; ++d) {
+    if (d >= s.ndst) break;
+    uint4* q = reinterpret_cast<uint4*>(static_cast<char*>(s.dst[d]) + off) + vi;
+    if (keep) st_v4_keep(q, r);
+    else st_v4(q, r);
+  }
+}
+
+// A whole 16 KiB tile from element b on, every pointer 16-byte aligned there: each thread
+// takes kUnroll vectors (batches of 2 past two sources), no bounds to check.
 template <class P, int NSRC, bool COH>
-__device__ __forceinline__ void piece_vec(const Seg& s, int64_t b, int64_t nvec, float scale) {
+__device__ __forceinline__ void piece_full(const Seg& s, int64_t b, float scale) {
   constexpr int L = P::kLanes;
   constexpr int UB = NSRC <= 2 ? kUnroll : kUnroll / 2;
   using Acc = typename P::Acc;
   const bool do_scale = (s.flags & kFlagScale) != 0;
+  const bool keep = (s.flags & kFlagKeep) != 0;
+  const int64_t off = b * P::kE;
+  const int t = (int)threadIdx.x;
+#pragma unroll
+  for (int u0 = 0; u0 < kUnroll; u0 += UB) {
+    uint4 v[NSRC][UB];
+#pragma unroll
+    for (int u = 0; u < UB; ++u)
+#pragma unroll
+      for (int k = 0; k < NSRC; ++k)
+        v[k][u] = Mem<COH>::v4(reinterpret_cast<const uint4*>(static_cast<const char*>(s.src[k]) + off) +
+                               t + (u0 + u) * kThreads);
+#pragma unroll
+    for (int u = 0; u < UB; ++u) {
+      uint4 r = v[0][u];
+      if (s.op != kOpCopy) {
+        Acc acc[L], w[L];
+        P::unpack(v[0][u], acc);
+#pragma unroll
+        for (int k = 1; k < NSRC; ++k) {
+          P::unpack(v[k][u], w);
+#pragma unroll
+          for (int i = 0; i < L; ++i) acc[i] = P::add(acc[i], w[i]);
+        }
+        if (do_scale) {
+#pragma unroll
+          for (int i = 0; i < L; ++i) acc[i] = P::scale(acc[i], scale);
+        }
+        r = P::pack(acc);
+      }
+      store_dsts(s, off, t + (u0 + u) * kThreads, r, keep);
+    }
+  }
+}
+
+// nvec 16-byte vectors from element b on, every pointer 16-byte aligned there. Loads of a
+// batch are issued together (4 vectors per thread per source, 2 past two sources).
+template <class P, int NSRC, bool COH>
+__device__ __forceinline__ void piece_vec(const Seg& s, int64_t b, int nvec, float scale) {
+  constexpr int L = P::kLanes;
+  constexpr int UB = NSRC <= 2 ? kUnroll : kUnroll / 2;
+  using Acc = typename P::Acc;
+  const bool do_scale = (s.flags & kFlagScale) != 0;
+  const bool keep = (s.flags & kFlagKeep) != 0;
   const uint4* src[NSRC];
 #pragma unroll
   for (int k = 0; k < NSRC; ++k)
     src[k] = reinterpret_cast<const uint4*>(static_cast<const char*>(s.src[k]) + b * P::kE);
 #pragma unroll 1
-  for (int64_t v0 = threadIdx.x; v0 < nvec; v0 += (int64_t)kThreads * UB) {
+  for (int v0 = (int)threadIdx.x; v0 < nvec; v0 += kThreads * UB) {
     uint4 v[NSRC][UB];
 #pragma unroll
     for (int u = 0; u < UB; ++u) {
-      const int64_t vi = v0 + (int64_t)u * kThreads;
+      const int vi = v0 + u * kThreads;
 #pragma unroll
       for (int k = 0; k < NSRC; ++k)
         v[k][u] = vi < nvec ? Mem<COH>::v4(src[k] + vi) : make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll
     for (int u = 0; u < UB; ++u) {
-      const int64_t vi = v0 + (int64_t)u * kThreads;
+      const int vi = v0 + u * kThreads;
       if (vi >= nvec) continue;
       uint4 r = v[0][u];
       if (s.op != kOpCopy) {
@@ -105,11 +161,7 @@ __device__ __forceinline__ void piece_vec(const Seg& s, int64_t b, int64_t nvec,
         }
         r = P::pack(acc);
       }
-#pragma unroll 1
-      for (int d = 0; d < s.ndst; ++d) {
-        uint4* q = reinterpret_cast<uint4*>(static_cast<char*>(s.dst[d]) + b * P::kE) + vi;
-        if (s.flags & kFlagKeep) st_v4_keep(q, r); else st_v4(q, r);
-      }
+      store_dsts(s, b * P::kE, vi, r, keep);
     }
   }
 }
@@ -118,11 +170,12 @@ __device__ __forceinline__ void piece_vec(const Seg& s, int64_t b, int64_t nvec,
 // 16-byte grid: each vector of such a source is funnel-shifted out of the two aligned
 // blocks it straddles (both hold bytes of the piece's own source range).
 template <class P, int NSRC, bool COH>
-__device__ __forceinline__ void piece_realign(const Seg& s, int64_t b, int64_t nvec, float scale) {
+__device__ __forceinline__ void piece_realign(const Seg& s, int64_t b, int nvec, float scale) {
   constexpr int L = P::kLanes;
   constexpr int UB = 2;
   using Acc = typename P::Acc;
   const bool do_scale = (s.flags & kFlagScale) != 0;
+  const bool keep = (s.flags & kFlagKeep) != 0;
   unsigned sig[NSRC];
   const uint4* a[NSRC];
 #pragma unroll
@@ -132,11 +185,11 @@ __device__ __forceinline__ void piece_realign(const Seg& s, int64_t b, int64_t n
     a[k] = reinterpret_cast<const uint4*>(p - sig[k]);
   }
 #pragma unroll 1
-  for (int64_t v0 = threadIdx.x; v0 < nvec; v0 += (int64_t)kThreads * UB) {
+  for (int v0 = (int)threadIdx.x; v0 < nvec; v0 += kThreads * UB) {
     uint4 v[NSRC][UB];
 #pragma unroll
     for (int u = 0; u < UB; ++u) {
-      const int64_t vi = v0 + (int64_t)u * kThreads;
+      const int vi = v0 + u * kThreads;
 #pragma unroll
       for (int k = 0; k < NSRC; ++k) {
         if (vi < nvec) {
@@ -149,7 +202,7 @@ __device__ __forceinline__ void piece_realign(const Seg& s, int64_t b, int64_t n
     }
 #pragma unroll
     for (int u = 0; u < UB; ++u) {
-      const int64_t vi = v0 + (int64_t)u * kThreads;
+      const int vi = v0 + u * kThreads;
       if (vi >= nvec) continue;
       uint4 r = v[0][u];
       if (s.op != kOpCopy) {
@@ -167,11 +220,7 @@ __device__ __forceinline__ void piece_realign(const Seg& s, int64_t b, int64_t n
         }
         r = P::pack(acc);
       }
-#pragma unroll 1
-      for (int d = 0; d < s.ndst; ++d) {
-        uint4* q = reinterpret_cast<uint4*>(static_cast<char*>(s.dst[d]) + b * P::kE) + vi;
-        if (s.flags & kFlagKeep) st_v4_keep(q, r); else st_v4(q, r);
-      }
+      store_dsts(s, b * P::kE, vi, r, keep);
     }
   }
 }
@@ -186,6 +235,19 @@ __device__ __noinline__ void run_piece(const Seg& s, int64_t base, int64_t len, 
   const unsigned md = mis(s.dst[0]);
   bool dsame = md % E == 0;
   for (int d = 1; d < s.ndst; ++d) dsame &= mis(s.dst[d]) == md;
+  if (dsame && md == 0 && len * E == kTileBytes) {
+    bool sal = true;
+    for (int k = 0; k < s.nsrc; ++k) sal &= mis(s.src[k]) == 0;
+    if (sal) {
+      switch (s.op == kOpCopy ? 1 : s.nsrc) {
+        case 1: piece_full<P, 1, COH>(s, base, scale); break;
+        case 2: piece_full<P, 2, COH>(s, base, scale); break;
+        case 3: piece_full<P, 3, COH>(s, base, scale); break;
+        default: piece_full<P, 4, COH>(s, base, scale); break;
+      }
+      return;
+    }
+  }
   if (!dsame) {
     piece_scalar<P, COH>(s, base, base + len, scale);
     return;
@@ -193,7 +255,7 @@ __device__ __noinline__ void run_piece(const Seg& s, int64_t base, int64_t len, 
   const int64_t head = min((int64_t)(((16u - md) & 15u) / E), len);
   piece_scalar<P, COH>(s, base, base + head, scale);
   const int64_t b1 = base + head;
-  const int64_t nvec = (len - head) / L;
+  const int nvec = (int)((len - head) / L);
   if (nvec > 0) {
     bool sal = true;
     for (int k = 0; k < s.nsrc; ++k)
