@@ -89,8 +89,8 @@ typedef enum {
  * between passes links identical element ranges; pieces that touch the same bytes, one of
  * them writing, form a group; one CTA runs tile t of every piece of a group in pass order
  * with a block barrier between passes. No CTA waits for another, and a consumer reads
- * from L2 what its own CTA just wrote. It takes programs without mixed-width (fp32
- * partial) segments whose pieces number at most 384 after cutting; past
+ * from L2 what its own CTA just wrote. It takes programs whose pieces number at most 384
+ * after cutting (fp32 partials of a bf16 payload included); past
  * RELAY_FUSED_MAX_BYTES of pass traffic, every such program but the coalesced 4-active
  * all-to-all (its pack, forward and unpack chains of single copies run faster pass by
  * pass; the others gain 4-25% from reading their producers' output from L2). Else a

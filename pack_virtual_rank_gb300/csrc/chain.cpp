@@ -34,20 +34,27 @@ struct Operand {
   uintptr_t lo, hi;  // bytes [lo, hi)
   int piece;
   bool write;
+  int width;         // bytes per element of this operand (an fp32 partial next to bf16: 4)
 };
+
+// Bytes per element of a segment's source k / destinations (program.h: mixed-width
+// segments carry an fp32 partial next to the payload type).
+int src_width(const Seg& s, int k, int E) { return (k == 1 && (s.flags & kFlagSrc1F32)) ? 4 : E; }
+int dst_width(const Seg& s, int E) { return (s.flags & kFlagOutF32) ? 4 : E; }
 
 void operands(const std::vector<Piece>& ps, int E, std::vector<Operand>* out) {
   out->clear();
   for (int i = 0; i < (int)ps.size(); ++i) {
     const Seg& s = ps[i].s;
-    const uintptr_t bytes = (uintptr_t)s.n * (uintptr_t)E;
     for (int k = 0; k < s.nsrc; ++k) {
+      const int w = src_width(s, k, E);
       const uintptr_t lo = reinterpret_cast<uintptr_t>(s.src[k]);
-      out->push_back(Operand{lo, lo + bytes, i, false});
+      out->push_back(Operand{lo, lo + (uintptr_t)s.n * (uintptr_t)w, i, false, w});
     }
+    const int w = dst_width(s, E);
     for (int d = 0; d < s.ndst; ++d) {
       const uintptr_t lo = reinterpret_cast<uintptr_t>(s.dst[d]);
-      out->push_back(Operand{lo, lo + bytes, i, true});
+      out->push_back(Operand{lo, lo + (uintptr_t)s.n * (uintptr_t)w, i, true, w});
     }
   }
   std::sort(out->begin(), out->end(), [](const Operand& a, const Operand& b) {
@@ -75,8 +82,8 @@ int find(std::vector<int>& parent, int x) {
 
 Seg advance(const Seg& s, int64_t e, int64_t n, int E) {
   Seg t = s;
-  for (int k = 0; k < t.nsrc; ++k) t.src[k] = static_cast<const char*>(t.src[k]) + e * E;
-  for (int d = 0; d < t.ndst; ++d) t.dst[d] = static_cast<char*>(t.dst[d]) + e * E;
+  for (int k = 0; k < t.nsrc; ++k) t.src[k] = static_cast<const char*>(t.src[k]) + e * src_width(s, k, E);
+  for (int d = 0; d < t.ndst; ++d) t.dst[d] = static_cast<char*>(t.dst[d]) + e * dst_width(s, E);
   t.n = n;
   return t;
 }
@@ -93,7 +100,9 @@ bool build_chain(const std::vector<Pass>& passes, int E, ChainPlan* out, std::st
   for (size_t p = 0; p < passes.size(); ++p)
     for (const Seg& s : passes[p].segs) {
       if (s.n <= 0) continue;
-      if (seg_mixed(s)) return fail("mixed-width segments");
+      // only bf16 payloads widen, and every fp32 operand must be 4-byte aligned
+      if (seg_mixed(s) && (E != 2 || !seg_operands_aligned(s, E)))
+        return fail("mixed-width segment on a payload other than bf16, or misaligned");
       ps.push_back(Piece{s, (int)p, (int)ps.size()});
     }
   if (ps.empty()) return fail("nothing to run");
@@ -107,12 +116,14 @@ bool build_chain(const std::vector<Pass>& passes, int E, ChainPlan* out, std::st
     bool bad = false;
     for_each_conflict(ops, [&](const Operand& a, const Operand& b) {
       if (ps[a.piece].pass == ps[b.piece].pass) bad = true;  // a race inside one pass
+      if (a.width != b.width) bad = true;                    // not element for element
       if (a.lo == b.lo && a.hi == b.hi) return;
       const uintptr_t lo = std::max(a.lo, b.lo), hi = std::min(a.hi, b.hi);
       for (const Operand* x : {&a, &b}) {
-        if ((lo - x->lo) % E || (hi - x->lo) % E) bad = true;
-        if (x->lo < lo) cuts[x->piece].push_back((int64_t)((lo - x->lo) / E));
-        if (x->hi > hi) cuts[x->piece].push_back((int64_t)((hi - x->lo) / E));
+        const uintptr_t w = (uintptr_t)x->width;
+        if ((lo - x->lo) % w || (hi - x->lo) % w) bad = true;
+        if (x->lo < lo) cuts[x->piece].push_back((int64_t)((lo - x->lo) / w));
+        if (x->hi > hi) cuts[x->piece].push_back((int64_t)((hi - x->lo) / w));
       }
     });
     if (bad) return fail("overlap that is not elementwise");
@@ -187,9 +198,9 @@ bool check_chain(const ChainPlan& c, int E, std::string* why) {
         return false;
       }
     }
-  auto rng = [&](const void* p, int64_t n) {
+  auto rng = [&](const void* p, int64_t bytes) {
     const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
-    return std::make_pair(lo, lo + (uintptr_t)(n * E));
+    return std::make_pair(lo, lo + (uintptr_t)bytes);
   };
   auto ov = [](std::pair<uintptr_t, uintptr_t> a, std::pair<uintptr_t, uintptr_t> b) {
     return a.first < b.second && b.first < a.second;
@@ -201,10 +212,10 @@ bool check_chain(const ChainPlan& c, int E, std::string* why) {
       if (same_group && c.level[i] != c.level[j]) continue;  // ordered by the block barrier
       const Seg &a = c.segs[i], &b = c.segs[j];
       for (int d = 0; d < a.ndst; ++d) {
-        const auto w = rng(a.dst[d], a.n);
+        const auto w = rng(a.dst[d], seg_dst_bytes(a, E));
         bool hit = false;
-        for (int k = 0; k < b.nsrc; ++k) hit |= ov(w, rng(b.src[k], b.n));
-        for (int k = 0; k < b.ndst; ++k) hit |= ov(w, rng(b.dst[k], b.n));
+        for (int k = 0; k < b.nsrc; ++k) hit |= ov(w, rng(b.src[k], seg_src_bytes(b, k, E)));
+        for (int k = 0; k < b.ndst; ++k) hit |= ov(w, rng(b.dst[k], seg_dst_bytes(b, E)));
         if (hit) {
           *why = "chained pieces " + std::to_string(i) + " and " + std::to_string(j) +
                  (same_group ? " of one pass of a group" : " of different groups") +

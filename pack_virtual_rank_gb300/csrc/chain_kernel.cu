@@ -225,6 +225,86 @@ __device__ __forceinline__ void piece_realign(const Seg& s, int64_t b, int nvec,
   }
 }
 
+// A mixed-width piece of a bf16 payload: the helper summing its bf16 slots into an fp32
+// partial (kFlagOutF32), or an owner adding its own bf16 value and the fp32 partial,
+// scaled once and rounded to bf16 (kFlagSrc1F32). 8 elements per step (one 16-byte bf16
+// vector, two fp32 vectors) when every operand is 16-byte aligned at `base`, else one
+// element at a time.
+template <bool COH>
+__device__ __noinline__ void piece_mixed(const Seg& s, int64_t base, int64_t len, float scale) {
+  const bool out_f32 = (s.flags & kFlagOutF32) != 0;
+  const bool src1_f32 = (s.flags & kFlagSrc1F32) != 0;
+  const bool do_scale = (s.flags & kFlagScale) != 0;
+  const bool keep = (s.flags & kFlagKeep) != 0;
+  auto sw = [&](int k) { return (k == 1 && src1_f32) ? 4 : 2; };
+  const int dw = out_f32 ? 4 : 2;
+  bool al = true;
+  for (int k = 0; k < s.nsrc; ++k)
+    al &= ((reinterpret_cast<uintptr_t>(s.src[k]) + (uintptr_t)(base * sw(k))) & 15u) == 0;
+  for (int d = 0; d < s.ndst; ++d)
+    al &= ((reinterpret_cast<uintptr_t>(s.dst[d]) + (uintptr_t)(base * dw)) & 15u) == 0;
+  int64_t done = 0;
+  if (al) {
+    const int nvec = (int)(len / 8);
+#pragma unroll 1
+    for (int v = (int)threadIdx.x; v < nvec; v += kThreads) {
+      const int64_t e = base + 8 * (int64_t)v;
+      float acc[8], t[8];
+      TBF16::unpack(Mem<COH>::v4(static_cast<const char*>(s.src[0]) + e * 2), acc);
+#pragma unroll 1
+      for (int k = 1; k < s.nsrc; ++k) {
+        if (k == 1 && src1_f32) {
+          const char* q = static_cast<const char*>(s.src[1]) + e * 4;
+          const uint4 lo = Mem<COH>::v4(q), hi = Mem<COH>::v4(q + 16);
+          t[0] = __uint_as_float(lo.x); t[1] = __uint_as_float(lo.y);
+          t[2] = __uint_as_float(lo.z); t[3] = __uint_as_float(lo.w);
+          t[4] = __uint_as_float(hi.x); t[5] = __uint_as_float(hi.y);
+          t[6] = __uint_as_float(hi.z); t[7] = __uint_as_float(hi.w);
+        } else {
+          TBF16::unpack(Mem<COH>::v4(static_cast<const char*>(s.src[k]) + e * 2), t);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], t[i]);
+      }
+      if (do_scale) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = __fmul_rn(acc[i], scale);
+      }
+#pragma unroll 1
+      for (int d = 0; d < s.ndst; ++d) {
+        if (out_f32) {
+          char* q = static_cast<char*>(s.dst[d]) + e * 4;
+          const uint4 lo = make_uint4(__float_as_uint(acc[0]), __float_as_uint(acc[1]),
+                                      __float_as_uint(acc[2]), __float_as_uint(acc[3]));
+          const uint4 hi = make_uint4(__float_as_uint(acc[4]), __float_as_uint(acc[5]),
+                                      __float_as_uint(acc[6]), __float_as_uint(acc[7]));
+          if (keep) { st_v4_keep(q, lo); st_v4_keep(q + 16, hi); }
+          else { st_v4(q, lo); st_v4(q + 16, hi); }
+        } else {
+          char* q = static_cast<char*>(s.dst[d]) + e * 2;
+          if (keep) st_v4_keep(q, TBF16::pack(acc)); else st_v4(q, TBF16::pack(acc));
+        }
+      }
+    }
+    done = 8 * (int64_t)nvec;
+  }
+#pragma unroll 1
+  for (int64_t i = base + done + threadIdx.x; i < base + len; i += kThreads) {
+    float acc = TBF16::template load1<COH>(static_cast<const char*>(s.src[0]) + i * 2);
+#pragma unroll 1
+    for (int k = 1; k < s.nsrc; ++k)
+      acc = __fadd_rn(acc, (k == 1 && src1_f32)
+                               ? TF32::template load1<COH>(static_cast<const char*>(s.src[1]) + i * 4)
+                               : TBF16::template load1<COH>(static_cast<const char*>(s.src[k]) + i * 2));
+    if (do_scale) acc = __fmul_rn(acc, scale);
+#pragma unroll 1
+    for (int d = 0; d < s.ndst; ++d) {
+      if (out_f32) TF32::store1(static_cast<char*>(s.dst[d]) + i * 4, acc);
+      else TBF16::store1(static_cast<char*>(s.dst[d]) + i * 2, acc);
+    }
+  }
+}
+
 // Elements [base, base + len) of segment s, whatever the alignment of its pointers there.
 template <class P, bool COH>
 __device__ __noinline__ void run_piece(const Seg& s, int64_t base, int64_t len, float scale) {
@@ -298,9 +378,17 @@ __global__ void __launch_bounds__(kThreads, 5) relay_chain_kernel(const __grid_c
       lvl = a.level[i];
     }
     // the first pass reads only memory written before the launch; later passes read what
-    // this CTA has just written, through L2
-    if (lvl == a.level[f]) run_piece<P, false>(a.seg[i], base, len, a.scale);
-    else run_piece<P, true>(a.seg[i], base, len, a.scale);
+    // this CTA has just written, through L2. fp32 partials exist only next to a bf16
+    // payload (the host refuses anything else).
+    const bool first = lvl == a.level[f];
+    if (P::kE == 2 && seg_mixed(a.seg[i])) {
+      if (first) piece_mixed<false>(a.seg[i], base, len, a.scale);
+      else piece_mixed<true>(a.seg[i], base, len, a.scale);
+    } else if (first) {
+      run_piece<P, false>(a.seg[i], base, len, a.scale);
+    } else {
+      run_piece<P, true>(a.seg[i], base, len, a.scale);
+    }
   }
 }
 

@@ -536,7 +536,7 @@ def _dry_call(coll, count, dt, A, R, sched, in_place, skew, flags=0):
 @pytest.mark.parametrize("coll", range(4))
 def test_chained_programs_are_race_free(coll):
     """Every small call, on every schedule, in-place form and buffer skew: the chained
-    launch's analysis takes the program (mixed-width ones excepted), and its independent
+    launch's analysis takes the program (mixed-width fp32 partials included), and its independent
     re-check finds no two CTAs touching the same bytes with one writing, and no race
     inside one pass of a group."""
     n = 0
@@ -558,7 +558,7 @@ def test_chained_programs_are_race_free(coll):
                                 st, how = _dry_call(coll, count, dt, A, R, sched, in_place, skew)
                                 assert st == rv.OK, rv.lib().relay_last_error()
                                 single = len(rv.relay_plan_passes(p, in_place)) < 2
-                                if p.wide_partial or single:
+                                if single:
                                     assert how == "dry run"
                                 else:
                                     assert how.startswith("chained"), (coll, A, R, count, sched)

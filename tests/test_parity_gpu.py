@@ -271,24 +271,29 @@ def test_one_launch_at_sizes_past_its_default(coll, form):
     """The one-launch forms forced on calls of many tiles per pass (cooperative: grid
     barriers between passes; chained: every dependency inside one CTA; both load
     through L2 what the launch wrote) match the oracle like the per-pass path."""
+    # the cooperative kernel has no mixed-width path: the fp32 partial only chained
+    partials = (rv.FLAG_PAYLOAD_PARTIAL, 0) if form == rv.FLAG_CHAINED else (rv.FLAG_PAYLOAD_PARTIAL,)
     for A in (2, 4):
         for count in (3 << 20, (1 << 21) + 129):
             scale = _scale(coll, A, rv.BF16)
             for in_place in (False, True):
                 if in_place and coll == rv.ALL_TO_ALL:
                     continue
-                c = hz.run(coll, A, 8, count, rv.BF16, scale, config=17, in_place=in_place,
-                           schedule=rv.SCHEDULE_RELAY, flags=form | rv.FLAG_PAYLOAD_PARTIAL)
-                want = "chained" if form == rv.FLAG_CHAINED else "cooperative"
-                assert c.launch.startswith(want), c.launch
-                hz.check_all(c)
+                for partial in partials:
+                    if partial == 0 and not (coll == rv.REDUCE_SCATTER and A == 4):
+                        continue
+                    c = hz.run(coll, A, 8, count, rv.BF16, scale, config=17, in_place=in_place,
+                               schedule=rv.SCHEDULE_RELAY, flags=form | partial)
+                    want = "chained" if form == rv.FLAG_CHAINED else "cooperative"
+                    assert c.launch.startswith(want), c.launch
+                    hz.check_all(c)
 
 
 def test_default_launch_forms():
-    """Small calls run chained by default; pass events, RELAY_FLAG_SEPARATE_PASSES and
-    mixed-width programs (a bf16 4-active reduce-scatter's fp32 partial) run pass by
-    pass; RELAY_FLAG_FUSED_PASSES runs the cooperative launch; large calls run chained
-    when no group spans more than two passes, else pass by pass."""
+    """Small calls run chained by default, mixed-width programs (a bf16 4-active
+    reduce-scatter's fp32 partial) included; pass events and RELAY_FLAG_SEPARATE_PASSES run
+    pass by pass; RELAY_FLAG_FUSED_PASSES runs the cooperative launch; large calls run
+    chained except the coalesced all-to-all, which runs pass by pass."""
     c = hz.run(rv.ALLREDUCE, 2, 8, 65536, rv.F32, 0.5, config=1, schedule=rv.SCHEDULE_RELAY)
     assert c.launch == "chained: 10 groups, 26 pieces"
     hz.check_all(c)
@@ -303,7 +308,11 @@ def test_default_launch_forms():
                flags=rv.FLAG_FUSED_PASSES)
     assert c.launch == "cooperative"
     c = hz.run(rv.REDUCE_SCATTER, 4, 8, 40_000, rv.BF16, 0.25, schedule=rv.SCHEDULE_RELAY)
-    assert c.wide and c.launch == "passes"
+    assert c.wide and c.launch.startswith("chained")
+    hz.check_all(c)
+    c = hz.run(rv.REDUCE_SCATTER, 4, 8, 40_000, rv.BF16, 0.25, schedule=rv.SCHEDULE_RELAY,
+               flags=rv.FLAG_FUSED_PASSES)
+    assert c.wide and c.launch == "passes"          # no mixed-width path in that kernel
     hz.check_all(c)
     c = hz.run(rv.ALLREDUCE, 4, 8, 1 << 27, rv.BF16, 0.25)      # 1.9 GiB of pass traffic
     assert c.launch.startswith("chained")

@@ -1,10 +1,11 @@
 """GPU parity at the full sizes of the five workloads the throughput metric is quoted on.
 
 Outputs up to 16 MiB per rank are compared element by element with the oracle. So is one
-size of every collective that takes the per-pass launches (more than 256 MiB of pass
-traffic): the 1 GiB-per-rank allreduce the bench times, and 128-135 MB per rank of the
-others, including an all-to-all with an odd segmentCount. The remaining large points are
-compared on windows around every chunk, slice and direct-region boundary plus random
+large size of every collective (more than 256 MiB of pass traffic): the 1 GiB-per-rank
+allreduce the bench times, and 128-135 MB per rank of the others, including an all-to-all
+with an odd segmentCount -- each under the library's default launch (chained, except the
+all-to-all) and again pass by pass, the form the bench times. The remaining large points
+are compared on windows around every chunk, slice and direct-region boundary plus random
 windows (the oracle computes each window from just the inputs it reads). Canaries and
 untouched inputs are checked in full everywhere.
 
@@ -40,13 +41,27 @@ def _check(c, full=False):
         hz.check_sampled(c)
         for g in c.bufs:
             assert g.guards_intact()
+    if full:
+        # the same call again, pass by pass, every element compared
+        args = c.rerun
+        del c
+        torch.cuda.empty_cache()
+        c = hz.run(*args[0], **dict(args[1], flags=rv.FLAG_SEPARATE_PASSES))
+        assert c.launch == "passes"
+        hz.check_full(c)
     del c
     torch.cuda.empty_cache()
 
 
-def _per_pass(c):
-    """The call took the per-pass launches: more than 256 MiB of pass traffic."""
+def _large(c):
+    """More than 256 MiB of pass traffic (past the small-call size)."""
     return sum(q["bytes_read"] + q["bytes_written"] for q in rv.relay_plan_passes(c.plan)) > 256 * MB
+
+
+def _run(*a, **kw):
+    c = hz.run(*a, **kw)
+    c.rerun = (a, kw)
+    return c
 
 
 def _big(nbytes):
@@ -54,7 +69,7 @@ def _big(nbytes):
 
 
 def test_allreduce_a2_fp32_65536_relay():
-    c = hz.run(rv.ALLREDUCE, 2, 8, 65536, rv.F32, 0.5, config=1, schedule=rv.SCHEDULE_RELAY)
+    c = _run(rv.ALLREDUCE, 2, 8, 65536, rv.F32, 0.5, config=1, schedule=rv.SCHEDULE_RELAY)
     p = c.plan
     assert (p.kind, p.chunk, p.dirA_size + p.dirB_size) == (rv.KIND_RELAY, 8192, 65536 // 4)
     t = rv.relay_plan_link_bytes(p)
@@ -65,12 +80,12 @@ def test_allreduce_a2_fp32_65536_relay():
 @pytest.mark.parametrize("nbytes", [64 * 1024 << k for k in range(15)])
 def test_allreduce_a2_bf16_sweep(nbytes):
     n = nbytes // 2
-    c = hz.run(rv.ALLREDUCE, 2, 8, n, rv.BF16, 0.5, config=2, gpu_generator=_big(nbytes))
+    c = _run(rv.ALLREDUCE, 2, 8, n, rv.BF16, 0.5, config=2, gpu_generator=_big(nbytes))
     assert c.plan.kind == (rv.KIND_RELAY if nbytes >= 2 * MB else rv.KIND_DIRECT)
     if nbytes < 2 * MB:
         assert c.plan.num_groups == 1
     full = nbytes == 1024 * MB          # the bench workload, whole
-    assert not full or _per_pass(c)
+    assert not full or _large(c)
     _check(c, full)
 
 
@@ -80,33 +95,33 @@ def test_reduce_scatter_a2_passthrough_sweep(nbytes, dtype):
     count = nbytes // 4
     m = count // 2
     scale = 0.5 if dtype == rv.F32 else 1.0
-    c = hz.run(rv.REDUCE_SCATTER, 2, 8, m, dtype, scale, config=3, gpu_generator=_big(nbytes))
+    c = _run(rv.REDUCE_SCATTER, 2, 8, m, dtype, scale, config=3, gpu_generator=_big(nbytes))
     assert c.plan.kind == rv.KIND_RELAY
     full = nbytes == 128 * MB
-    assert not full or _per_pass(c)
+    assert not full or _large(c)
     _check(c, full)
 
 
 @pytest.mark.parametrize("nbytes", [MB << k for k in range(11)])
 def test_allreduce_a4_bf16_sweep(nbytes):
     n = nbytes // 2
-    c = hz.run(rv.ALLREDUCE, 4, 8, n, rv.BF16, 0.25, config=4, gpu_generator=_big(nbytes))
+    c = _run(rv.ALLREDUCE, 4, 8, n, rv.BF16, 0.25, config=4, gpu_generator=_big(nbytes))
     assert c.plan.kind == (rv.KIND_RELAY if nbytes >= 2 * MB else rv.KIND_DIRECT)
     full = nbytes == 128 * MB
-    assert not full or _per_pass(c)
+    assert not full or _large(c)
     _check(c, full)
 
 
 @pytest.mark.parametrize("nbytes", [MB << k for k in range(11)])
 def test_reduce_scatter_a4_flat_sweep(nbytes):
     m = nbytes // 2 // 4
-    c = hz.run(rv.REDUCE_SCATTER, 4, 8, m, rv.BF16, 0.25, config=4, gpu_generator=_big(nbytes))
+    c = _run(rv.REDUCE_SCATTER, 4, 8, m, rv.BF16, 0.25, config=4, gpu_generator=_big(nbytes))
     assert c.plan.kind == (rv.KIND_RELAY if nbytes > 48 * MB else rv.KIND_DIRECT)
     if c.plan.kind == rv.KIND_RELAY:
         # item 6: the helper needs 1.5x recvCount, within the 2x recvCount contract
         assert c.plan.helper_elems * 2 == 3 * m
     full = nbytes == 128 * MB
-    assert not full or _per_pass(c)
+    assert not full or _large(c)
     _check(c, full)
 
 
@@ -117,12 +132,12 @@ AG_SIZES = [int(13.5 * MB), 27 * MB, 54 * MB, 108 * MB, 135 * MB, 256 * MB, 512 
 @pytest.mark.parametrize("dtype", [rv.BF16, rv.I32])
 def test_all_gather_a4_sweep(nbytes, dtype):
     S = nbytes // rv.ESIZE[dtype]
-    c = hz.run(rv.ALL_GATHER, 4, 8, S, dtype, config=5, schedule=rv.SCHEDULE_RELAY,
+    c = _run(rv.ALL_GATHER, 4, 8, S, dtype, config=5, schedule=rv.SCHEDULE_RELAY,
                gpu_generator=_big(nbytes))
     p = c.plan
     assert p.direct_g2 >= 3 * p.direct_g1     # direct region split 1:(A-1)
     full = nbytes == 135 * MB
-    assert not full or _per_pass(c)
+    assert not full or _large(c)
     _check(c, full)
 
 
@@ -131,12 +146,12 @@ def test_all_gather_a4_sweep(nbytes, dtype):
 def test_all_to_all_a4_coalesced_sweep(nbytes, dtype):
     count = nbytes // rv.ESIZE[dtype]
     seg = count // 12
-    c = hz.run(rv.ALL_TO_ALL, 4, 8, seg, dtype, config=5, schedule=rv.SCHEDULE_RELAY,
+    c = _run(rv.ALL_TO_ALL, 4, 8, seg, dtype, config=5, schedule=rv.SCHEDULE_RELAY,
                gpu_generator=_big(nbytes))
     assert [q["name"] for q in rv.relay_plan_passes(c.plan)] == ["pack", "helper_forward",
                                                                   "unpack"]
     full = nbytes == 135 * MB
-    assert not full or _per_pass(c)
+    assert not full or _large(c)
     _check(c, full)
 
 
@@ -146,7 +161,7 @@ def test_all_to_all_a4_odd_segment_count_full(dtype):
     off the 16-byte grid, so the pack and unpack copies realign their sources; compared
     element by element on the per-pass launches."""
     seg = 128 * MB // rv.ESIZE[dtype] // 4 + 1
-    c = hz.run(rv.ALL_TO_ALL, 4, 8, seg, dtype, config=5, schedule=rv.SCHEDULE_RELAY,
+    c = _run(rv.ALL_TO_ALL, 4, 8, seg, dtype, config=5, schedule=rv.SCHEDULE_RELAY,
                gpu_generator=True)
-    assert seg % 2 == 1 and _per_pass(c)
+    assert seg % 2 == 1 and _large(c)
     _check(c, True)
