@@ -1043,6 +1043,7 @@ def run_sweep(args):
         # the whole call under the library's default launch policy (one cooperative
         # launch for small calls), timed around the call
         whole = []
+        default_form = None
         if not args.graph:
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             for _ in range(reps):
@@ -1053,6 +1054,7 @@ def run_sweep(args):
                 e1.record()
                 torch.cuda.synchronize()
                 whole.append(e0.elapsed_time(e1))
+            default_form = rv.last_launch()
         # the same call replayed from a CUDA graph: device time only, without the host's
         # planning and launch work that the timing around a direct call includes
         whole_graph = []
@@ -1114,7 +1116,8 @@ def run_sweep(args):
                         "frac_call_default_policy_graph": round(tot_b / gm / 1e6 / peak, 3)})
         if whole:
             wm = statistics.median(whole)
-            row.update({"ms_call_default_policy": round(wm, 4),
+            row.update({"launch_default_policy": default_form,
+                        "ms_call_default_policy": round(wm, 4),
                         "gbs_call_default_policy": round(tot_b / wm / 1e6, 1),
                         "frac_call_default_policy": round(tot_b / wm / 1e6 / peak, 3)})
         # a row whose timed calls took less than 0.15 s repeats the same call (L2 flushed
