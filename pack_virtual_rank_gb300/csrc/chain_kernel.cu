@@ -33,10 +33,10 @@ struct ChainArgs {
 };
 
 // Elements [b, e) of a piece one at a time (copies move raw bits).
-template <class P, bool COH>
+template <class P, bool COH, bool COPY = false>
 __device__ __forceinline__ void piece_scalar(const Seg& s, int64_t b, int64_t e, float scale) {
   using Acc = typename P::Acc;
-  const bool copy = s.op == kOpCopy;
+  const bool copy = COPY || s.op == kOpCopy;
   const bool do_scale = (s.flags & kFlagScale) != 0;
 #pragma unroll 1
   for (int64_t i = b + threadIdx.x; i < e; i += kThreads) {
@@ -77,7 +77,7 @@ __device__ __forceinline__ void store_dsts(const Seg& s, int64_t off, int vi, ui
 
 // A whole 16 KiB tile from element b on, every pointer 16-byte aligned there: each thread
 // takes kUnroll vectors (batches of 2 past two sources), no bounds to check.
-template <class P, int NSRC, bool COH>
+template <class P, int NSRC, bool COH, bool COPY = false>
 __device__ __forceinline__ void piece_full(const Seg& s, int64_t b, float scale) {
   constexpr int L = P::kLanes;
   constexpr int UB = NSRC <= 2 ? kUnroll : kUnroll / 2;
@@ -98,7 +98,7 @@ __device__ __forceinline__ void piece_full(const Seg& s, int64_t b, float scale)
 #pragma unroll
     for (int u = 0; u < UB; ++u) {
       uint4 r = v[0][u];
-      if (s.op != kOpCopy) {
+      if (!COPY && s.op != kOpCopy) {
         Acc acc[L], w[L];
         P::unpack(v[0][u], acc);
 #pragma unroll
@@ -120,7 +120,7 @@ __device__ __forceinline__ void piece_full(const Seg& s, int64_t b, float scale)
 
 // nvec 16-byte vectors from element b on, every pointer 16-byte aligned there. Loads of a
 // batch are issued together (4 vectors per thread per source, 2 past two sources).
-template <class P, int NSRC, bool COH>
+template <class P, int NSRC, bool COH, bool COPY = false>
 __device__ __forceinline__ void piece_vec(const Seg& s, int64_t b, int nvec, float scale) {
   constexpr int L = P::kLanes;
   constexpr int UB = NSRC <= 2 ? kUnroll : kUnroll / 2;
@@ -146,7 +146,7 @@ __device__ __forceinline__ void piece_vec(const Seg& s, int64_t b, int nvec, flo
       const int vi = v0 + u * kThreads;
       if (vi >= nvec) continue;
       uint4 r = v[0][u];
-      if (s.op != kOpCopy) {
+      if (!COPY && s.op != kOpCopy) {
         Acc acc[L], t[L];
         P::unpack(v[0][u], acc);
 #pragma unroll
@@ -169,7 +169,7 @@ __device__ __forceinline__ void piece_vec(const Seg& s, int64_t b, int nvec, flo
 // The same with the destinations aligned at element b but one or two sources off the
 // 16-byte grid: each vector of such a source is funnel-shifted out of the two aligned
 // blocks it straddles (both hold bytes of the piece's own source range).
-template <class P, int NSRC, bool COH>
+template <class P, int NSRC, bool COH, bool COPY = false>
 __device__ __forceinline__ void piece_realign(const Seg& s, int64_t b, int nvec, float scale) {
   constexpr int L = P::kLanes;
   constexpr int UB = 2;
@@ -205,7 +205,7 @@ __device__ __forceinline__ void piece_realign(const Seg& s, int64_t b, int nvec,
       const int vi = v0 + u * kThreads;
       if (vi >= nvec) continue;
       uint4 r = v[0][u];
-      if (s.op != kOpCopy) {
+      if (!COPY && s.op != kOpCopy) {
         Acc acc[L], t[L];
         P::unpack(v[0][u], acc);
 #pragma unroll
@@ -306,60 +306,61 @@ __device__ __noinline__ void piece_mixed(const Seg& s, int64_t base, int64_t len
 }
 
 // Elements [base, base + len) of segment s, whatever the alignment of its pointers there.
-template <class P, bool COH>
+// COPY: the launch holds copies only (the reduction paths are compiled out).
+template <class P, bool COH, bool COPY>
 __device__ __noinline__ void run_piece(const Seg& s, int64_t base, int64_t len, float scale) {
   constexpr int E = P::kE, L = P::kLanes;
   auto mis = [&](const void* p) {
     return (unsigned)((reinterpret_cast<uintptr_t>(p) + (uintptr_t)(base * E)) & 15u);
   };
+  const int nsrc = COPY || s.op == kOpCopy ? 1 : s.nsrc;
   const unsigned md = mis(s.dst[0]);
   bool dsame = md % E == 0;
   for (int d = 1; d < s.ndst; ++d) dsame &= mis(s.dst[d]) == md;
   if (dsame && md == 0 && len * E == kTileBytes) {
     bool sal = true;
-    for (int k = 0; k < s.nsrc; ++k) sal &= mis(s.src[k]) == 0;
+    for (int k = 0; k < nsrc; ++k) sal &= mis(s.src[k]) == 0;
     if (sal) {
-      switch (s.op == kOpCopy ? 1 : s.nsrc) {
-        case 1: piece_full<P, 1, COH>(s, base, scale); break;
-        case 2: piece_full<P, 2, COH>(s, base, scale); break;
-        case 3: piece_full<P, 3, COH>(s, base, scale); break;
-        default: piece_full<P, 4, COH>(s, base, scale); break;
-      }
+      if (COPY || nsrc == 1) piece_full<P, 1, COH, COPY>(s, base, scale);
+      else if (nsrc == 2) piece_full<P, 2, COH>(s, base, scale);
+      else if (nsrc == 3) piece_full<P, 3, COH>(s, base, scale);
+      else piece_full<P, 4, COH>(s, base, scale);
       return;
     }
   }
   if (!dsame) {
-    piece_scalar<P, COH>(s, base, base + len, scale);
+    piece_scalar<P, COH, COPY>(s, base, base + len, scale);
     return;
   }
   const int64_t head = min((int64_t)(((16u - md) & 15u) / E), len);
-  piece_scalar<P, COH>(s, base, base + head, scale);
+  piece_scalar<P, COH, COPY>(s, base, base + head, scale);
   const int64_t b1 = base + head;
   const int nvec = (int)((len - head) / L);
   if (nvec > 0) {
     bool sal = true;
-    for (int k = 0; k < s.nsrc; ++k)
+    for (int k = 0; k < nsrc; ++k)
       sal &= ((reinterpret_cast<uintptr_t>(s.src[k]) + (uintptr_t)(b1 * E)) & 15u) == 0;
     if (sal) {
-      switch (s.op == kOpCopy ? 1 : s.nsrc) {
-        case 1: piece_vec<P, 1, COH>(s, b1, nvec, scale); break;
-        case 2: piece_vec<P, 2, COH>(s, b1, nvec, scale); break;
-        case 3: piece_vec<P, 3, COH>(s, b1, nvec, scale); break;
-        default: piece_vec<P, 4, COH>(s, b1, nvec, scale); break;
-      }
-    } else if (s.op == kOpCopy || s.nsrc == 1) {
-      piece_realign<P, 1, COH>(s, b1, nvec, scale);
-    } else if (s.nsrc == 2) {
+      if (COPY || nsrc == 1) piece_vec<P, 1, COH, COPY>(s, b1, nvec, scale);
+      else if (nsrc == 2) piece_vec<P, 2, COH>(s, b1, nvec, scale);
+      else if (nsrc == 3) piece_vec<P, 3, COH>(s, b1, nvec, scale);
+      else piece_vec<P, 4, COH>(s, b1, nvec, scale);
+    } else if (COPY || nsrc == 1) {
+      piece_realign<P, 1, COH, COPY>(s, b1, nvec, scale);
+    } else if (nsrc == 2) {
       piece_realign<P, 2, COH>(s, b1, nvec, scale);
     } else {
       piece_scalar<P, COH>(s, b1, b1 + nvec * L, scale);
     }
   }
-  piece_scalar<P, COH>(s, b1 + nvec * L, base + len, scale);
+  piece_scalar<P, COH, COPY>(s, b1 + nvec * L, base + len, scale);
 }
 
-template <class P, int CAP>
-__global__ void __launch_bounds__(kThreads, 5) relay_chain_kernel(const __grid_constant__ ChainArgs<CAP> a) {
+// COPY: every piece of the launch is a copy (the all-gather and all-to-all programs); that
+// instantiation needs fewer registers and runs 8 CTAs per SM instead of 5.
+template <class P, int CAP, bool COPY>
+__global__ void __launch_bounds__(kThreads, COPY ? 8 : 5)
+    relay_chain_kernel(const __grid_constant__ ChainArgs<CAP> a) {
   const int t = blockIdx.x;
   // the last group whose first task is <= t (uniform across the CTA)
   int lo = 0, hi = a.ngroup - 1;
@@ -381,20 +382,20 @@ __global__ void __launch_bounds__(kThreads, 5) relay_chain_kernel(const __grid_c
     // this CTA has just written, through L2. fp32 partials exist only next to a bf16
     // payload (the host refuses anything else).
     const bool first = lvl == a.level[f];
-    if (P::kE == 2 && seg_mixed(a.seg[i])) {
+    if (!COPY && P::kE == 2 && seg_mixed(a.seg[i])) {
       if (first) piece_mixed<false>(a.seg[i], base, len, a.scale);
       else piece_mixed<true>(a.seg[i], base, len, a.scale);
     } else if (first) {
-      run_piece<P, false>(a.seg[i], base, len, a.scale);
+      run_piece<P, false, COPY>(a.seg[i], base, len, a.scale);
     } else {
-      run_piece<P, true>(a.seg[i], base, len, a.scale);
+      run_piece<P, true, COPY>(a.seg[i], base, len, a.scale);
     }
   }
 }
 
 template <class P, int CAP>
 cudaError_t launch_chain_cap(const ChainPlan& c, float scale, int64_t tile, cudaStream_t stream,
-                             int* ntask_out) {
+                             int* ntask_out, bool copy_only) {
   static thread_local ChainArgs<CAP> a;  // up to ~31 KiB: keep it off the stack
   const int G = (int)c.gn.size();
   int64_t tasks = 0;
@@ -413,7 +414,8 @@ cudaError_t launch_chain_cap(const ChainPlan& c, float scale, int64_t tile, cuda
   a.scale = scale;
   a.tile = (int32_t)tile;
   *ntask_out = (int)tasks;
-  relay_chain_kernel<P, CAP><<<(unsigned)tasks, kThreads, 0, stream>>>(a);
+  if (copy_only) relay_chain_kernel<P, CAP, true><<<(unsigned)tasks, kThreads, 0, stream>>>(a);
+  else relay_chain_kernel<P, CAP, false><<<(unsigned)tasks, kThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
@@ -421,9 +423,11 @@ template <class P>
 cudaError_t launch_chain_typed(const ChainPlan& c, float scale, int64_t tile, cudaStream_t stream,
                                int* ntask) {
   const size_t n = c.segs.size();
-  if (n <= 32) return launch_chain_cap<P, 32>(c, scale, tile, stream, ntask);
-  if (n <= 128) return launch_chain_cap<P, 128>(c, scale, tile, stream, ntask);
-  return launch_chain_cap<P, kChainMaxPieces>(c, scale, tile, stream, ntask);
+  bool copy_only = true;
+  for (const Seg& sg : c.segs) copy_only &= sg.op == kOpCopy;
+  if (n <= 32) return launch_chain_cap<P, 32>(c, scale, tile, stream, ntask, copy_only);
+  if (n <= 128) return launch_chain_cap<P, 128>(c, scale, tile, stream, ntask, copy_only);
+  return launch_chain_cap<P, kChainMaxPieces>(c, scale, tile, stream, ntask, copy_only);
 }
 
 }  // namespace
