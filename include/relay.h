@@ -82,7 +82,8 @@ typedef enum {
 #define RELAY_FLAG_FUSED_PASSES 8  /* one cooperative launch for the whole call whenever it
                                       qualifies, whatever its size */
 #define RELAY_FLAG_CHAINED 32      /* one chained launch for the whole call whenever its
-                                      program allows it, whatever its size and depth */
+                                      program allows it (the default does the same; the flag
+                                      documents the intent) */
 /* Launch policy. A call that records pass events, or sets RELAY_FLAG_SEPARATE_PASSES,
  * launches each pass separately. Any other call runs as ONE chained launch where its
  * program allows: the segments of all passes are cut into pieces so that each dependency
@@ -90,11 +91,8 @@ typedef enum {
  * them writing, form a group; one CTA runs tile t of every piece of a group in pass order
  * with a block barrier between passes. No CTA waits for another, and a consumer reads
  * from L2 what its own CTA just wrote. It takes programs whose pieces number at most 384
- * after cutting (fp32 partials of a bf16 payload included); past
- * RELAY_FUSED_MAX_BYTES of pass traffic, every such program but the coalesced 4-active
- * all-to-all (its pack, forward and unpack chains of single copies run faster pass by
- * pass; the others gain 4-25% from reading their producers' output from L2). Else a
- * call of at most RELAY_FUSED_MAX_BYTES runs as one cooperative launch (at most 4 passes
+ * after cutting (fp32 partials of a bf16 payload included). Else a call of at most
+ * RELAY_FUSED_MAX_BYTES runs as one cooperative launch (at most 4 passes
  * and 384 segments after alignment splitting, no mixed-width segments; passes separated
  * by grid-wide barriers), and anything else pass by pass.
  * relay_last_launch() names the form the calling thread's last call took. */

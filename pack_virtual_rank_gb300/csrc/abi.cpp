@@ -234,9 +234,9 @@ relay_status_t execute(const std::vector<Pass>& passes, const std::vector<Range>
       if (find_hazard(ps, E, &why))
         return fail(RELAY_ERR_UNSUPPORTED, "internal (one-launch phase): " + why);
   }
-  // Launch policy. Pass events need the per-pass launches. Otherwise a call of at most
-  // RELAY_FUSED_MAX_BYTES of pass traffic (or any call, when forced) runs as one chained
-  // launch where its program allows it, else as one cooperative launch, else pass by pass.
+  // Launch policy. Pass events need the per-pass launches. Otherwise a call runs as one
+  // chained launch where its program allows it; else a call of at most
+  // RELAY_FUSED_MAX_BYTES of pass traffic runs as one cooperative launch; else pass by pass.
   const bool events_wanted = opts && opts->pass_events;
   const bool one_launch = !events_wanted && !(flags & RELAY_FLAG_SEPARATE_PASSES);
   int64_t bytes = 0;
@@ -250,19 +250,13 @@ relay_status_t execute(const std::vector<Pass>& passes, const std::vector<Range>
   const ChainPlan* chain = nullptr;
   bool chained = false;
   if (try_chain) {
-    // past the small-call size, not the coalesced all-to-all (its pack, forward and
-    // unpack chains of single copies ran faster pass by pass)
-    bool unpack = false;
-    for (const Pass& ps : passes) unpack |= ps.kind == RELAY_PASS_UNPACK;
-    if (small || (flags & RELAY_FLAG_CHAINED) || !unpack) {
-      ChainMemo& m = chain_for(passes, E);
-      chained = m.ok;
-      chain = &m.plan;
-      if (chained && (flags & RELAY_FLAG_CHECK_HAZARDS) && !m.checked) {
-        if (!check_chain(m.plan, E, &why))
-          return fail(RELAY_ERR_UNSUPPORTED, "internal (chained launch): " + why);
-        m.checked = true;
-      }
+    ChainMemo& m = chain_for(passes, E);
+    chained = m.ok;
+    chain = &m.plan;
+    if (chained && (flags & RELAY_FLAG_CHECK_HAZARDS) && !m.checked) {
+      if (!check_chain(m.plan, E, &why))
+        return fail(RELAY_ERR_UNSUPPORTED, "internal (chained launch): " + why);
+      m.checked = true;
     }
   }
   const std::string chain_desc =

@@ -3,8 +3,8 @@
 Outputs up to 16 MiB per rank are compared element by element with the oracle. So is one
 large size of every collective (more than 256 MiB of pass traffic): the 1 GiB-per-rank
 allreduce the bench times, and 128-135 MB per rank of the others, including an all-to-all
-with an odd segmentCount -- each under the library's default launch (chained, except the
-all-to-all) and again pass by pass, the form the bench times. The remaining large points
+with an odd segmentCount -- each under the library's default launch (chained) and again
+pass by pass, the form the bench times. The remaining large points
 are compared on windows around every chunk, slice and direct-region boundary plus random
 windows (the oracle computes each window from just the inputs it reads). Canaries and
 untouched inputs are checked in full everywhere.
