@@ -293,7 +293,7 @@ def test_default_launch_forms():
     """Small calls run chained by default, mixed-width programs (a bf16 4-active
     reduce-scatter's fp32 partial) included; pass events and RELAY_FLAG_SEPARATE_PASSES run
     pass by pass; RELAY_FLAG_FUSED_PASSES runs the cooperative launch; large calls run
-    chained except the coalesced all-to-all, which runs pass by pass."""
+    chained too, the coalesced all-to-all's three-pass chains of copies included."""
     c = hz.run(rv.ALLREDUCE, 2, 8, 65536, rv.F32, 0.5, config=1, schedule=rv.SCHEDULE_RELAY)
     assert c.launch == "chained: 10 groups, 26 pieces"
     hz.check_all(c)
@@ -318,7 +318,7 @@ def test_default_launch_forms():
     assert c.launch.startswith("chained")
     c = hz.run(rv.ALL_TO_ALL, 4, 8, (1 << 29) // 12, rv.BF16, schedule=rv.SCHEDULE_RELAY,
                gpu_generator=True)                              # 3-pass chains, 1.5 GB
-    assert c.launch == "passes"
+    assert c.launch.startswith("chained")
 
 
 @pytest.mark.parametrize("case", ["ar2", "a2a_odd"])
