@@ -306,10 +306,12 @@ __device__ __noinline__ void piece_mixed(const Seg& s, int64_t base, int64_t len
 }
 
 // Elements [base, base + len) of segment s, whatever the alignment of its pointers there.
-// COPY: the launch holds copies only (the reduction paths are compiled out).
-template <class P, bool COH, bool COPY>
+// MAXSRC: the most sources a reduction of the launch has (1: copies only); the paths for
+// more are compiled out.
+template <class P, bool COH, int MAXSRC>
 __device__ __noinline__ void run_piece(const Seg& s, int64_t base, int64_t len, float scale) {
   constexpr int E = P::kE, L = P::kLanes;
+  constexpr bool COPY = MAXSRC == 1;
   auto mis = [&](const void* p) {
     return (unsigned)((reinterpret_cast<uintptr_t>(p) + (uintptr_t)(base * E)) & 15u);
   };
@@ -322,9 +324,13 @@ __device__ __noinline__ void run_piece(const Seg& s, int64_t base, int64_t len, 
     for (int k = 0; k < nsrc; ++k) sal &= mis(s.src[k]) == 0;
     if (sal) {
       if (COPY || nsrc == 1) piece_full<P, 1, COH, COPY>(s, base, scale);
-      else if (nsrc == 2) piece_full<P, 2, COH>(s, base, scale);
-      else if (nsrc == 3) piece_full<P, 3, COH>(s, base, scale);
-      else piece_full<P, 4, COH>(s, base, scale);
+      else if constexpr (MAXSRC >= 2) {
+        if (nsrc == 2) piece_full<P, 2, COH>(s, base, scale);
+        else if constexpr (MAXSRC > 2) {
+          if (nsrc == 3) piece_full<P, 3, COH>(s, base, scale);
+          else piece_full<P, 4, COH>(s, base, scale);
+        }
+      }
       return;
     }
   }
@@ -342,13 +348,17 @@ __device__ __noinline__ void run_piece(const Seg& s, int64_t base, int64_t len, 
       sal &= ((reinterpret_cast<uintptr_t>(s.src[k]) + (uintptr_t)(b1 * E)) & 15u) == 0;
     if (sal) {
       if (COPY || nsrc == 1) piece_vec<P, 1, COH, COPY>(s, b1, nvec, scale);
-      else if (nsrc == 2) piece_vec<P, 2, COH>(s, b1, nvec, scale);
-      else if (nsrc == 3) piece_vec<P, 3, COH>(s, b1, nvec, scale);
-      else piece_vec<P, 4, COH>(s, b1, nvec, scale);
+      else if constexpr (MAXSRC >= 2) {
+        if (nsrc == 2) piece_vec<P, 2, COH>(s, b1, nvec, scale);
+        else if constexpr (MAXSRC > 2) {
+          if (nsrc == 3) piece_vec<P, 3, COH>(s, b1, nvec, scale);
+          else piece_vec<P, 4, COH>(s, b1, nvec, scale);
+        }
+      }
     } else if (COPY || nsrc == 1) {
       piece_realign<P, 1, COH, COPY>(s, b1, nvec, scale);
     } else if (nsrc == 2) {
-      piece_realign<P, 2, COH>(s, b1, nvec, scale);
+      if constexpr (MAXSRC >= 2) piece_realign<P, 2, COH>(s, b1, nvec, scale);
     } else {
       piece_scalar<P, COH>(s, b1, b1 + nvec * L, scale);
     }
@@ -356,10 +366,12 @@ __device__ __noinline__ void run_piece(const Seg& s, int64_t base, int64_t len, 
   piece_scalar<P, COH, COPY>(s, b1 + nvec * L, base + len, scale);
 }
 
-// COPY: every piece of the launch is a copy (the all-gather and all-to-all programs); that
-// instantiation needs fewer registers and runs 8 CTAs per SM instead of 5.
-template <class P, int CAP, bool COPY>
-__global__ void __launch_bounds__(kThreads, COPY ? 8 : 5)
+// MAXSRC: the most sources any reduction of the launch has, 4 for any program (fp32
+// partials included). Programs of copies only (all-gather, all-to-all) take MAXSRC = 1 and
+// run 8 CTAs per SM at 32 registers; those whose reductions have at most two sources (the
+// 2-active collectives) take MAXSRC = 2 and run 6; the rest run 5.
+template <class P, int CAP, int MAXSRC>
+__global__ void __launch_bounds__(kThreads, MAXSRC == 1 ? 8 : MAXSRC == 2 ? 6 : 5)
     relay_chain_kernel(const __grid_constant__ ChainArgs<CAP> a) {
   const int t = blockIdx.x;
   // the last group whose first task is <= t (uniform across the CTA)
@@ -382,20 +394,20 @@ __global__ void __launch_bounds__(kThreads, COPY ? 8 : 5)
     // this CTA has just written, through L2. fp32 partials exist only next to a bf16
     // payload (the host refuses anything else).
     const bool first = lvl == a.level[f];
-    if (!COPY && P::kE == 2 && seg_mixed(a.seg[i])) {
+    if (MAXSRC > 2 && P::kE == 2 && seg_mixed(a.seg[i])) {
       if (first) piece_mixed<false>(a.seg[i], base, len, a.scale);
       else piece_mixed<true>(a.seg[i], base, len, a.scale);
     } else if (first) {
-      run_piece<P, false, COPY>(a.seg[i], base, len, a.scale);
+      run_piece<P, false, MAXSRC>(a.seg[i], base, len, a.scale);
     } else {
-      run_piece<P, true, COPY>(a.seg[i], base, len, a.scale);
+      run_piece<P, true, MAXSRC>(a.seg[i], base, len, a.scale);
     }
   }
 }
 
 template <class P, int CAP>
 cudaError_t launch_chain_cap(const ChainPlan& c, float scale, int64_t tile, cudaStream_t stream,
-                             int* ntask_out, bool copy_only) {
+                             int* ntask_out, int max_src) {
   static thread_local ChainArgs<CAP> a;  // up to ~31 KiB: keep it off the stack
   const int G = (int)c.gn.size();
   int64_t tasks = 0;
@@ -414,8 +426,9 @@ cudaError_t launch_chain_cap(const ChainPlan& c, float scale, int64_t tile, cuda
   a.scale = scale;
   a.tile = (int32_t)tile;
   *ntask_out = (int)tasks;
-  if (copy_only) relay_chain_kernel<P, CAP, true><<<(unsigned)tasks, kThreads, 0, stream>>>(a);
-  else relay_chain_kernel<P, CAP, false><<<(unsigned)tasks, kThreads, 0, stream>>>(a);
+  if (max_src == 1) relay_chain_kernel<P, CAP, 1><<<(unsigned)tasks, kThreads, 0, stream>>>(a);
+  else if (max_src == 2) relay_chain_kernel<P, CAP, 2><<<(unsigned)tasks, kThreads, 0, stream>>>(a);
+  else relay_chain_kernel<P, CAP, 4><<<(unsigned)tasks, kThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
@@ -423,11 +436,12 @@ template <class P>
 cudaError_t launch_chain_typed(const ChainPlan& c, float scale, int64_t tile, cudaStream_t stream,
                                int* ntask) {
   const size_t n = c.segs.size();
-  bool copy_only = true;
-  for (const Seg& sg : c.segs) copy_only &= sg.op == kOpCopy;
-  if (n <= 32) return launch_chain_cap<P, 32>(c, scale, tile, stream, ntask, copy_only);
-  if (n <= 128) return launch_chain_cap<P, 128>(c, scale, tile, stream, ntask, copy_only);
-  return launch_chain_cap<P, kChainMaxPieces>(c, scale, tile, stream, ntask, copy_only);
+  int max_src = 1;
+  for (const Seg& sg : c.segs)
+    if (sg.op != kOpCopy) max_src = std::max<int>(max_src, seg_mixed(sg) ? kMaxSrc : sg.nsrc);
+  if (n <= 32) return launch_chain_cap<P, 32>(c, scale, tile, stream, ntask, max_src);
+  if (n <= 128) return launch_chain_cap<P, 128>(c, scale, tile, stream, ntask, max_src);
+  return launch_chain_cap<P, kChainMaxPieces>(c, scale, tile, stream, ntask, max_src);
 }
 
 }  // namespace
