@@ -513,6 +513,24 @@ def run_ours(args):
     default_ms = d0.elapsed_time(d1)
     default_clocks = clk_d.summary()
 
+    # and once more with every scratch line written back to memory (RELAY_FLAG_KEEP_SCRATCH):
+    # what dropping the chained launch's dead scratch lines from L2 saves
+    keep = rv.make_opts(flags=rv.FLAG_KEEP_SCRATCH)
+    for _ in range(args.warmup):
+        rv.relay_allreduce(send, recv, scratch, count, rv.BF16, A, R, SCALE, keep)
+    keep_form = rv.last_launch()
+    k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    with Clocks(local, enabled=not args.kernel_only) as clk_k:
+        barrier()
+        k0.record(stream)
+        for k in range(args.steps):
+            rv.relay_allreduce(send, recv, scratch, count, rv.BF16, A, R, SCALE, keep)
+        k1.record(stream)
+        barrier()
+    keep_ms = k0.elapsed_time(k1)
+    keep_clocks = clk_k.summary()
+
     # every other workload of the metric at one size, timed the same way with its own
     # clock record (rank 0 only: replicas add nothing to a per-collective table)
     per_wl = None
@@ -690,9 +708,17 @@ def run_ours(args):
                 "note": "the same steps without pass events, under the library's default launch "
                         "policy; the same algorithmic bytes per step. A chained launch runs each "
                         "tile's producer and consumer passes in one CTA, so the consumers' reads "
-                        "of what their producers just wrote are served from L2: DRAM traffic is "
-                        "below the algorithmic bytes and the fraction may exceed 1",
-                "clocks": default_clocks},
+                        "of what their producers just wrote are served from L2, and the scratch "
+                        "lines its last consumer has read are dropped from L2 unwritten: DRAM "
+                        "traffic is below the algorithmic bytes and the fraction may exceed 1",
+                "clocks": default_clocks,
+                "keep_scratch": {
+                    "launch": keep_form, "ms_per_step": round(keep_ms / args.steps, 4),
+                    "value": round(whole_job_gbs(nbytes, args.steps, world, keep_ms), 2),
+                    "frac": round(whole_job_gbs(nbytes, args.steps, world, keep_ms) / world / peak, 4),
+                    "note": "the same chained steps with RELAY_FLAG_KEEP_SCRATCH: every scratch "
+                            "line is written back to memory",
+                    "clocks": keep_clocks}},
         }
         if per_wl is not None:
             head = {"workload": "2: allreduce A=2 of R=8, bf16, 1 GiB per rank (the headline above)",

@@ -84,6 +84,11 @@ typedef enum {
 #define RELAY_FLAG_CHAINED 32      /* one chained launch for the whole call whenever its
                                       program allows it (the default does the same; the flag
                                       documents the intent) */
+#define RELAY_FLAG_KEEP_SCRATCH 64 /* chained launch: write every scratch line back to
+                                      memory. By default a CTA drops from L2, without a
+                                      write-back, the whole 128-byte lines of device-memory
+                                      scratch that an earlier pass of its chain wrote and that
+                                      nothing reads again in the call */
 /* Launch policy. A call that records pass events, or sets RELAY_FLAG_SEPARATE_PASSES,
  * launches each pass separately. Any other call runs as ONE chained launch where its
  * program allows: the segments of all passes are cut into pieces so that each dependency
@@ -236,6 +241,8 @@ int64_t relay_passthrough_helper_size(int64_t count_g, int A, int num_chunks);
  *   send/recv entries of helpers are ignored (may be NULL).
  * All device pointers; element-aligned; any further alignment is optional (16-byte
  * aligned buffers take the vectorized path).
+ * Scratch is workspace: every scratch byte a call reads it wrote earlier in the same call,
+ * and its contents after the call are unspecified (see RELAY_FLAG_KEEP_SCRATCH).
  * Aliasing: every buffer must be disjoint from every other except the in-place forms:
  *   allreduce      recv[a] == send[a]                          (D115998369)
  *   reduce-scatter recv[a] == send[a] + a*count elements       (D115998376)
@@ -382,7 +389,8 @@ relay_status_t relay_test_staged_wait(void* dst, const void* src, size_t count,
 /* Human-readable text of the last error this thread's calls produced. */
 const char* relay_last_error(void);
 /* How the calling thread's last collective call was launched: "chained: G groups, P
- * pieces", "cooperative" or "passes" (see the launch policy above); "dry run" for a
+ * pieces, D dropped" (D: scratch sources whose dead lines the launch drops from L2),
+ * "cooperative" or "passes" (see the launch policy above); "dry run" for a
  * RELAY_FLAG_DRY_RUN call that would not run chained, "none" before the first call. */
 const char* relay_last_launch(void);
 int relay_abi_version(void);

@@ -8,7 +8,7 @@ batched CUDA kernels (``csrc/``) behind the C ABI in ``include/relay.h``.
 """
 from ._binding import (  # noqa: F401
     ALL_GATHER, ALL_TO_ALL, ALLREDUCE, ERR_CUDA, ERR_INVALID_ARGUMENT, ERR_UNSUPPORTED, OK, BF16, COLLECTIVES, ESIZE, F32, FLAG_CHECK_HAZARDS, FLAG_DRY_RUN, FLAG_FUSED_PASSES, FLAG_SEPARATE_PASSES,
-    FLAG_PAYLOAD_PARTIAL, FLAG_CHAINED, I32, last_launch, device_status,
+    FLAG_PAYLOAD_PARTIAL, FLAG_CHAINED, FLAG_KEEP_SCRATCH, I32, last_launch, device_status,
     KIND_DIRECT, KIND_LEGACY, KIND_RELAY, KIND_ZERO_CHUNK, PASS_NAMES, REDUCE_SCATTER,
     SCHEDULE_AUTO, SCHEDULE_DIRECT, SCHEDULE_LEGACY, SCHEDULE_RELAY, LIB_PATH, RelayError,
     RelayOpts, RelayPassInfo, RelayPlan, alloc_scratch, dtype_code, lib, make_opts,

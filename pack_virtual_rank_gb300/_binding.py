@@ -27,6 +27,7 @@ FLAG_SEPARATE_PASSES = 4
 FLAG_FUSED_PASSES = 8
 FLAG_PAYLOAD_PARTIAL = 16
 FLAG_CHAINED = 32
+FLAG_KEEP_SCRATCH = 64
 ESIZE = {F32: 4, BF16: 2, I32: 4}
 PASS_NAMES = ("group1", "group2", "group3", "active_reduce", "pack", "helper_forward", "unpack")
 

@@ -56,6 +56,7 @@ struct FakeBuffers {
 struct Range {
   uintptr_t lo, hi;  // [lo, hi)
   std::string what;
+  bool scratch = false;  // a scratch buffer of the call (its contents afterwards: unspecified)
 };
 
 bool overlaps(const Range& a, const Range& b) { return a.lo < b.hi && b.lo < a.hi; }
@@ -159,6 +160,7 @@ relay_status_t validate_group(const relay_plan_t& p, void* const* send, void* co
     if (reinterpret_cast<uintptr_t>(scratch[l]) % E)
       return fail(RELAY_ERR_INVALID_ARGUMENT, name("scratch", l) + " not element-aligned");
     add(scratch[l], need, name("scratch", l));
+    ranges->back().scratch = true;
   }
   return RELAY_OK;
 }
@@ -177,6 +179,7 @@ relay_status_t check_disjoint(const std::vector<Range>& ranges) {
 // case) skips the analysis, which costs more host time than a small call's kernel.
 struct ChainMemo {
   std::vector<unsigned char> key;
+  std::vector<ByteRange> scratch;  // the scratch whose dead lines the plan drops
   ChainPlan plan;
   bool ok = false;
   bool checked = false;
@@ -185,7 +188,28 @@ struct ChainMemo {
 constexpr size_t kChainMemoSize = 8;
 thread_local std::vector<ChainMemo> g_chain_memo;
 
-ChainMemo& chain_for(const std::vector<Pass>& passes, int E) {
+// Scratch ranges whose dead lines the chained launch may drop: device memory only (the
+// collectives take device pointers; anything else keeps every line). A dry run launches
+// nothing and queries nothing: it takes every scratch buffer as device memory.
+std::vector<ByteRange> droppable(const std::vector<ByteRange>& scratch, bool dry) {
+  std::vector<ByteRange> out;
+  for (const ByteRange& r : scratch) {
+    if (!dry) {
+      cudaPointerAttributes at{};
+      if (cudaPointerGetAttributes(&at, reinterpret_cast<const void*>(r.lo)) != cudaSuccess) {
+        cudaGetLastError();
+        continue;
+      }
+      if (at.type != cudaMemoryTypeDevice) continue;
+    }
+    out.push_back(r);
+  }
+  return out;
+}
+
+// scratch: the call's scratch buffers (empty when every line is to be kept).
+ChainMemo& chain_for(const std::vector<Pass>& passes, int E, const std::vector<ByteRange>& scratch,
+                     bool dry) {
   thread_local std::vector<unsigned char> key;
   key.clear();
   auto put = [&](const void* p, size_t n) {
@@ -193,6 +217,10 @@ ChainMemo& chain_for(const std::vector<Pass>& passes, int E) {
     key.insert(key.end(), b, b + n);
   };
   put(&E, sizeof E);
+  put(&dry, sizeof dry);
+  const size_t ns = scratch.size();
+  put(&ns, sizeof ns);
+  if (ns) put(scratch.data(), ns * sizeof(ByteRange));
   for (const Pass& ps : passes) {
     const size_t n = ps.segs.size();
     put(&n, sizeof n);
@@ -211,7 +239,8 @@ ChainMemo& chain_for(const std::vector<Pass>& passes, int E) {
   g_chain_memo.emplace_back();
   ChainMemo& m = g_chain_memo.back();
   m.key = key;
-  m.ok = build_chain(passes, E, &m.plan, &m.why);
+  m.scratch = droppable(scratch, dry);
+  m.ok = build_chain(passes, E, m.scratch, &m.plan, &m.why);
   return m;
 }
 
@@ -250,19 +279,28 @@ relay_status_t execute(const std::vector<Pass>& passes, const std::vector<Range>
   const ChainPlan* chain = nullptr;
   bool chained = false;
   if (try_chain) {
-    ChainMemo& m = chain_for(passes, E);
+    std::vector<ByteRange> scratch;
+    if (!(flags & RELAY_FLAG_KEEP_SCRATCH))
+      for (const Range& r : ranges)
+        if (r.scratch) scratch.push_back(ByteRange{r.lo, r.hi});
+    ChainMemo& m = chain_for(passes, E, scratch, (flags & RELAY_FLAG_DRY_RUN) != 0);
     chained = m.ok;
     chain = &m.plan;
     if (chained && (flags & RELAY_FLAG_CHECK_HAZARDS) && !m.checked) {
-      if (!check_chain(m.plan, E, &why))
+      if (!check_chain(m.plan, E, m.scratch, &why))
         return fail(RELAY_ERR_UNSUPPORTED, "internal (chained launch): " + why);
       m.checked = true;
     }
   }
-  const std::string chain_desc =
-      chained ? "chained: " + std::to_string(chain->gn.size()) + " groups, " +
-                    std::to_string(chain->segs.size()) + " pieces"
-              : std::string();
+  std::string chain_desc;
+  if (chained) {
+    int dropped = 0;
+    for (uint8_t d : chain->drop)
+      for (unsigned m = d; m; m &= m - 1) ++dropped;
+    chain_desc = "chained: " + std::to_string(chain->gn.size()) + " groups, " +
+                 std::to_string(chain->segs.size()) + " pieces, " + std::to_string(dropped) +
+                 " dropped";
+  }
   if (flags & RELAY_FLAG_DRY_RUN) {
     g_last_launch = chained ? chain_desc : "dry run";
     return RELAY_OK;

@@ -80,6 +80,54 @@ int find(std::vector<int>& parent, int x) {
   return x;
 }
 
+ByteRange src_range(const Seg& s, int k, int E) {
+  const uintptr_t lo = reinterpret_cast<uintptr_t>(s.src[k]);
+  return ByteRange{lo, lo + (uintptr_t)s.n * (uintptr_t)src_width(s, k, E)};
+}
+ByteRange dst_range(const Seg& s, int d, int E) {
+  const uintptr_t lo = reinterpret_cast<uintptr_t>(s.dst[d]);
+  return ByteRange{lo, lo + (uintptr_t)s.n * (uintptr_t)dst_width(s, E)};
+}
+bool overlap(const ByteRange& a, const ByteRange& b) { return a.lo < b.hi && b.lo < a.hi; }
+bool same(const ByteRange& a, const ByteRange& b) { return a.lo == b.lo && a.hi == b.hi; }
+bool inside_any(const ByteRange& r, const std::vector<ByteRange>& v) {
+  for (const ByteRange& b : v)
+    if (r.lo >= b.lo && r.hi <= b.hi) return true;
+  return false;
+}
+// Sources a segment's kernel reads: a copy reads source 0 only.
+int sources_read(const Seg& s) { return s.op == kOpCopy ? 1 : s.nsrc; }
+
+// Bit k of drop[i]: source k of piece i lies in scratch, an earlier pass of the piece's
+// group wrote exactly those bytes, and nothing of the group touches them after this read
+// (nothing of another group touches them at all: a writer and its readers share a group).
+void mark_drops(ChainPlan* c, int E, const std::vector<ByteRange>& scratch) {
+  c->drop.assign(c->segs.size(), 0);
+  if (scratch.empty()) return;
+  for (size_t g = 0; g + 1 < c->gfirst.size(); ++g) {
+    const int f = c->gfirst[g], l = c->gfirst[g + 1];
+    for (int i = f; i < l; ++i) {
+      const Seg& s = c->segs[i];
+      for (int k = 0; k < sources_read(s); ++k) {
+        const ByteRange r = src_range(s, k, E);
+        if (!inside_any(r, scratch)) continue;
+        bool produced = false, live = false;
+        for (int j = f; j < l && !live; ++j) {
+          const Seg& t = c->segs[j];
+          for (int d = 0; d < t.ndst; ++d) {
+            const ByteRange w = dst_range(t, d, E);
+            if (c->level[j] < c->level[i]) produced |= same(w, r);
+            else live |= overlap(w, r);  // rewritten by this pass or a later one
+          }
+          if (c->level[j] > c->level[i])
+            for (int q = 0; q < sources_read(t); ++q) live |= overlap(src_range(t, q, E), r);
+        }
+        if (produced && !live) c->drop[i] |= (uint8_t)(1u << k);
+      }
+    }
+  }
+}
+
 Seg advance(const Seg& s, int64_t e, int64_t n, int E) {
   Seg t = s;
   for (int k = 0; k < t.nsrc; ++k) t.src[k] = static_cast<const char*>(t.src[k]) + e * src_width(s, k, E);
@@ -90,7 +138,8 @@ Seg advance(const Seg& s, int64_t e, int64_t n, int E) {
 
 }  // namespace
 
-bool build_chain(const std::vector<Pass>& passes, int E, ChainPlan* out, std::string* why) {
+bool build_chain(const std::vector<Pass>& passes, int E, const std::vector<ByteRange>& scratch,
+                 ChainPlan* out, std::string* why) {
   auto fail = [&](const std::string& m) {
     if (why) *why = m;
     return false;
@@ -177,14 +226,20 @@ bool build_chain(const std::vector<Pass>& passes, int E, ChainPlan* out, std::st
     }
   }
   out->gfirst.push_back((int32_t)out->segs.size());
+  mark_drops(out, E, scratch);
   return true;
 }
 
 // An independent re-check of a chained program (host hazard checks): no two pieces of
 // different groups touch the same bytes with either writing, and no two pieces of one
 // group's pass do. Quadratic in the pieces, so only run when the caller asks for checks.
-bool check_chain(const ChainPlan& c, int E, std::string* why) {
+bool check_chain(const ChainPlan& c, int E, const std::vector<ByteRange>& scratch,
+                 std::string* why) {
   const int G = (int)c.gn.size();
+  if (c.drop.size() != c.segs.size()) {
+    *why = "chained program without a drop mask per piece";
+    return false;
+  }
   std::vector<int> group(c.segs.size());
   for (int g = 0; g < G; ++g)
     for (int i = c.gfirst[g]; i < c.gfirst[g + 1]; ++i) {
@@ -223,6 +278,39 @@ bool check_chain(const ChainPlan& c, int E, std::string* why) {
           return false;
         }
       }
+    }
+  // A dropped source: scratch, written exactly by an earlier pass of its group, and touched
+  // by nothing after the read (no piece of another group, no later pass of its own group,
+  // no write in its own pass).
+  for (size_t i = 0; i < c.segs.size(); ++i)
+    for (int k = 0; k < 8; ++k) {
+      if (!((c.drop[i] >> k) & 1)) continue;
+      const Seg& a = c.segs[i];
+      auto bad = [&](const std::string& m) {
+        *why = "chained piece " + std::to_string(i) + " drops source " + std::to_string(k) + ": " + m;
+        return false;
+      };
+      if (k >= sources_read(a)) return bad("a source the piece does not read");
+      const auto r = rng(a.src[k], seg_src_bytes(a, k, E));
+      const ByteRange br{r.first, r.second};
+      if (!inside_any(br, scratch)) return bad("not inside a scratch buffer");
+      bool produced = false;
+      for (size_t j = 0; j < c.segs.size(); ++j) {
+        const Seg& b = c.segs[j];
+        const bool other = group[j] != group[i];
+        const bool later = !other && c.level[j] > c.level[i];
+        const bool earlier = !other && c.level[j] < c.level[i];
+        for (int d = 0; d < b.ndst; ++d) {
+          const auto w = rng(b.dst[d], seg_dst_bytes(b, E));
+          if (earlier) produced |= w == r;
+          else if (ov(w, r)) return bad("written again, or by another group");
+        }
+        if (other || later)
+          for (int q = 0; q < sources_read(b); ++q)
+            if (ov(rng(b.src[q], seg_src_bytes(b, q, E)), r))
+              return bad("read after the drop, or by another group");
+      }
+      if (!produced) return bad("no earlier pass of its group wrote exactly these bytes");
     }
   return true;
 }

@@ -30,7 +30,9 @@ struct ChainArgs {
   Seg seg[CAP];               // tile0: first task of the piece's group
   int16_t gfirst[CAP + 1];    // first piece of each group, then one past the last
   uint8_t level[CAP];         // pass of each piece
+  uint8_t drop[CAP];          // sources whose lines go dead after this piece (program.h)
 };
+static_assert(sizeof(ChainArgs<kChainMaxPieces>) <= 32764, "kernel parameter space");
 
 // Elements [b, e) of a piece one at a time (copies move raw bits).
 template <class P, bool COH, bool COPY = false>
@@ -305,6 +307,24 @@ __device__ __noinline__ void piece_mixed(const Seg& s, int64_t base, int64_t len
   }
 }
 
+// The whole 128-byte lines of this tile's part of each source in `mask`: scratch that no
+// later pass reads, dropped from L2 so that it is never written back to memory. Partial
+// lines at the ends may hold a neighbour's live bytes and stay.
+template <class P>
+__device__ __noinline__ void drop_lines(const Seg& s, unsigned mask, int64_t base, int64_t len) {
+#pragma unroll 1
+  for (int k = 0; k < kMaxSrc; ++k) {
+    if (!((mask >> k) & 1u)) continue;
+    const int64_t w = (k == 1 && (s.flags & kFlagSrc1F32)) ? 4 : P::kE;
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(s.src[k]) + (uintptr_t)(base * w);
+    const uintptr_t hi = lo + (uintptr_t)(len * w);
+    const uintptr_t first = (lo + 127) & ~(uintptr_t)127, last = hi & ~(uintptr_t)127;
+#pragma unroll 1
+    for (uintptr_t q = first + (uintptr_t)threadIdx.x * 128; q < last; q += (uintptr_t)kThreads * 128)
+      discard_l2(reinterpret_cast<const void*>(q));
+  }
+}
+
 // Elements [base, base + len) of segment s, whatever the alignment of its pointers there.
 // MAXSRC: the most sources a reduction of the launch has (1: copies only); the paths for
 // more are compiled out.
@@ -403,6 +423,15 @@ __global__ void __launch_bounds__(kThreads, MAXSRC == 1 ? 8 : MAXSRC == 2 ? 6 : 
       run_piece<P, true, MAXSRC>(a.seg[i], base, len, a.scale);
     }
   }
+  // Scratch whose last reader has run: once every thread's reads are done, its lines are
+  // dead, and dropping them spares the write-back of bytes nothing will read.
+  unsigned any = 0;
+  for (int i = f; i < l; ++i) any |= a.drop[i];
+  if (any) {
+    __syncthreads();
+    for (int i = f; i < l; ++i)
+      if (a.drop[i]) drop_lines<P>(a.seg[i], a.drop[i], base, len);
+  }
 }
 
 template <class P, int CAP>
@@ -417,6 +446,7 @@ cudaError_t launch_chain_cap(const ChainPlan& c, float scale, int64_t tile, cuda
       a.seg[i] = c.segs[i];
       a.seg[i].tile0 = (int32_t)tasks;
       a.level[i] = c.level[i];
+      a.drop[i] = c.drop[i];
     }
     tasks += (c.gn[g] + tile - 1) / tile;
   }

@@ -80,6 +80,11 @@ __device__ __forceinline__ void st_u32(void* p, uint32_t v) {
 __device__ __forceinline__ void st_u16(void* p, uint16_t v) {
   asm volatile("st.global.u16 [%0], %1;" ::"l"(p), "h"(v) : "memory");
 }
+// Invalidate the 128-byte L2 line at p (128-byte aligned, device memory) without writing
+// it back: for dead data only, whose bytes are unspecified afterwards.
+__device__ __forceinline__ void discard_l2(const void* p) {
+  asm volatile("discard.global.L2 [%0], 128;" ::"l"(__cvta_generic_to_global(p)) : "memory");
+}
 
 // ------------------------------------------------------------- payload traits --
 // bf16 is the upper half of a binary32, so widening is a shift; narrowing rounds to

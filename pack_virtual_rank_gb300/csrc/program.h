@@ -163,11 +163,21 @@ constexpr int kChainMaxPieces = 384;
 struct ChainPlan {
   std::vector<Seg> segs;        // every group's pieces contiguous, in pass order
   std::vector<uint8_t> level;   // pass of each piece
+  // Per piece, bit k: source k is scratch that an earlier pass of the group wrote and that
+  // nothing touches after this read. Its CTA drops those bytes' whole 128-byte lines from
+  // L2 without a write-back once the tile's last pass is done.
+  std::vector<uint8_t> drop;
   std::vector<int32_t> gfirst;  // first piece of each group, then one past the last
   std::vector<int64_t> gn;      // elements of each piece of the group
 };
-bool build_chain(const std::vector<Pass>& passes, int E, ChainPlan* out, std::string* why);
-bool check_chain(const ChainPlan& c, int E, std::string* why);
+struct ByteRange {
+  uintptr_t lo, hi;  // [lo, hi)
+};
+// scratch: the call's scratch buffers whose dead lines may be dropped (device memory).
+bool build_chain(const std::vector<Pass>& passes, int E, const std::vector<ByteRange>& scratch,
+                 ChainPlan* out, std::string* why);
+bool check_chain(const ChainPlan& c, int E, const std::vector<ByteRange>& scratch,
+                 std::string* why);
 // Launches the chained kernel; false (nothing launched) when the program does not fit one
 // launch's parameters.
 bool launch_chain(int dtype, const ChainPlan& c, float scale, cudaStream_t stream,

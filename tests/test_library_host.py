@@ -533,12 +533,21 @@ def _dry_call(coll, count, dt, A, R, sched, in_place, skew, flags=0):
     return st, rv.last_launch()
 
 
+def _dropped(how):
+    """D of a "chained: G groups, P pieces, D dropped" launch description."""
+    m = re.fullmatch(r"chained: (\d+) groups, (\d+) pieces, (\d+) dropped", how)
+    assert m, how
+    return int(m.group(3))
+
+
 @pytest.mark.parametrize("coll", range(4))
 def test_chained_programs_are_race_free(coll):
     """Every small call, on every schedule, in-place form and buffer skew: the chained
     launch's analysis takes the program (mixed-width fp32 partials included), and its independent
-    re-check finds no two CTAs touching the same bytes with one writing, and no race
-    inside one pass of a group."""
+    re-check finds no two CTAs touching the same bytes with one writing, no race inside
+    one pass of a group, and no dropped scratch line that anything reads after the drop.
+    Relay programs drop their helpers' consumed scratch; RELAY_FLAG_KEEP_SCRATCH drops
+    nothing."""
     n = 0
     for A in (2, 4):
         for R in (A + 1, 8):
@@ -562,5 +571,11 @@ def test_chained_programs_are_race_free(coll):
                                     assert how == "dry run"
                                 else:
                                     assert how.startswith("chained"), (coll, A, R, count, sched)
+                                    # helpers' scratch is always consumed by a later pass
+                                    if p.helper_elems > 0 and count >= 1000:
+                                        assert _dropped(how) > 0, how
+                                    st, kept = _dry_call(coll, count, dt, A, R, sched, in_place,
+                                                         skew, rv.FLAG_KEEP_SCRATCH)
+                                    assert st == rv.OK and _dropped(kept) == 0, kept
                                 n += 1
     assert n > 500

@@ -295,11 +295,11 @@ def test_default_launch_forms():
     pass by pass; RELAY_FLAG_FUSED_PASSES runs the cooperative launch; large calls run
     chained too, the coalesced all-to-all's three-pass chains of copies included."""
     c = hz.run(rv.ALLREDUCE, 2, 8, 65536, rv.F32, 0.5, config=1, schedule=rv.SCHEDULE_RELAY)
-    assert c.launch == "chained: 10 groups, 26 pieces"
+    assert c.launch == "chained: 10 groups, 26 pieces, 16 dropped"
     hz.check_all(c)
     c = hz.run(rv.ALLREDUCE, 2, 8, 65536, rv.F32, 0.5, config=1, schedule=rv.SCHEDULE_RELAY,
                in_place=True)
-    assert c.launch == "chained: 8 groups, 26 pieces"
+    assert c.launch == "chained: 8 groups, 26 pieces, 16 dropped"
     hz.check_all(c)
     c = hz.run(rv.ALLREDUCE, 2, 8, 65536, rv.F32, 0.5, schedule=rv.SCHEDULE_RELAY,
                flags=rv.FLAG_SEPARATE_PASSES)
