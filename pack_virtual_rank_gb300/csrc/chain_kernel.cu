@@ -65,58 +65,74 @@ __device__ __forceinline__ void piece_scalar(const Seg& s, int64_t b, int64_t e,
   }
 }
 
-// Vector vi of every destination, byte offset `off` into each: kept in L2 when a later
-// pass of this CTA reads it, else streamed.
-__device__ __forceinline__ void store_dsts(const Seg& s, int64_t off, int vi, uint4 r, bool keep) {
+// A batch's results r[u] (vector vi0 + u * kThreads of the piece from byte offset `off`)
+// to every destination: kept in L2 when a later pass of this CTA reads them, else
+// streamed. Each destination pointer is read once per batch: the stores' memory clobbers
+// would otherwise make the compiler reload it from parameter space for every vector.
+// CHECK: vectors at or past nvec are skipped.
+template <int UB, bool CHECK>
+__device__ __forceinline__ void store_batch(const Seg& s, int ndst, int64_t off, int vi0, int nvec,
+                                            const uint4 (&r)[UB], bool keep) {
 #pragma unroll
   for (int d = 0; d < kMaxDst; ++d) {
-    if (d >= s.ndst) break;
-    uint4* q = reinterpret_cast<uint4*>(static_cast<char*>(s.dst[d]) + off) + vi;
-    if (keep) st_v4_keep(q, r);
-    else st_v4(q, r);
+    if (d >= ndst) break;
+    uint4* q = reinterpret_cast<uint4*>(static_cast<char*>(s.dst[d]) + off);
+#pragma unroll
+    for (int u = 0; u < UB; ++u) {
+      const int vi = vi0 + u * kThreads;
+      if (CHECK && vi >= nvec) break;
+      if (keep) st_v4_keep(q + vi, r[u]);
+      else st_v4(q + vi, r[u]);
+    }
   }
+}
+
+// r = the sum of v[0..NSRC) lane by lane, scaled if asked, rounded to the payload type.
+template <class P, int NSRC>
+__device__ __forceinline__ uint4 reduce_vec(const uint4 (&v)[NSRC], bool do_scale, float scale) {
+  constexpr int L = P::kLanes;
+  using Acc = typename P::Acc;
+  Acc acc[L], w[L];
+  P::unpack(v[0], acc);
+#pragma unroll
+  for (int k = 1; k < NSRC; ++k) {
+    P::unpack(v[k], w);
+#pragma unroll
+    for (int i = 0; i < L; ++i) acc[i] = P::add(acc[i], w[i]);
+  }
+  if (do_scale) {
+#pragma unroll
+    for (int i = 0; i < L; ++i) acc[i] = P::scale(acc[i], scale);
+  }
+  return P::pack(acc);
 }
 
 // A whole 16 KiB tile from element b on, every pointer 16-byte aligned there: each thread
 // takes kUnroll vectors (batches of 2 past two sources), no bounds to check.
 template <class P, int NSRC, bool COH, bool COPY = false>
 __device__ __forceinline__ void piece_full(const Seg& s, int64_t b, float scale) {
-  constexpr int L = P::kLanes;
   constexpr int UB = NSRC <= 2 ? kUnroll : kUnroll / 2;
-  using Acc = typename P::Acc;
+  const bool reduce = !COPY && s.op != kOpCopy;
   const bool do_scale = (s.flags & kFlagScale) != 0;
   const bool keep = (s.flags & kFlagKeep) != 0;
+  const int ndst = s.ndst;
   const int64_t off = b * P::kE;
   const int t = (int)threadIdx.x;
+  const uint4* src[NSRC];
+#pragma unroll
+  for (int k = 0; k < NSRC; ++k)
+    src[k] = reinterpret_cast<const uint4*>(static_cast<const char*>(s.src[k]) + off) + t;
 #pragma unroll
   for (int u0 = 0; u0 < kUnroll; u0 += UB) {
-    uint4 v[NSRC][UB];
+    uint4 v[UB][NSRC];
 #pragma unroll
     for (int u = 0; u < UB; ++u)
 #pragma unroll
-      for (int k = 0; k < NSRC; ++k)
-        v[k][u] = Mem<COH>::v4(reinterpret_cast<const uint4*>(static_cast<const char*>(s.src[k]) + off) +
-                               t + (u0 + u) * kThreads);
+      for (int k = 0; k < NSRC; ++k) v[u][k] = Mem<COH>::v4(src[k] + (u0 + u) * kThreads);
+    uint4 r[UB];
 #pragma unroll
-    for (int u = 0; u < UB; ++u) {
-      uint4 r = v[0][u];
-      if (!COPY && s.op != kOpCopy) {
-        Acc acc[L], w[L];
-        P::unpack(v[0][u], acc);
-#pragma unroll
-        for (int k = 1; k < NSRC; ++k) {
-          P::unpack(v[k][u], w);
-#pragma unroll
-          for (int i = 0; i < L; ++i) acc[i] = P::add(acc[i], w[i]);
-        }
-        if (do_scale) {
-#pragma unroll
-          for (int i = 0; i < L; ++i) acc[i] = P::scale(acc[i], scale);
-        }
-        r = P::pack(acc);
-      }
-      store_dsts(s, off, t + (u0 + u) * kThreads, r, keep);
-    }
+    for (int u = 0; u < UB; ++u) r[u] = reduce ? reduce_vec<P, NSRC>(v[u], do_scale, scale) : v[u][0];
+    store_batch<UB, false>(s, ndst, off, t + u0 * kThreads, 0, r, keep);
   }
 }
 
@@ -124,47 +140,29 @@ __device__ __forceinline__ void piece_full(const Seg& s, int64_t b, float scale)
 // batch are issued together (4 vectors per thread per source, 2 past two sources).
 template <class P, int NSRC, bool COH, bool COPY = false>
 __device__ __forceinline__ void piece_vec(const Seg& s, int64_t b, int nvec, float scale) {
-  constexpr int L = P::kLanes;
   constexpr int UB = NSRC <= 2 ? kUnroll : kUnroll / 2;
-  using Acc = typename P::Acc;
+  const bool reduce = !COPY && s.op != kOpCopy;
   const bool do_scale = (s.flags & kFlagScale) != 0;
   const bool keep = (s.flags & kFlagKeep) != 0;
+  const int ndst = s.ndst;
   const uint4* src[NSRC];
 #pragma unroll
   for (int k = 0; k < NSRC; ++k)
     src[k] = reinterpret_cast<const uint4*>(static_cast<const char*>(s.src[k]) + b * P::kE);
 #pragma unroll 1
   for (int v0 = (int)threadIdx.x; v0 < nvec; v0 += kThreads * UB) {
-    uint4 v[NSRC][UB];
+    uint4 v[UB][NSRC];
 #pragma unroll
     for (int u = 0; u < UB; ++u) {
       const int vi = v0 + u * kThreads;
 #pragma unroll
       for (int k = 0; k < NSRC; ++k)
-        v[k][u] = vi < nvec ? Mem<COH>::v4(src[k] + vi) : make_uint4(0u, 0u, 0u, 0u);
+        v[u][k] = vi < nvec ? Mem<COH>::v4(src[k] + vi) : make_uint4(0u, 0u, 0u, 0u);
     }
+    uint4 r[UB];
 #pragma unroll
-    for (int u = 0; u < UB; ++u) {
-      const int vi = v0 + u * kThreads;
-      if (vi >= nvec) continue;
-      uint4 r = v[0][u];
-      if (!COPY && s.op != kOpCopy) {
-        Acc acc[L], t[L];
-        P::unpack(v[0][u], acc);
-#pragma unroll
-        for (int k = 1; k < NSRC; ++k) {
-          P::unpack(v[k][u], t);
-#pragma unroll
-          for (int i = 0; i < L; ++i) acc[i] = P::add(acc[i], t[i]);
-        }
-        if (do_scale) {
-#pragma unroll
-          for (int i = 0; i < L; ++i) acc[i] = P::scale(acc[i], scale);
-        }
-        r = P::pack(acc);
-      }
-      store_dsts(s, b * P::kE, vi, r, keep);
-    }
+    for (int u = 0; u < UB; ++u) r[u] = reduce ? reduce_vec<P, NSRC>(v[u], do_scale, scale) : v[u][0];
+    store_batch<UB, true>(s, ndst, b * P::kE, v0, nvec, r, keep);
   }
 }
 
@@ -173,11 +171,11 @@ __device__ __forceinline__ void piece_vec(const Seg& s, int64_t b, int nvec, flo
 // blocks it straddles (both hold bytes of the piece's own source range).
 template <class P, int NSRC, bool COH, bool COPY = false>
 __device__ __forceinline__ void piece_realign(const Seg& s, int64_t b, int nvec, float scale) {
-  constexpr int L = P::kLanes;
   constexpr int UB = 2;
-  using Acc = typename P::Acc;
+  const bool reduce = !COPY && s.op != kOpCopy;
   const bool do_scale = (s.flags & kFlagScale) != 0;
   const bool keep = (s.flags & kFlagKeep) != 0;
+  const int ndst = s.ndst;
   unsigned sig[NSRC];
   const uint4* a[NSRC];
 #pragma unroll
@@ -188,42 +186,24 @@ __device__ __forceinline__ void piece_realign(const Seg& s, int64_t b, int nvec,
   }
 #pragma unroll 1
   for (int v0 = (int)threadIdx.x; v0 < nvec; v0 += kThreads * UB) {
-    uint4 v[NSRC][UB];
+    uint4 v[UB][NSRC];
 #pragma unroll
     for (int u = 0; u < UB; ++u) {
       const int vi = v0 + u * kThreads;
 #pragma unroll
       for (int k = 0; k < NSRC; ++k) {
         if (vi < nvec) {
-          v[k][u] = Mem<COH>::v4(a[k] + vi);
-          if (sig[k] != 0) v[k][u] = shift_pair(v[k][u], Mem<COH>::v4(a[k] + vi + 1), sig[k]);
+          v[u][k] = Mem<COH>::v4(a[k] + vi);
+          if (sig[k] != 0) v[u][k] = shift_pair(v[u][k], Mem<COH>::v4(a[k] + vi + 1), sig[k]);
         } else {
-          v[k][u] = make_uint4(0u, 0u, 0u, 0u);
+          v[u][k] = make_uint4(0u, 0u, 0u, 0u);
         }
       }
     }
+    uint4 r[UB];
 #pragma unroll
-    for (int u = 0; u < UB; ++u) {
-      const int vi = v0 + u * kThreads;
-      if (vi >= nvec) continue;
-      uint4 r = v[0][u];
-      if (!COPY && s.op != kOpCopy) {
-        Acc acc[L], t[L];
-        P::unpack(v[0][u], acc);
-#pragma unroll
-        for (int k = 1; k < NSRC; ++k) {
-          P::unpack(v[k][u], t);
-#pragma unroll
-          for (int i = 0; i < L; ++i) acc[i] = P::add(acc[i], t[i]);
-        }
-        if (do_scale) {
-#pragma unroll
-          for (int i = 0; i < L; ++i) acc[i] = P::scale(acc[i], scale);
-        }
-        r = P::pack(acc);
-      }
-      store_dsts(s, b * P::kE, vi, r, keep);
-    }
+    for (int u = 0; u < UB; ++u) r[u] = reduce ? reduce_vec<P, NSRC>(v[u], do_scale, scale) : v[u][0];
+    store_batch<UB, true>(s, ndst, b * P::kE, v0, nvec, r, keep);
   }
 }
 
