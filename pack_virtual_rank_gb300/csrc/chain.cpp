@@ -98,6 +98,18 @@ bool inside_any(const ByteRange& r, const std::vector<ByteRange>& v) {
 // Sources a segment's kernel reads: a copy reads source 0 only.
 int sources_read(const Seg& s) { return s.op == kOpCopy ? 1 : s.nsrc; }
 
+// A piece whose operands all sit on 16-byte boundaries and share one width: the kernel
+// runs it with thread t on vectors t, t + 256, ... and the scalar tail element t, t + 256,
+// ... of every tile, whichever path it takes.
+bool thread_local_piece(const Seg& s) {
+  if (seg_mixed(s)) return false;
+  for (int k = 0; k < sources_read(s); ++k)
+    if (reinterpret_cast<uintptr_t>(s.src[k]) % 16) return false;
+  for (int d = 0; d < s.ndst; ++d)
+    if (reinterpret_cast<uintptr_t>(s.dst[d]) % 16) return false;
+  return true;
+}
+
 // Bit k of drop[i]: source k of piece i lies in scratch, an earlier pass of the piece's
 // group wrote exactly those bytes, and nothing of the group touches them after this read
 // (nothing of another group touches them at all: a writer and its readers share a group).
@@ -227,6 +239,12 @@ bool build_chain(const std::vector<Pass>& passes, int E, const std::vector<ByteR
   }
   out->gfirst.push_back((int32_t)out->segs.size());
   mark_drops(out, E, scratch);
+  out->local.assign(out->gn.size(), 0);
+  for (size_t g = 0; g < out->gn.size(); ++g) {
+    bool local = true;
+    for (int i = out->gfirst[g]; i < out->gfirst[g + 1]; ++i) local &= thread_local_piece(out->segs[i]);
+    out->local[g] = local ? 1 : 0;
+  }
   return true;
 }
 
@@ -236,10 +254,22 @@ bool build_chain(const std::vector<Pass>& passes, int E, const std::vector<ByteR
 bool check_chain(const ChainPlan& c, int E, const std::vector<ByteRange>& scratch,
                  std::string* why) {
   const int G = (int)c.gn.size();
-  if (c.drop.size() != c.segs.size()) {
-    *why = "chained program without a drop mask per piece";
+  if (c.drop.size() != c.segs.size() || c.local.size() != c.gn.size()) {
+    *why = "chained program without a drop mask per piece or a flag per group";
     return false;
   }
+  for (int g = 0; g < G; ++g)
+    for (int i = c.gfirst[g]; c.local[g] && i < c.gfirst[g + 1]; ++i) {
+      const Seg& s = c.segs[i];
+      bool ok = !seg_mixed(s);
+      for (int k = 0; k < sources_read(s); ++k) ok &= reinterpret_cast<uintptr_t>(s.src[k]) % 16 == 0;
+      for (int d = 0; d < s.ndst; ++d) ok &= reinterpret_cast<uintptr_t>(s.dst[d]) % 16 == 0;
+      if (!ok) {
+        *why = "chained group " + std::to_string(g) + " runs without block barriers but piece " +
+               std::to_string(i) + " is mixed-width or off the 16-byte grid";
+        return false;
+      }
+    }
   std::vector<int> group(c.segs.size());
   for (int g = 0; g < G; ++g)
     for (int i = c.gfirst[g]; i < c.gfirst[g + 1]; ++i) {

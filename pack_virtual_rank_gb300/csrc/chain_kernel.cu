@@ -31,6 +31,7 @@ struct ChainArgs {
   int16_t gfirst[CAP + 1];    // first piece of each group, then one past the last
   uint8_t level[CAP];         // pass of each piece
   uint8_t drop[CAP];          // sources whose lines go dead after this piece (program.h)
+  uint8_t local[CAP];         // per group: dependencies stay inside each thread (program.h)
 };
 static_assert(sizeof(ChainArgs<kChainMaxPieces>) <= 32764, "kernel parameter space");
 
@@ -289,18 +290,20 @@ __device__ __noinline__ void piece_mixed(const Seg& s, int64_t base, int64_t len
 
 // The whole 128-byte lines of this tile's part of each source in `mask`: scratch that no
 // later pass reads, dropped from L2 so that it is never written back to memory. Partial
-// lines at the ends may hold a neighbour's live bytes and stay.
+// lines at the ends may hold a neighbour's live bytes and stay. A tile's part of one
+// source is at most 32 KiB (an fp32 partial beside a 16 KiB bf16 tile): one line per
+// thread; the loop only guards that bound.
 template <class P>
-__device__ __noinline__ void drop_lines(const Seg& s, unsigned mask, int64_t base, int64_t len) {
+__device__ __forceinline__ void drop_lines(const Seg& s, unsigned mask, int64_t base, int64_t len) {
 #pragma unroll 1
   for (int k = 0; k < kMaxSrc; ++k) {
     if (!((mask >> k) & 1u)) continue;
     const int64_t w = (k == 1 && (s.flags & kFlagSrc1F32)) ? 4 : P::kE;
     const uintptr_t lo = reinterpret_cast<uintptr_t>(s.src[k]) + (uintptr_t)(base * w);
     const uintptr_t hi = lo + (uintptr_t)(len * w);
-    const uintptr_t first = (lo + 127) & ~(uintptr_t)127, last = hi & ~(uintptr_t)127;
 #pragma unroll 1
-    for (uintptr_t q = first + (uintptr_t)threadIdx.x * 128; q < last; q += (uintptr_t)kThreads * 128)
+    for (uintptr_t q = ((lo + 127) & ~(uintptr_t)127) + (uintptr_t)threadIdx.x * 128; q + 128 <= hi;
+         q += (uintptr_t)kThreads * 128)
       discard_l2(reinterpret_cast<const void*>(q));
   }
 }
@@ -383,11 +386,14 @@ __global__ void __launch_bounds__(kThreads, MAXSRC == 1 ? 8 : MAXSRC == 2 ? 6 : 
   const int f = a.gfirst[lo], l = a.gfirst[lo + 1];
   const int64_t base = (int64_t)(t - a.seg[f].tile0) * a.tile;
   const int64_t len = min((int64_t)a.tile, a.seg[f].n - base);
+  // in a group whose dependencies stay inside each thread, program order alone puts a
+  // thread's loads of the next pass after its own stores of this one
+  const bool local = a.local[lo] != 0;
   int lvl = a.level[f];
   for (int i = f; i < l; ++i) {
     if (a.level[i] != lvl) {
       // the previous pass's stores of this tile are visible to the whole CTA after this
-      __syncthreads();
+      if (!local) __syncthreads();
       lvl = a.level[i];
     }
     // the first pass reads only memory written before the launch; later passes read what
@@ -431,6 +437,7 @@ cudaError_t launch_chain_cap(const ChainPlan& c, float scale, int64_t tile, cuda
     tasks += (c.gn[g] + tile - 1) / tile;
   }
   a.gfirst[G] = (int16_t)c.gfirst[G];
+  for (int g = 0; g < G; ++g) a.local[g] = c.local[g];
   a.ngroup = G;
   a.ntask = (int32_t)tasks;
   a.scale = scale;
