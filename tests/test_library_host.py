@@ -579,3 +579,46 @@ def test_chained_programs_are_race_free(coll):
                                     assert st == rv.OK and _dropped(kept) == 0, kept
                                 n += 1
     assert n > 500
+
+
+def test_repeated_calls_reuse_nothing_stale():
+    """A call repeated on the same arguments reuses its prepared program; every argument
+    that shapes the program keys it. The scale check still runs on a repeat, a call that
+    failed validation is never reused, and more distinct calls than the memo holds,
+    interleaved, each keep their own program."""
+    L = rv.lib()
+    R = 8
+
+    def call(A, count, dt, sched, scale, send_base=1, recv_base=10, overlap=False):
+        opts = rv.make_opts(schedule=sched, flags=rv.FLAG_DRY_RUN)
+        send = [((r + send_base) << 40) for r in range(A)]
+        recv = [((r + recv_base) << 40) for r in range(A)]
+        if overlap:
+            recv[1] = send[0] + 64
+        scratch = [((r + 20) << 40) for r in range(R)]
+        arr = lambda xs: (ctypes.c_void_p * R)(*(xs + [None] * (R - len(xs))))
+        st = L.relay_allreduce(arr(send), arr(recv), arr(scratch), count, dt, A, R, scale,
+                               ctypes.byref(opts), None)
+        return st, rv.last_launch()
+
+    # int32 takes scale 1 only, on the first call and on a repeat alike
+    assert call(2, 65536, rv.I32, rv.SCHEDULE_RELAY, 1.0)[0] == rv.OK
+    assert call(2, 65536, rv.I32, rv.SCHEDULE_RELAY, 0.5)[0] == rv.ERR_INVALID_ARGUMENT
+    assert call(2, 65536, rv.I32, rv.SCHEDULE_RELAY, 1.0)[0] == rv.OK
+    # overlapping buffers fail every time
+    for _ in range(3):
+        assert call(2, 65536, rv.F32, rv.SCHEDULE_RELAY, 0.5, overlap=True)[0] == rv.ERR_INVALID_ARGUMENT
+    # distinct calls, more than the memo holds, interleaved: each gives its own program
+    cases = [(A, count, sched) for A in (2, 4) for count in (65536, 4109, 1 << 20)
+             for sched in (rv.SCHEDULE_RELAY, rv.SCHEDULE_DIRECT)]
+    first = {}
+    for rep in range(3):
+        for i, (A, count, sched) in enumerate(cases):
+            st, how = call(A, count, rv.F32, sched, 1.0 / A, send_base=40 + 4 * i,
+                           recv_base=100 + 4 * i)
+            assert st == rv.OK, rv.lib().relay_last_error()
+            key = (A, count, sched)
+            if rep == 0:
+                first[key] = how
+            assert how == first[key], (key, how, first[key])
+    assert len(set(first.values())) > 2
