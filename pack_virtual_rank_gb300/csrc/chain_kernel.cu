@@ -21,17 +21,22 @@ namespace {
 // a 16-byte boundary, then 16-byte vectors (sources realigned from two aligned blocks when
 // only they are off the grid), then a scalar tail.
 
+// The small tables come first and the segment table last, so that every table the kernel
+// indexes by a run-time value starts within the block's first 2 KiB. With the drop table
+// at parameter offsets 31,890-32,274 of the 384-piece block, the kernel on GB300 did not
+// see its values (no line of those programs was ever dropped), although a probe kernel
+// read every byte of a 32,752-byte parameter correctly by index from offset 0.
 template <int CAP>
 struct ChainArgs {
   int32_t ngroup;
   int32_t ntask;
   float scale;
   int32_t tile;               // elements per task
-  Seg seg[CAP];               // tile0: first task of the piece's group
-  int16_t gfirst[CAP + 1];    // first piece of each group, then one past the last
   uint8_t level[CAP];         // pass of each piece
   uint8_t drop[CAP];          // sources whose lines go dead after this piece (program.h)
   uint8_t local[CAP];         // per group: dependencies stay inside each thread (program.h)
+  int16_t gfirst[CAP + 1];    // first piece of each group, then one past the last
+  Seg seg[CAP];               // tile0: first task of the piece's group
 };
 static_assert(sizeof(ChainArgs<kChainMaxPieces>) <= 32764, "kernel parameter space");
 

@@ -136,3 +136,53 @@ def test_dropped_lines_keep_every_live_byte(flush, case, skew_units):
     assert _dropped(k.launch) == 0, k.launch
     for a in range(A):
         assert np.array_equal(hz.host(k.recv[a]), got[a]), "kept and dropped scratch disagree"
+
+
+TIER_CASES = [
+    # one program per size of the chained kernel's parameter table (up to 32, 128 and 384
+    # pieces): coll, A, R, dtype, count, smallest and largest piece count of the tier
+    (rv.ALLREDUCE, 2, 8, rv.BF16, 1 << 20, 1, 32),
+    (rv.REDUCE_SCATTER, 4, 8, rv.BF16, 1 << 18, 33, 128),
+    (rv.ALL_GATHER, 4, 8, rv.BF16, 1 << 20, 33, 128),
+    (rv.ALL_TO_ALL, 4, 8, rv.BF16, 1 << 18, 129, 384),
+    (rv.ALL_TO_ALL, 4, 8, rv.BF16, (1 << 18) + 1, 129, 384),
+]
+
+
+@pytest.mark.parametrize("case", TIER_CASES,
+                         ids=[f"{NAMES[t[0]]}-A{t[1]}-{t[4]}" for t in TIER_CASES])
+def test_dropped_lines_leave_l2_unwritten(flush, case):
+    """Dropped lines really leave L2 without a write-back, whatever the size of the
+    kernel's parameter table: the scratch (a few MiB, well inside L2) holds a stale value in
+    memory under a live one in L2 before the call; afterwards nearly every scratch byte
+    reads back stale (what memory held), and with RELAY_FLAG_KEEP_SCRATCH nearly none does
+    (only data bytes that happen to equal the stale byte)."""
+    coll, A, R, dtype, count, lo, hi = case
+    fractions = []
+    for flags in (0, rv.FLAG_KEEP_SCRATCH):
+        opts = rv.make_opts(schedule=rv.SCHEDULE_RELAY, flags=flags)
+        plan = rv.relay_plan(coll, count, dtype, A, R, opts)
+        xs = hz.make_inputs(11, A, plan.input_elems, dtype, "cuda")
+        ys = [torch.empty(plan.output_elems, dtype=xs[0].dtype, device="cuda") for _ in range(A)]
+        scratch = rv.alloc_scratch(plan, "cuda")
+        live = [s for s in scratch if s is not None]
+        for s in live:
+            s.view(torch.uint8).fill_(STALE)
+        flush.fill_(1)
+        for s in live:
+            s.view(torch.uint8).fill_(LIVE)
+        fn = rv.COLLECTIVES[coll]
+        pad = [None] * (R - A)
+        if coll in (rv.ALLREDUCE, rv.REDUCE_SCATTER):
+            fn(xs + pad, ys + pad, scratch, count, dtype, A, R, 1.0 / A, opts)
+        else:
+            fn(xs + pad, ys + pad, scratch, count, dtype, A, R, opts)
+        how = rv.last_launch()
+        torch.cuda.synchronize()
+        m = re.fullmatch(r"chained: (\d+) groups, (\d+) pieces, (\d+) dropped", how)
+        assert m and lo <= int(m.group(2)) <= hi, how
+        total = sum(s.numel() * s.element_size() for s in live)
+        stale = sum(int((s.view(torch.uint8) == STALE).sum().item()) for s in live)
+        fractions.append(stale / total)
+    assert fractions[0] >= 0.9, fractions
+    assert fractions[1] <= 0.02, fractions
