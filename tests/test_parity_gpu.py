@@ -9,6 +9,8 @@ out-of-place, and no launch may hold two segments that race (checked on the host
 
 Page: "Link-balance the sharded relay schedules (up to 3.2x vs NCCL)".
 """
+import re
+
 import numpy as np
 import pytest
 import torch
@@ -287,6 +289,21 @@ def test_one_launch_at_sizes_past_its_default(coll, form):
                     want = "chained" if form == rv.FLAG_CHAINED else "cooperative"
                     assert c.launch.startswith(want), c.launch
                     hz.check_all(c)
+
+
+@pytest.mark.parametrize("coll,R,dtype,count", [
+    (rv.REDUCE_SCATTER, 21, rv.BF16, 16391),   # 372 pieces, fp32 partials
+    (rv.REDUCE_SCATTER, 21, rv.F32, 65613),    # 372 pieces
+    (rv.ALL_TO_ALL, 13, rv.BF16, 16391),       # 352 pieces
+])
+def test_largest_chained_programs(coll, R, dtype, count):
+    """Programs near the chained launch's 384-piece limit (the last entries of the largest
+    parameter table) match the oracle element by element under the default launch."""
+    scale = 0.25 if coll == rv.REDUCE_SCATTER else 1.0
+    c = hz.run(coll, 4, R, count, dtype, scale, config=23, schedule=rv.SCHEDULE_RELAY)
+    m = re.fullmatch(r"chained: (\d+) groups, (\d+) pieces, (\d+) dropped", c.launch)
+    assert m and int(m.group(2)) >= 350, c.launch
+    hz.check_all(c)
 
 
 def test_default_launch_forms():

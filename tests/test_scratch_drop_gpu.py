@@ -146,11 +146,12 @@ TIER_CASES = [
     (rv.ALL_GATHER, 4, 8, rv.BF16, 1 << 20, 33, 128),
     (rv.ALL_TO_ALL, 4, 8, rv.BF16, 1 << 18, 129, 384),
     (rv.ALL_TO_ALL, 4, 8, rv.BF16, (1 << 18) + 1, 129, 384),
+    (rv.REDUCE_SCATTER, 4, 21, rv.BF16, 16391, 129, 384),   # 372 pieces: the table's top
 ]
 
 
 @pytest.mark.parametrize("case", TIER_CASES,
-                         ids=[f"{NAMES[t[0]]}-A{t[1]}-{t[4]}" for t in TIER_CASES])
+                         ids=[f"{NAMES[t[0]]}-A{t[1]}-R{t[2]}-{t[4]}" for t in TIER_CASES])
 def test_dropped_lines_leave_l2_unwritten(flush, case):
     """Dropped lines really leave L2 without a write-back, whatever the size of the
     kernel's parameter table: the scratch (a few MiB, well inside L2) holds a stale value in
