@@ -313,6 +313,26 @@ __device__ __forceinline__ void drop_lines(const Seg& s, unsigned mask, int64_t 
   }
 }
 
+// A whole 16 KiB tile of segment s from element base on, every pointer 16-byte aligned
+// there (the caller knows: its group is flagged aligned). Programs of a 4-byte payload with
+// reductions take it instead of the general executor: apart from it, the common case gets
+// a register allocation of its own, which measured up to 7% faster there. bf16 full tiles
+// (6% slower this way) and copy-only programs (up to 1.5% slower) stay on the general
+// executor's own fast path.
+template <class P, bool COH, int MAXSRC>
+__device__ __noinline__ void run_full(const Seg& s, int64_t base, float scale) {
+  constexpr bool COPY = MAXSRC == 1;
+  const int nsrc = COPY || s.op == kOpCopy ? 1 : s.nsrc;
+  if (COPY || nsrc == 1) piece_full<P, 1, COH, COPY>(s, base, scale);
+  else if constexpr (MAXSRC >= 2) {
+    if (nsrc == 2) piece_full<P, 2, COH>(s, base, scale);
+    else if constexpr (MAXSRC > 2) {
+      if (nsrc == 3) piece_full<P, 3, COH>(s, base, scale);
+      else piece_full<P, 4, COH>(s, base, scale);
+    }
+  }
+}
+
 // Elements [base, base + len) of segment s, whatever the alignment of its pointers there.
 // MAXSRC: the most sources a reduction of the launch has (1: copies only); the paths for
 // more are compiled out.
@@ -394,6 +414,8 @@ __global__ void __launch_bounds__(kThreads, MAXSRC == 1 ? 8 : MAXSRC == 2 ? 6 : 
   // in a group whose dependencies stay inside each thread, program order alone puts a
   // thread's loads of the next pass after its own stores of this one
   const bool local = a.local[lo] != 0;
+  // every piece of an aligned group is 16-byte aligned at every tile base
+  const bool full = local && len * P::kE == kTileBytes;
   int lvl = a.level[f];
   for (int i = f; i < l; ++i) {
     if (a.level[i] != lvl) {
@@ -408,6 +430,9 @@ __global__ void __launch_bounds__(kThreads, MAXSRC == 1 ? 8 : MAXSRC == 2 ? 6 : 
     if (MAXSRC > 2 && P::kE == 2 && seg_mixed(a.seg[i])) {
       if (first) piece_mixed<false>(a.seg[i], base, len, a.scale);
       else piece_mixed<true>(a.seg[i], base, len, a.scale);
+    } else if (P::kE == 4 && MAXSRC >= 2 && full) {
+      if (first) run_full<P, false, MAXSRC>(a.seg[i], base, a.scale);
+      else run_full<P, true, MAXSRC>(a.seg[i], base, a.scale);
     } else if (first) {
       run_piece<P, false, MAXSRC>(a.seg[i], base, len, a.scale);
     } else {
