@@ -813,7 +813,7 @@ def run_per_workload(rv, synth, dev, steps, warmup, peak, clk, min_window_s=0.3)
         torch.cuda.synchronize()
         per_call, per_pass, n_calls = [], [[] for _ in passes], 0
         t0 = time.time()
-        total_ms = 0.0
+        total_ms, round_ms = 0.0, []
         while True:
             if small:
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -836,6 +836,7 @@ def run_per_workload(rv, synth, dev, steps, warmup, peak, clk, min_window_s=0.3)
                 e1.record(stream)
                 torch.cuda.synchronize()
                 total_ms += e0.elapsed_time(e1)
+                round_ms.append(e0.elapsed_time(e1) / steps)
                 for k in range(steps):
                     for i in range(len(passes)):
                         per_pass[i].append(ev[k][i].elapsed_time(ev[k][i + 1]))
@@ -843,7 +844,9 @@ def run_per_workload(rv, synth, dev, steps, warmup, peak, clk, min_window_s=0.3)
             if time.time() - t0 >= min_window_s:
                 break
         t1 = time.time()
-        ms = statistics.median(per_call) if small else total_ms / n_calls
+        # large calls: the median over rounds of each round's time per call, so that a host
+        # stall in one round (the GPU idles between calls) does not move the figure
+        ms = statistics.median(per_call) if small else statistics.median(round_ms)
         gbs = nbytes / ms / 1e6
         row = {"workload": label, "collective": name, "A": Ap, "R": R, "dtype": dt, "count": count,
                "schedule": ["relay", "zero_chunk", "direct", "legacy"][plan.kind],
@@ -851,8 +854,12 @@ def run_per_workload(rv, synth, dev, steps, warmup, peak, clk, min_window_s=0.3)
                "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
                "timing": ("median of single calls, each after an L2 flush, default launch "
                           "policy" if small else
-                          "back-to-back calls, pass events, inputs larger than L2"),
+                          "back-to-back calls, pass events, inputs larger than L2; median over "
+                          "rounds of each round's time per call"),
                "clocks": clk.window(t0, t1) if clk is not None else None}
+        if not small:
+            row["rounds"] = len(round_ms)
+            row["ms_mean_all_calls"] = round(total_ms / n_calls, 5)
         if small:
             # the same call captured in a CUDA graph: (a) one replay per timed window after
             # an L2 flush, timed around the replay (includes the graph launch); (b) 20 calls
