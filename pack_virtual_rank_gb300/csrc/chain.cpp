@@ -98,11 +98,11 @@ bool inside_any(const ByteRange& r, const std::vector<ByteRange>& v) {
 // Sources a segment's kernel reads: a copy reads source 0 only.
 int sources_read(const Seg& s) { return s.op == kOpCopy ? 1 : s.nsrc; }
 
-// A piece whose operands all sit on 16-byte boundaries and share one width: the kernel
-// runs it with thread t on vectors t, t + 256, ... and the scalar tail element t, t + 256,
-// ... of every tile, whichever path it takes.
+// A piece whose operands all sit on 16-byte boundaries: the kernel runs it with thread t on
+// 16-byte payload vectors t, t + 256, ... (elements 8v .. 8v + 7 of a bf16 piece, and the
+// same elements of an fp32 partial beside it) and the scalar tail elements t, t + 256, ...
+// of every tile, whichever path it takes.
 bool thread_local_piece(const Seg& s) {
-  if (seg_mixed(s)) return false;
   for (int k = 0; k < sources_read(s); ++k)
     if (reinterpret_cast<uintptr_t>(s.src[k]) % 16) return false;
   for (int d = 0; d < s.ndst; ++d)
@@ -261,12 +261,12 @@ bool check_chain(const ChainPlan& c, int E, const std::vector<ByteRange>& scratc
   for (int g = 0; g < G; ++g)
     for (int i = c.gfirst[g]; c.local[g] && i < c.gfirst[g + 1]; ++i) {
       const Seg& s = c.segs[i];
-      bool ok = !seg_mixed(s);
+      bool ok = true;
       for (int k = 0; k < sources_read(s); ++k) ok &= reinterpret_cast<uintptr_t>(s.src[k]) % 16 == 0;
       for (int d = 0; d < s.ndst; ++d) ok &= reinterpret_cast<uintptr_t>(s.dst[d]) % 16 == 0;
       if (!ok) {
         *why = "chained group " + std::to_string(g) + " runs without block barriers but piece " +
-               std::to_string(i) + " is mixed-width or off the 16-byte grid";
+               std::to_string(i) + " is off the 16-byte grid";
         return false;
       }
     }

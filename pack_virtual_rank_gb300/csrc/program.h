@@ -169,8 +169,8 @@ struct ChainPlan {
   std::vector<uint8_t> drop;
   std::vector<int32_t> gfirst;  // first piece of each group, then one past the last
   std::vector<int64_t> gn;      // elements of each piece of the group
-  // Per group, 1: no piece is mixed-width and every operand is 16-byte aligned at the
-  // group's first element. Every executor path then gives thread t the same elements of
+  // Per group, 1: every operand is 16-byte aligned at the group's first element. Every
+  // executor path (the mixed-width one included) then gives thread t the same elements of
   // every piece, so each dependency between passes stays inside one thread and needs no
   // block barrier.
   std::vector<uint8_t> local;
