@@ -2,8 +2,9 @@
 // pieces is chain.cpp).
 //
 // One ordinary launch for a whole call: CTA t runs tile t of one group of pieces in pass
-// order, with a block barrier between passes, so every dependency of the schedule stays
-// inside one CTA and no CTA ever waits for another.
+// order, with a block barrier between passes where a dependency crosses threads, so every
+// dependency of the schedule stays inside one CTA and no CTA ever waits for another; then it
+// drops the group's dead scratch lines from L2.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -14,12 +15,10 @@
 namespace relay {
 namespace {
 
-// One ordinary launch for a whole call: CTA t runs tile t of one group of pieces (chain.cpp)
-// in pass order, with a block barrier between passes, so every dependency of the schedule
-// stays inside one CTA and no CTA ever waits for another. A piece is any element range of
-// a segment; its alignment is sorted out here: a scalar head until the destinations sit on
-// a 16-byte boundary, then 16-byte vectors (sources realigned from two aligned blocks when
-// only they are off the grid), then a scalar tail.
+// A piece is any element range of a segment (chain.cpp); its alignment is sorted out here:
+// a scalar head until the destinations sit on a 16-byte boundary, then 16-byte vectors
+// (sources realigned from two aligned blocks when only they are off the grid), then a
+// scalar tail.
 
 // The small tables come first and the segment table last, so that every table the kernel
 // indexes by a run-time value starts within the block's first 2 KiB. With the drop table
@@ -412,9 +411,9 @@ __global__ void __launch_bounds__(kThreads, MAXSRC == 1 ? 8 : MAXSRC == 2 ? 6 : 
       else piece_mixed<true>(a.seg[i], base, len, a.scale);
     } else if (MAXSRC >= 2 && full) {
       // A whole aligned tile, inline in the kernel: apart from the general executor (which
-      // spills under these register limits) it gets a spill-free allocation, measured 3-8%
-      // faster on every reducing program but the bf16 2-active allreduce (4% faster than
-      // the executor's own fast path, equal to an out-of-line one).
+      // spills under these register limits) it gets a spill-free allocation, measured 3-9%
+      // faster than the executor's own fast path on every reducing program. Copy-only
+      // programs gained nothing from it and keep the executor.
       const Seg& sg = a.seg[i];
       const int ns = sg.op == kOpCopy ? 1 : sg.nsrc;
       if (first) {
@@ -452,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, MAXSRC == 1 ? 8 : MAXSRC == 2 ? 6 : 
 template <class P, int CAP>
 cudaError_t launch_chain_cap(const ChainPlan& c, float scale, int64_t tile, cudaStream_t stream,
                              int* ntask_out, int max_src) {
-  static thread_local ChainArgs<CAP> a;  // up to ~31 KiB: keep it off the stack
+  static thread_local ChainArgs<CAP> a;  // up to ~32 KiB: keep it off the stack
   const int G = (int)c.gn.size();
   int64_t tasks = 0;
   for (int g = 0; g < G; ++g) {
