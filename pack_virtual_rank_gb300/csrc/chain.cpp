@@ -72,6 +72,22 @@ void for_each_conflict(const std::vector<Operand>& ops, Fn fn) {
       if (ops[i].piece != ops[j].piece && (ops[i].write || ops[j].write)) fn(ops[i], ops[j]);
 }
 
+// Every pair of copies of one pass whose sources overlap element for element (same width,
+// offsets on the element grid): fn(a, b) with their source operands. Such copies can share
+// one load once their source ranges coincide.
+template <class Fn>
+void for_each_shared_read(const std::vector<Operand>& ops, const std::vector<Piece>& ps, Fn fn) {
+  for (size_t i = 0; i < ops.size(); ++i)
+    for (size_t j = i + 1; j < ops.size() && ops[j].lo < ops[i].hi; ++j) {
+      const Operand &a = ops[i], &b = ops[j];
+      if (a.write || b.write || a.piece == b.piece || a.width != b.width) continue;
+      const Piece &pa = ps[a.piece], &pb = ps[b.piece];
+      if (pa.pass != pb.pass || pa.s.op != kOpCopy || pb.s.op != kOpCopy) continue;
+      if ((b.lo - a.lo) % (uintptr_t)a.width) continue;  // sorted: b.lo >= a.lo
+      fn(a, b);
+    }
+}
+
 int find(std::vector<int>& parent, int x) {
   while (parent[x] != x) {
     parent[x] = parent[parent[x]];
@@ -150,8 +166,12 @@ Seg advance(const Seg& s, int64_t e, int64_t n, int E) {
 
 }  // namespace
 
-bool build_chain(const std::vector<Pass>& passes, int E, const std::vector<ByteRange>& scratch,
-                 ChainPlan* out, std::string* why) {
+namespace {
+
+// merge_reads: also cut copies of one pass at each other's source boundaries and merge the
+// ones that then read the same bytes (see build_chain).
+bool build_chain_with(const std::vector<Pass>& passes, int E, const std::vector<ByteRange>& scratch,
+                      bool merge_reads, ChainPlan* out, std::string* why) {
   auto fail = [&](const std::string& m) {
     if (why) *why = m;
     return false;
@@ -188,6 +208,16 @@ bool build_chain(const std::vector<Pass>& passes, int E, const std::vector<ByteR
       }
     });
     if (bad) return fail("overlap that is not elementwise");
+    if (merge_reads)
+      for_each_shared_read(ops, ps, [&](const Operand& a, const Operand& b) {
+        if (a.lo == b.lo && a.hi == b.hi) return;
+        const uintptr_t lo = std::max(a.lo, b.lo), hi = std::min(a.hi, b.hi);
+        for (const Operand* x : {&a, &b}) {
+          const uintptr_t w = (uintptr_t)x->width;
+          if (x->lo < lo) cuts[x->piece].push_back((int64_t)((lo - x->lo) / w));
+          if (x->hi > hi) cuts[x->piece].push_back((int64_t)((hi - x->lo) / w));
+        }
+      });
     bool any = false;
     std::vector<Piece> next;
     next.reserve(ps.size());
@@ -204,6 +234,36 @@ bool build_chain(const std::vector<Pass>& passes, int E, const std::vector<ByteR
     for (size_t i = 0; i < next.size(); ++i) next[i].order = (int)i;
     ps.swap(next);
     if (!any) break;
+  }
+
+  // 1b. Copies of one pass that read exactly the same bytes become one copy with all their
+  // destinations (at most kMaxDst): one load per element instead of one per copy. Every
+  // store of the schedule still happens. (An all-gather's self copy and its scatter of the
+  // same input to helpers and peers are such copies.)
+  if (merge_reads) {
+    std::vector<Piece> next;
+    next.reserve(ps.size());
+    std::vector<int> open;  // indices into next of copies that may still absorb another
+    for (const Piece& p : ps) {
+      bool merged = false;
+      if (p.s.op == kOpCopy)
+        for (int j : open) {
+          Seg& t = next[j].s;
+          if (next[j].pass != p.pass || t.src[0] != p.s.src[0] || t.n != p.s.n ||
+              t.flags != p.s.flags || t.ndst + p.s.ndst > kMaxDst)
+            continue;
+          for (int d = 0; d < p.s.ndst; ++d) t.dst[t.ndst + d] = p.s.dst[d];
+          t.ndst = (uint8_t)(t.ndst + p.s.ndst);
+          merged = true;
+          break;
+        }
+      if (merged) continue;
+      if (p.s.op == kOpCopy) open.push_back((int)next.size());
+      next.push_back(p);
+    }
+    for (size_t i = 0; i < next.size(); ++i) next[i].order = (int)i;
+    ps.swap(next);
+    operands(ps, E, &ops);
   }
 
   // 2. Join conflicting pieces into groups. A piece whose output a later pass reads keeps
@@ -246,6 +306,16 @@ bool build_chain(const std::vector<Pass>& passes, int E, const std::vector<ByteR
     out->local[g] = local ? 1 : 0;
   }
   return true;
+}
+
+}  // namespace
+
+// Copies of one pass that read the same bytes share their loads where the program still
+// fits one launch that way; otherwise the program is built without that merge.
+bool build_chain(const std::vector<Pass>& passes, int E, const std::vector<ByteRange>& scratch,
+                 ChainPlan* out, std::string* why) {
+  return build_chain_with(passes, E, scratch, true, out, why) ||
+         build_chain_with(passes, E, scratch, false, out, why);
 }
 
 // An independent re-check of a chained program (host hazard checks): no two pieces of
