@@ -177,14 +177,19 @@ bool build_chain_with(const std::vector<Pass>& passes, int E, const std::vector<
     return false;
   };
   if (passes.size() > 200) return fail("too many passes");
+  // A piece runs in its segment's one-launch phase: its own pass, or an earlier one where
+  // the program builder found that its data allow it (program.h, SegMeta::phase); the
+  // host's hazard checks verify those phases for the cooperative launch as well.
   std::vector<Piece> ps;
   for (size_t p = 0; p < passes.size(); ++p)
-    for (const Seg& s : passes[p].segs) {
+    for (size_t i = 0; i < passes[p].segs.size(); ++i) {
+      const Seg& s = passes[p].segs[i];
       if (s.n <= 0) continue;
       // only bf16 payloads widen, and every fp32 operand must be 4-byte aligned
       if (seg_mixed(s) && (E != 2 || !seg_operands_aligned(s, E)))
         return fail("mixed-width segment on a payload other than bf16, or misaligned");
-      ps.push_back(Piece{s, (int)p, (int)ps.size()});
+      const int ph = i < passes[p].meta.size() ? passes[p].meta[i].phase : -1;
+      ps.push_back(Piece{s, (ph >= 0 && (size_t)ph < p) ? ph : (int)p, (int)ps.size()});
     }
   if (ps.empty()) return fail("nothing to run");
 

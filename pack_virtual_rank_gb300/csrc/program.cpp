@@ -356,6 +356,10 @@ void build_a4_all_gather(Builder& B, const relay_plan_t& p) {
     B.begin(RELAY_PASS_G2);
     for (int h = 0; h < H; ++h)
       for (int k = 0; k < A; ++k) B.copy(1, A + h, B.Hh(h, k * oc), others(k, h * oc), oc);
+    // The second direct part reads only inputs and writes output blocks nothing else
+    // touches, so the one-launch forms may run it with group 1 (where it shares its loads
+    // with the actives' own copies of the same input).
+    B.phase(0);
     for (int a = 0; a < A; ++a)
       B.copy(1, a, B.X(a, P + p.direct_g1), others(a, P + p.direct_g1), p.direct_g2);
   }
