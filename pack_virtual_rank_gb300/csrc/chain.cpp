@@ -9,7 +9,8 @@
 // bytes (one of them writing) joined into a group, and each group tiled: one CTA runs tile
 // t of every piece of a group, in pass order, with a block barrier between passes. Nothing
 // one CTA reads or writes is touched by another CTA, so no CTA ever waits for another,
-// and the schedule's transfers and reductions still run exactly as the passes state them.
+// and the schedule's transfers and reductions all still run, each in its pass or in the
+// earlier one-launch phase its data allow (the cooperative launch's phases).
 //
 // Page: "Link-balance the sharded relay schedules (up to 3.2x vs NCCL)", items 3 and 5:
 // in the latency-bound regime a group boundary costs a round trip; here it costs a block
