@@ -31,6 +31,7 @@ struct ChainArgs {
   int32_t ntask;
   float scale;
   int32_t tile;               // elements per task
+  int32_t mult;               // CTA b runs task (b * mult) mod ntask (mult coprime to ntask)
   uint8_t level[CAP];         // pass of each piece
   uint8_t drop[CAP];          // sources whose lines go dead after this piece (program.h)
   uint8_t local[CAP];         // per group: dependencies stay inside each thread (program.h)
@@ -380,7 +381,8 @@ __device__ __noinline__ void run_piece(const Seg& s, int64_t base, int64_t len, 
 template <class P, int CAP, int MAXSRC>
 __global__ void __launch_bounds__(kThreads, MAXSRC == 1 ? 8 : MAXSRC == 2 ? 6 : 5)
     relay_chain_kernel(const __grid_constant__ ChainArgs<CAP> a) {
-  const int t = blockIdx.x;
+  // the task of this CTA (a permutation of the grid; see the launcher)
+  const int t = (int)(((int64_t)blockIdx.x * a.mult) % a.ntask);
   // the last group whose first task is <= t (uniform across the CTA)
   int lo = 0, hi = a.ngroup - 1;
   while (lo < hi) {
@@ -470,6 +472,29 @@ cudaError_t launch_chain_cap(const ChainPlan& c, float scale, int64_t tile, cuda
   a.ntask = (int32_t)tasks;
   a.scale = scale;
   a.tile = (int32_t)tile;
+  // Programs whose chains span three or more passes (the 4-active all-to-all and
+  // reduce-scatter) spread each wave of CTAs over every group: tasks about a resident CTA's
+  // share of the grid apart, the step coprime to the task count. The all-to-all's
+  // latency-bound chains then share each SM with its streaming copies (4.5-4.9% faster; the
+  // reduce-scatter 0.7%). Two-pass programs lost 1-6% that way, to DRAM locality, and keep
+  // their tasks in group order.
+  int levels = 0;
+  for (uint8_t l : c.level) levels = std::max(levels, (int)l + 1);
+  int64_t m = 1;
+  if (levels >= 3) {
+    const int64_t resident = (int64_t)sm_count() * (max_src == 1 ? 8 : max_src == 2 ? 6 : 5);
+    m = std::max<int64_t>(1, tasks / resident);
+    auto gcd = [](int64_t x, int64_t y) {
+      while (y) {
+        const int64_t r = x % y;
+        x = y;
+        y = r;
+      }
+      return x;
+    };
+    while (gcd(m, tasks) != 1) ++m;
+  }
+  a.mult = (int32_t)m;
   *ntask_out = (int)tasks;
   if (max_src == 1) relay_chain_kernel<P, CAP, 1><<<(unsigned)tasks, kThreads, 0, stream>>>(a);
   else if (max_src == 2) relay_chain_kernel<P, CAP, 2><<<(unsigned)tasks, kThreads, 0, stream>>>(a);
