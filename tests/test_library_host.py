@@ -622,3 +622,15 @@ def test_repeated_calls_reuse_nothing_stale():
                 first[key] = how
             assert how == first[key], (key, how, first[key])
     assert len(set(first.values())) > 2
+
+
+def test_chained_all_gather_shares_its_loads():
+    """The 4-active all-gather's chained program merges each active's own copy with the
+    copies that scatter the same input bytes to helpers and peers (one load, several
+    stores), the second direct part included (it runs in the first one-launch phase):
+    24 groups of 40 pieces at R=8, where separate copies would make 28 groups of 44. The
+    2-active all-gather's program (18 groups of 30 pieces) is pinned beside it."""
+    st, how = _dry_call(rv.ALL_GATHER, 1 << 20, rv.BF16, 4, 8, rv.SCHEDULE_RELAY, False, 0)
+    assert st == rv.OK and how.startswith("chained: 24 groups, 40 pieces"), how
+    st, how = _dry_call(rv.ALL_GATHER, 1 << 20, rv.BF16, 2, 8, rv.SCHEDULE_RELAY, False, 0)
+    assert st == rv.OK and how.startswith("chained: 18 groups, 30 pieces"), how
