@@ -375,11 +375,14 @@ __device__ __noinline__ void run_piece(const Seg& s, int64_t base, int64_t len, 
 }
 
 // MAXSRC: the most sources any reduction of the launch has, 4 for any program (fp32
-// partials included). Programs of copies only (all-gather, all-to-all) take MAXSRC = 1 and
-// run 8 CTAs per SM at 32 registers; those whose reductions have at most two sources (the
-// 2-active collectives) take MAXSRC = 2 and run 6; the rest run 5.
-template <class P, int CAP, int MAXSRC>
-__global__ void __launch_bounds__(kThreads, MAXSRC == 1 ? 8 : MAXSRC == 2 ? 6 : 5)
+// partials included). MINB: CTAs per SM the build is held to. Programs of copies only
+// (all-gather, all-to-all) take MAXSRC = 1 and run 8 CTAs per SM at 32 registers; those
+// whose reductions have at most two sources (the 2-active collectives) take MAXSRC = 2 and
+// run 6 at 40. Of the rest, programs with fp32 partials (the 4-active bf16 reduce-scatter,
+// whose mixed-width executor stays spill-free at 40 registers) run 6, 3-12% faster than at
+// 5; the others (the 4-active allreduce) run 5 at 48, 2.4% faster than at 6.
+template <class P, int CAP, int MAXSRC, int MINB>
+__global__ void __launch_bounds__(kThreads, MINB)
     relay_chain_kernel(const __grid_constant__ ChainArgs<CAP> a) {
   // the task of this CTA (a permutation of the grid; see the launcher)
   const int t = (int)(((int64_t)blockIdx.x * a.mult) % a.ntask);
@@ -452,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, MAXSRC == 1 ? 8 : MAXSRC == 2 ? 6 : 
 
 template <class P, int CAP>
 cudaError_t launch_chain_cap(const ChainPlan& c, float scale, int64_t tile, cudaStream_t stream,
-                             int* ntask_out, int max_src) {
+                             int* ntask_out, int max_src, bool mixed) {
   static thread_local ChainArgs<CAP> a;  // up to ~32 KiB: keep it off the stack
   const int G = (int)c.gn.size();
   int64_t tasks = 0;
@@ -482,7 +485,7 @@ cudaError_t launch_chain_cap(const ChainPlan& c, float scale, int64_t tile, cuda
   for (uint8_t l : c.level) levels = std::max(levels, (int)l + 1);
   int64_t m = 1;
   if (levels >= 3) {
-    const int64_t resident = (int64_t)sm_count() * (max_src == 1 ? 8 : max_src == 2 ? 6 : 5);
+    const int64_t resident = (int64_t)sm_count() * (max_src == 1 ? 8 : max_src == 2 || mixed ? 6 : 5);
     m = std::max<int64_t>(1, tasks / resident);
     auto gcd = [](int64_t x, int64_t y) {
       while (y) {
@@ -496,9 +499,10 @@ cudaError_t launch_chain_cap(const ChainPlan& c, float scale, int64_t tile, cuda
   }
   a.mult = (int32_t)m;
   *ntask_out = (int)tasks;
-  if (max_src == 1) relay_chain_kernel<P, CAP, 1><<<(unsigned)tasks, kThreads, 0, stream>>>(a);
-  else if (max_src == 2) relay_chain_kernel<P, CAP, 2><<<(unsigned)tasks, kThreads, 0, stream>>>(a);
-  else relay_chain_kernel<P, CAP, 4><<<(unsigned)tasks, kThreads, 0, stream>>>(a);
+  if (max_src == 1) relay_chain_kernel<P, CAP, 1, 8><<<(unsigned)tasks, kThreads, 0, stream>>>(a);
+  else if (max_src == 2) relay_chain_kernel<P, CAP, 2, 6><<<(unsigned)tasks, kThreads, 0, stream>>>(a);
+  else if (mixed) relay_chain_kernel<P, CAP, 4, 6><<<(unsigned)tasks, kThreads, 0, stream>>>(a);
+  else relay_chain_kernel<P, CAP, 4, 5><<<(unsigned)tasks, kThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
@@ -507,11 +511,14 @@ cudaError_t launch_chain_typed(const ChainPlan& c, float scale, int64_t tile, cu
                                int* ntask) {
   const size_t n = c.segs.size();
   int max_src = 1;
-  for (const Seg& sg : c.segs)
+  bool mixed = false;
+  for (const Seg& sg : c.segs) {
     if (sg.op != kOpCopy) max_src = std::max<int>(max_src, seg_mixed(sg) ? kMaxSrc : sg.nsrc);
-  if (n <= 32) return launch_chain_cap<P, 32>(c, scale, tile, stream, ntask, max_src);
-  if (n <= 128) return launch_chain_cap<P, 128>(c, scale, tile, stream, ntask, max_src);
-  return launch_chain_cap<P, kChainMaxPieces>(c, scale, tile, stream, ntask, max_src);
+    mixed |= seg_mixed(sg);
+  }
+  if (n <= 32) return launch_chain_cap<P, 32>(c, scale, tile, stream, ntask, max_src, mixed);
+  if (n <= 128) return launch_chain_cap<P, 128>(c, scale, tile, stream, ntask, max_src, mixed);
+  return launch_chain_cap<P, kChainMaxPieces>(c, scale, tile, stream, ntask, max_src, mixed);
 }
 
 }  // namespace
