@@ -40,34 +40,68 @@ struct ChainArgs {
 };
 static_assert(sizeof(ChainArgs<kChainMaxPieces>) <= 32764, "kernel parameter space");
 
-// Elements [b, e) of a piece one at a time (copies move raw bits).
-template <class P, bool COH, bool COPY = false>
+// Elements [b, e) of a piece one at a time (copies move raw bits), U elements per thread
+// per batch: each source's loads of a batch are issued together, then combined in source
+// order. The general executor of the 4-source build takes U = 4 (off-grid 4-active calls
+// 13-25% faster); the others keep U = 1, which their register limits fit better.
+template <class P, bool COH, bool COPY = false, int U = 1>
 __device__ __forceinline__ void piece_scalar(const Seg& s, int64_t b, int64_t e, float scale) {
   using Acc = typename P::Acc;
   const bool copy = COPY || s.op == kOpCopy;
   const bool do_scale = (s.flags & kFlagScale) != 0;
 #pragma unroll 1
-  for (int64_t i = b + threadIdx.x; i < e; i += kThreads) {
-    const int64_t off = i * P::kE;
+  for (int64_t i0 = b + threadIdx.x; i0 < e; i0 += (int64_t)kThreads * U) {
     if (copy) {
-      if (P::kE == 4) {
-        const uint32_t x = Mem<COH>::u32(static_cast<const char*>(s.src[0]) + off);
+      uint32_t x[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t i = i0 + (int64_t)u * kThreads;
+        const char* q = static_cast<const char*>(s.src[0]) + i * P::kE;
+        x[u] = i >= e ? 0u : P::kE == 4 ? Mem<COH>::u32(q) : (uint32_t)Mem<COH>::u16(q);
+      }
 #pragma unroll 1
-        for (int d = 0; d < s.ndst; ++d) st_u32(static_cast<char*>(s.dst[d]) + off, x);
-      } else {
-        const uint16_t x = Mem<COH>::u16(static_cast<const char*>(s.src[0]) + off);
-#pragma unroll 1
-        for (int d = 0; d < s.ndst; ++d) st_u16(static_cast<char*>(s.dst[d]) + off, x);
+      for (int d = 0; d < s.ndst; ++d) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int64_t i = i0 + (int64_t)u * kThreads;
+          if (i >= e) break;
+          char* q = static_cast<char*>(s.dst[d]) + i * P::kE;
+          if (P::kE == 4) st_u32(q, x[u]);
+          else st_u16(q, (uint16_t)x[u]);
+        }
       }
       continue;
     }
-    Acc acc = P::template load1<COH>(static_cast<const char*>(s.src[0]) + off);
+    Acc acc[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t i = i0 + (int64_t)u * kThreads;
+      acc[u] = i >= e ? Acc(0) : P::template load1<COH>(static_cast<const char*>(s.src[0]) + i * P::kE);
+    }
 #pragma unroll 1
-    for (int k = 1; k < s.nsrc; ++k)
-      acc = P::add(acc, P::template load1<COH>(static_cast<const char*>(s.src[k]) + off));
-    if (do_scale) acc = P::scale(acc, scale);
+    for (int k = 1; k < s.nsrc; ++k) {
+      Acc w[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t i = i0 + (int64_t)u * kThreads;
+        w[u] = i >= e ? Acc(0) : P::template load1<COH>(static_cast<const char*>(s.src[k]) + i * P::kE);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) acc[u] = P::add(acc[u], w[u]);
+    }
+    if (do_scale) {
+#pragma unroll
+      for (int u = 0; u < U; ++u) acc[u] = P::scale(acc[u], scale);
+    }
 #pragma unroll 1
-    for (int d = 0; d < s.ndst; ++d) P::store1(static_cast<char*>(s.dst[d]) + off, acc);
+    for (int d = 0; d < s.ndst; ++d) {
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t i = i0 + (int64_t)u * kThreads;
+        if (i >= e) break;
+        P::store1(static_cast<char*>(s.dst[d]) + i * P::kE, acc[u]);
+      }
+    }
   }
 }
 
@@ -216,8 +250,9 @@ __device__ __forceinline__ void piece_realign(const Seg& s, int64_t b, int nvec,
 // A mixed-width piece of a bf16 payload: the helper summing its bf16 slots into an fp32
 // partial (kFlagOutF32), or an owner adding its own bf16 value and the fp32 partial,
 // scaled once and rounded to bf16 (kFlagSrc1F32). 8 elements per step (one 16-byte bf16
-// vector, two fp32 vectors) when every operand is 16-byte aligned at `base`, else one
-// element at a time.
+// vector, two fp32 vectors) when the destinations and an fp32 source are 16-byte aligned at
+// `base` (a bf16 source off that grid is funnel-shifted out of the two aligned blocks it
+// straddles, both holding bytes of its own range), else one element at a time.
 template <bool COH>
 __device__ __noinline__ void piece_mixed(const Seg& s, int64_t base, int64_t len, float scale) {
   const bool out_f32 = (s.flags & kFlagOutF32) != 0;
@@ -228,9 +263,17 @@ __device__ __noinline__ void piece_mixed(const Seg& s, int64_t base, int64_t len
   const int dw = out_f32 ? 4 : 2;
   bool al = true;
   for (int k = 0; k < s.nsrc; ++k)
-    al &= ((reinterpret_cast<uintptr_t>(s.src[k]) + (uintptr_t)(base * sw(k))) & 15u) == 0;
+    if (sw(k) == 4) al &= ((reinterpret_cast<uintptr_t>(s.src[k]) + (uintptr_t)(base * 4)) & 15u) == 0;
   for (int d = 0; d < s.ndst; ++d)
     al &= ((reinterpret_cast<uintptr_t>(s.dst[d]) + (uintptr_t)(base * dw)) & 15u) == 0;
+  // the 8 bf16 elements of source k from element e on, whatever its alignment
+  auto bf16_vec = [&](int k, int64_t e) {
+    const char* p = static_cast<const char*>(s.src[k]) + e * 2;
+    const unsigned sig = (unsigned)(reinterpret_cast<uintptr_t>(p) & 15u);
+    const uint4* q = reinterpret_cast<const uint4*>(p - sig);
+    const uint4 lo = Mem<COH>::v4(q);
+    return sig ? shift_pair(lo, Mem<COH>::v4(q + 1), sig) : lo;
+  };
   int64_t done = 0;
   if (al) {
     const int nvec = (int)(len / 8);
@@ -238,7 +281,7 @@ __device__ __noinline__ void piece_mixed(const Seg& s, int64_t base, int64_t len
     for (int v = (int)threadIdx.x; v < nvec; v += kThreads) {
       const int64_t e = base + 8 * (int64_t)v;
       float acc[8], t[8];
-      TBF16::unpack(Mem<COH>::v4(static_cast<const char*>(s.src[0]) + e * 2), acc);
+      TBF16::unpack(bf16_vec(0, e), acc);
 #pragma unroll 1
       for (int k = 1; k < s.nsrc; ++k) {
         if (k == 1 && src1_f32) {
@@ -249,7 +292,7 @@ __device__ __noinline__ void piece_mixed(const Seg& s, int64_t base, int64_t len
           t[4] = __uint_as_float(hi.x); t[5] = __uint_as_float(hi.y);
           t[6] = __uint_as_float(hi.z); t[7] = __uint_as_float(hi.w);
         } else {
-          TBF16::unpack(Mem<COH>::v4(static_cast<const char*>(s.src[k]) + e * 2), t);
+          TBF16::unpack(bf16_vec(k, e), t);
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], t[i]);
@@ -276,19 +319,45 @@ __device__ __noinline__ void piece_mixed(const Seg& s, int64_t base, int64_t len
     }
     done = 8 * (int64_t)nvec;
   }
+  // The rest one element at a time, U elements per thread per batch: each source's loads
+  // of a batch are issued together, then added in source order as above.
+  constexpr int U = 4;
+  const int64_t end = base + len;
 #pragma unroll 1
-  for (int64_t i = base + done + threadIdx.x; i < base + len; i += kThreads) {
-    float acc = TBF16::template load1<COH>(static_cast<const char*>(s.src[0]) + i * 2);
+  for (int64_t i0 = base + done + threadIdx.x; i0 < end; i0 += (int64_t)kThreads * U) {
+    float acc[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t i = i0 + (int64_t)u * kThreads;
+      acc[u] = i < end ? TBF16::template load1<COH>(static_cast<const char*>(s.src[0]) + i * 2) : 0.f;
+    }
 #pragma unroll 1
-    for (int k = 1; k < s.nsrc; ++k)
-      acc = __fadd_rn(acc, (k == 1 && src1_f32)
-                               ? TF32::template load1<COH>(static_cast<const char*>(s.src[1]) + i * 4)
-                               : TBF16::template load1<COH>(static_cast<const char*>(s.src[k]) + i * 2));
-    if (do_scale) acc = __fmul_rn(acc, scale);
+    for (int k = 1; k < s.nsrc; ++k) {
+      float w[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t i = i0 + (int64_t)u * kThreads;
+        w[u] = i >= end ? 0.f
+               : (k == 1 && src1_f32)
+                   ? TF32::template load1<COH>(static_cast<const char*>(s.src[1]) + i * 4)
+                   : TBF16::template load1<COH>(static_cast<const char*>(s.src[k]) + i * 2);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) acc[u] = __fadd_rn(acc[u], w[u]);
+    }
+    if (do_scale) {
+#pragma unroll
+      for (int u = 0; u < U; ++u) acc[u] = __fmul_rn(acc[u], scale);
+    }
 #pragma unroll 1
     for (int d = 0; d < s.ndst; ++d) {
-      if (out_f32) TF32::store1(static_cast<char*>(s.dst[d]) + i * 4, acc);
-      else TBF16::store1(static_cast<char*>(s.dst[d]) + i * 2, acc);
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t i = i0 + (int64_t)u * kThreads;
+        if (i >= end) break;
+        if (out_f32) TF32::store1(static_cast<char*>(s.dst[d]) + i * 4, acc[u]);
+        else TBF16::store1(static_cast<char*>(s.dst[d]) + i * 2, acc[u]);
+      }
     }
   }
 }
@@ -320,6 +389,7 @@ template <class P, bool COH, int MAXSRC>
 __device__ __noinline__ void run_piece(const Seg& s, int64_t base, int64_t len, float scale) {
   constexpr int E = P::kE, L = P::kLanes;
   constexpr bool COPY = MAXSRC == 1;
+  constexpr int SU = MAXSRC > 2 ? 4 : 1;  // elements per thread per batch, one at a time
   auto mis = [&](const void* p) {
     return (unsigned)((reinterpret_cast<uintptr_t>(p) + (uintptr_t)(base * E)) & 15u);
   };
@@ -343,11 +413,11 @@ __device__ __noinline__ void run_piece(const Seg& s, int64_t base, int64_t len, 
     }
   }
   if (!dsame) {
-    piece_scalar<P, COH, COPY>(s, base, base + len, scale);
+    piece_scalar<P, COH, COPY, SU>(s, base, base + len, scale);
     return;
   }
   const int64_t head = min((int64_t)(((16u - md) & 15u) / E), len);
-  piece_scalar<P, COH, COPY>(s, base, base + head, scale);
+  piece_scalar<P, COH, COPY, SU>(s, base, base + head, scale);
   const int64_t b1 = base + head;
   const int nvec = (int)((len - head) / L);
   if (nvec > 0) {
@@ -368,10 +438,10 @@ __device__ __noinline__ void run_piece(const Seg& s, int64_t base, int64_t len, 
     } else if (nsrc == 2) {
       if constexpr (MAXSRC >= 2) piece_realign<P, 2, COH>(s, b1, nvec, scale);
     } else {
-      piece_scalar<P, COH>(s, b1, b1 + nvec * L, scale);
+      piece_scalar<P, COH, false, SU>(s, b1, b1 + nvec * L, scale);
     }
   }
-  piece_scalar<P, COH, COPY>(s, b1 + nvec * L, base + len, scale);
+  piece_scalar<P, COH, COPY, SU>(s, b1 + nvec * L, base + len, scale);
 }
 
 // MAXSRC: the most sources any reduction of the launch has, 4 for any program (fp32
