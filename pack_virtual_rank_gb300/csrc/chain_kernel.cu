@@ -211,7 +211,7 @@ __device__ __forceinline__ void piece_vec(const Seg& s, int64_t b, int nvec, flo
 // blocks it straddles (both hold bytes of the piece's own source range).
 template <class P, int NSRC, bool COH, bool COPY = false>
 __device__ __forceinline__ void piece_realign(const Seg& s, int64_t b, int nvec, float scale) {
-  constexpr int UB = 2;
+  constexpr int UB = NSRC <= 2 ? 2 : 1;
   const bool reduce = !COPY && s.op != kOpCopy;
   const bool do_scale = (s.flags & kFlagScale) != 0;
   const bool keep = (s.flags & kFlagKeep) != 0;
@@ -437,8 +437,9 @@ __device__ __noinline__ void run_piece(const Seg& s, int64_t base, int64_t len, 
       piece_realign<P, 1, COH, COPY>(s, b1, nvec, scale);
     } else if (nsrc == 2) {
       if constexpr (MAXSRC >= 2) piece_realign<P, 2, COH>(s, b1, nvec, scale);
-    } else {
-      piece_scalar<P, COH, false, SU>(s, b1, b1 + nvec * L, scale);
+    } else if constexpr (MAXSRC > 2) {
+      if (nsrc == 3) piece_realign<P, 3, COH>(s, b1, nvec, scale);
+      else piece_realign<P, 4, COH>(s, b1, nvec, scale);
     }
   }
   piece_scalar<P, COH, COPY, SU>(s, b1 + nvec * L, base + len, scale);
